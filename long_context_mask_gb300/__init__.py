@@ -1,0 +1,26 @@
+"""GB300-native block-sparse attention: Python binding of ``libbsa.so``.
+
+Every compute step runs in the CUDA library; this module only marshals
+arguments (device pointers of torch tensors, sizes, the current CUDA stream)
+into the C-ABI declared in ``include/bsa.h``.  There is no CPU fallback: if
+the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+from .binding import (  # noqa: F401
+    BLOCK,
+    BsaError,
+    IDX_MASK_U8,
+    IDX_THRESHOLD_F32,
+    IDX_TOPK_F32,
+    build_index,
+    dense_attention_flops,
+    device_status,
+    effective_flops,
+    forward,
+    lib_path,
+    load_library,
+    reorder_rows,
+    resident_ctas,
+    sample_blocks,
+)

@@ -1,0 +1,177 @@
+"""ctypes binding of libbsa.so (argument marshalling only).
+
+Names mirror the C-ABI in include/bsa.h.  Tensors are torch CUDA tensors; the
+binding passes their device pointers, their sizes and the current CUDA
+stream.  No arithmetic of the method happens here.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(HERE, "libbsa.so")
+
+BLOCK = 128
+IDX_MASK_U8, IDX_THRESHOLD_F32, IDX_TOPK_F32 = 0, 1, 2
+
+STATUS_NAMES = {0: "BSA_OK", 1: "BSA_ERR_INVALID_ARG", 2: "BSA_ERR_UNSUPPORTED",
+                3: "BSA_ERR_OVERFLOW", 4: "BSA_ERR_CUDA", 5: "BSA_ERR_TIMEOUT",
+                6: "BSA_ERR_BOUNDS"}
+
+EXPORTS = ("bsa_build_index", "bsa_reorder_rows", "bsa_sample_blocks", "bsa_forward",
+           "bsa_device_status", "bsa_resident_ctas", "bsa_status_string")
+
+
+class BsaError(RuntimeError):
+    def __init__(self, call: str, code: int):
+        super().__init__(f"{call} failed: {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libbsa.so (raises if it was not built: there is no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"libbsa.so not found at {_LIB_PATH}; run __graft_entry__.build()")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    lib.bsa_build_index.argtypes = [i32, P, i64, i32, f32, P, i32, P, P, i32, P]
+    lib.bsa_reorder_rows.argtypes = [P, P, i64, i32, i32, P, P]
+    lib.bsa_sample_blocks.argtypes = [P, i64, i32, P, P, i32, i32, P, P, P, P, i32, P]
+    lib.bsa_forward.argtypes = [P, P, P, i32, i32, i32, i32, P, P, i32, P, P, P, P, f32, P, P, P]
+    lib.bsa_device_status.argtypes = [P, ctypes.POINTER(i32)]
+    lib.bsa_resident_ctas.argtypes = [i32]
+    lib.bsa_status_string.argtypes = [i32]
+    lib.bsa_status_string.restype = ctypes.c_char_p
+    for name in ("bsa_build_index", "bsa_reorder_rows", "bsa_sample_blocks", "bsa_forward",
+                 "bsa_device_status", "bsa_resident_ctas"):
+        getattr(lib, name).restype = i32
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(call, code):
+    if code != 0:
+        raise BsaError(call, code)
+
+
+def _dtype(t, name, *dtypes):
+    if t is not None and t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+
+
+def build_index(mode: int, src, kv_idx, kv_cnt, *, p: float = 0.0, k_per_row=None,
+                k_const: int = 0, stream=None):
+    """Fill kv_idx [rows, max_kv] / kv_cnt [rows] from src [rows, nKB] (see bsa.h)."""
+    import torch
+    _dtype(src, "src", torch.uint8 if mode == IDX_MASK_U8 else torch.float32)
+    _dtype(kv_idx, "kv_idx", torch.int32)
+    _dtype(kv_cnt, "kv_cnt", torch.int32)
+    _dtype(k_per_row, "k_per_row", torch.int32)
+    rows, nkb = src.shape
+    code = load_library().bsa_build_index(mode, _ptr(src), rows, nkb, float(p), _ptr(k_per_row),
+                                          int(k_const), _ptr(kv_idx), _ptr(kv_cnt),
+                                          kv_idx.shape[1], _stream(stream))
+    _check("bsa_build_index", code)
+
+
+def reorder_rows(kv_cnt, wave: int, row_perm, *, order_in=None, stream=None):
+    """row_perm [heads, nQB] from kv_cnt [heads, nQB] (WaveAlign stage 2)."""
+    import torch
+    _dtype(kv_cnt, "kv_cnt", torch.int32)
+    _dtype(row_perm, "row_perm", torch.int32)
+    _dtype(order_in, "order_in", torch.int32)
+    heads, nqb = kv_cnt.shape
+    code = load_library().bsa_reorder_rows(_ptr(kv_cnt), _ptr(order_in), heads, nqb, int(wave),
+                                           _ptr(row_perm), _stream(stream))
+    _check("bsa_reorder_rows", code)
+
+
+def sample_blocks(scores, exact_idx, exact_cnt, m: int, u, kv_idx, kv_cnt, log_w, *, stream=None):
+    """Exact list + PPSWOR sample with log-weights (InstaGen section 3.2.1)."""
+    import torch
+    _dtype(scores, "scores", torch.float32)
+    _dtype(u, "u", torch.float64)
+    rows, nkb = scores.shape
+    code = load_library().bsa_sample_blocks(_ptr(scores), rows, nkb, _ptr(exact_idx),
+                                            _ptr(exact_cnt), exact_idx.shape[1], int(m), _ptr(u),
+                                            _ptr(kv_idx), _ptr(kv_cnt), _ptr(log_w),
+                                            kv_idx.shape[1], _stream(stream))
+    _check("bsa_sample_blocks", code)
+
+
+def forward(q, k, v, kv_idx, kv_cnt, o, lse, *, log_w=None, q_map=None, kv_map=None,
+            row_perm=None, scale: float = 0.0, stream=None):
+    """Block-sparse attention forward: fills o [B,H,N,D] bf16 and lse [B,H,N] fp32."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _dtype(t, n, torch.bfloat16)
+    _dtype(lse, "lse", torch.float32)
+    _dtype(log_w, "log_w", torch.float32)
+    B, H, N, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape or o.shape != q.shape:
+        raise ValueError("q, k, v, o must share the shape [B, H, N, D]")
+    code = load_library().bsa_forward(_ptr(q), _ptr(k), _ptr(v), B, H, N, D, _ptr(kv_idx),
+                                      _ptr(kv_cnt), kv_idx.shape[1], _ptr(log_w), _ptr(q_map),
+                                      _ptr(kv_map), _ptr(row_perm), float(scale), _ptr(o),
+                                      _ptr(lse), _stream(stream))
+    _check("bsa_forward", code)
+
+
+def device_status(stream=None) -> int:
+    """Read and clear the device status word (synchronises the stream)."""
+    out = ctypes.c_int32(0)
+    _check("bsa_device_status", load_library().bsa_device_status(_stream(stream), ctypes.byref(out)))
+    return out.value
+
+
+def resident_ctas(D: int) -> int:
+    n = load_library().bsa_resident_ctas(int(D))
+    if n <= 0:
+        raise BsaError("bsa_resident_ctas", 4)
+    return n
+
+
+def effective_flops(kv_cnt, D: int) -> float:
+    """FLOPs of the computed blocks: sum(cnt) * 4 * 128 * 128 * D (QK^T and PV)."""
+    total = int(kv_cnt.sum().item()) if hasattr(kv_cnt, "sum") else int(sum(kv_cnt))
+    return float(total) * 4.0 * BLOCK * BLOCK * D
+
+
+def dense_attention_flops(N: int, H: int, D: int, causal: bool = False, B: int = 1) -> float:
+    """4 N^2 D per head (two N x N x D products), halved for causal attention."""
+    f = 4.0 * N * N * D * H * B
+    return f / 2 if causal else f
+
+
+__all__ = ["BLOCK", "BsaError", "IDX_MASK_U8", "IDX_THRESHOLD_F32", "IDX_TOPK_F32", "build_index",
+           "reorder_rows", "sample_blocks", "forward", "device_status", "resident_ctas",
+           "effective_flops", "dense_attention_flops", "load_library", "lib_path", "EXPORTS",
+           "math"]

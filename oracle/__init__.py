@@ -1,0 +1,181 @@
+"""Block-sparse attention oracle (fp64 CPU reference).
+
+TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
+CPU-baseline leg are the only callers.  The product path (the CUDA library and
+its binding) never imports this package, and this package never imports the
+product path.  Every function wraps the plain C in ``bsa_oracle.c`` through
+ctypes and takes/returns numpy arrays.  The passages each function follows are
+listed at the top of ``bsa_oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "bsa_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+# -ffp-contract=off: the sampler's integer decisions come from fp64 sums that
+# must round exactly as written (no fused multiply-add), on x86 and on Arm.
+CFLAGS = ["-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off", "-std=c11"]
+
+
+def build(force: bool = False) -> str:
+    """Compile bsa_oracle.c into liboracle.so next to it (gcc, no GPU)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        i32, i64, f32, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_double
+        lib.oracle_index_mask_u8.argtypes = [P, i64, i32, P, P, i32]
+        lib.oracle_index_mask_u8.restype = i64
+        lib.oracle_index_threshold.argtypes = [P, i64, i32, f32, P, P, i32]
+        lib.oracle_index_threshold.restype = i64
+        lib.oracle_index_topk.argtypes = [P, i64, i32, P, i32, P, P, i32]
+        lib.oracle_index_topk.restype = i64
+        lib.oracle_reorder_rows.argtypes = [P, P, i64, i32, i32, P]
+        lib.oracle_reorder_rows.restype = None
+        lib.oracle_sample_blocks.argtypes = [P, i64, i32, P, P, i32, i32, P, P, P, P, i32]
+        lib.oracle_sample_blocks.restype = i64
+        lib.oracle_attention.argtypes = [P, P, P, i32, i32, i32, i32, P, P, i32, P, P, P,
+                                         f64, P, i64, P, P, P]
+        lib.oracle_attention.restype = None
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = i32
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def index_mask(mask, max_kv=None):
+    """mask uint8 [rows, nKB] -> (kv_idx int32 [rows, max_kv], kv_cnt int32 [rows], n_overflow)."""
+    mask = _c(mask, np.uint8)
+    rows, nkb = mask.shape
+    max_kv = nkb if max_kv is None else int(max_kv)
+    idx = np.empty((rows, max_kv), np.int32)
+    cnt = np.empty(rows, np.int32)
+    ov = _load().oracle_index_mask_u8(_ptr(mask), rows, nkb, _ptr(idx), _ptr(cnt), max_kv)
+    return idx, cnt, int(ov)
+
+
+def index_threshold(T, p, max_kv=None):
+    """Threshold map fp32 [rows, nKB], keep T <= p (fp32) -> (kv_idx, kv_cnt, n_overflow)."""
+    T = _c(T, np.float32)
+    rows, nkb = T.shape
+    max_kv = nkb if max_kv is None else int(max_kv)
+    idx = np.empty((rows, max_kv), np.int32)
+    cnt = np.empty(rows, np.int32)
+    ov = _load().oracle_index_threshold(_ptr(T), rows, nkb, float(np.float32(p)), _ptr(idx),
+                                        _ptr(cnt), max_kv)
+    return idx, cnt, int(ov)
+
+
+def index_topk(scores, k, max_kv=None):
+    """Top-k per row (score desc, ties to the lower block), listed in ascending block order.
+
+    ``k`` is an int or an int32 array [rows]."""
+    scores = _c(scores, np.float32)
+    rows, nkb = scores.shape
+    if np.isscalar(k):
+        kpr, kc = None, int(k)
+        kmax = kc
+    else:
+        kpr, kc = _c(k, np.int32), 0
+        kmax = int(kpr.max()) if rows else 0
+    max_kv = min(nkb, kmax) if max_kv is None else int(max_kv)
+    max_kv = max(max_kv, 1)
+    idx = np.empty((rows, max_kv), np.int32)
+    cnt = np.empty(rows, np.int32)
+    ov = _load().oracle_index_topk(_ptr(scores), rows, nkb, _ptr(kpr), kc, _ptr(idx), _ptr(cnt),
+                                   max_kv)
+    return idx, cnt, int(ov)
+
+
+def reorder_rows(kv_cnt, wave, order_in=None):
+    """kv_cnt int32 [heads, nQB] -> row_perm int32 [heads, nQB] (WaveAlign stage 2)."""
+    kv_cnt = _c(kv_cnt, np.int32)
+    heads, nqb = kv_cnt.shape
+    order_in = _c(order_in, np.int32)
+    perm = np.empty((heads, nqb), np.int32)
+    _load().oracle_reorder_rows(_ptr(kv_cnt), _ptr(order_in), heads, nqb, int(wave), _ptr(perm))
+    return perm
+
+
+def sample_blocks(scores, exact_idx, exact_cnt, m, u, max_kv):
+    """Exact list + PPSWOR/systematic-PPS sample -> (kv_idx, kv_cnt, log_w, n_overflow)."""
+    scores = _c(scores, np.float32)
+    rows, nkb = scores.shape
+    exact_idx = _c(exact_idx, np.int32)
+    exact_cnt = _c(exact_cnt, np.int32)
+    u = _c(u, np.float64)
+    idx = np.empty((rows, max_kv), np.int32)
+    cnt = np.empty(rows, np.int32)
+    lw = np.empty((rows, max_kv), np.float32)
+    ov = _load().oracle_sample_blocks(_ptr(scores), rows, nkb, _ptr(exact_idx), _ptr(exact_cnt),
+                                      exact_idx.shape[1], int(m), _ptr(u), _ptr(idx), _ptr(cnt),
+                                      _ptr(lw), int(max_kv))
+    return idx, cnt, lw, int(ov)
+
+
+def attention(q, k, v, kv_idx, kv_cnt, log_w=None, q_map=None, kv_map=None, scale=0.0,
+              sel=None):
+    """Block-sparse attention from the definition, fp64.
+
+    q, k, v: uint16 bf16 bit patterns [B, H, N, D] (or torch bf16 tensors on CPU).
+    kv_idx [B*H*nQB, max_kv], kv_cnt [B*H*nQB]; log_w like kv_idx or None;
+    q_map / kv_map int32 [B*H, N] or None.  ``sel`` lists the flat query blocks
+    (bh * nQB + qb) to evaluate (all when None).
+    Returns (O fp64 [nsel*128, D], LSE fp64 [nsel*128], tok int32 [nsel*128]),
+    where row x belongs to original query token tok[x] of head sel[x // 128] // nQB.
+    """
+    q, k, v = (_as_u16(t) for t in (q, k, v))
+    B, H, N, D = q.shape
+    nqb = N // 128
+    kv_idx = _c(kv_idx, np.int32)
+    kv_cnt = _c(kv_cnt, np.int32)
+    max_kv = kv_idx.shape[1]
+    log_w = _c(log_w, np.float32)
+    q_map = _c(q_map, np.int32)
+    kv_map = _c(kv_map, np.int32)
+    sel = np.arange(B * H * nqb, dtype=np.int64) if sel is None else _c(sel, np.int64)
+    n = sel.shape[0]
+    O = np.empty((n * 128, D), np.float64)
+    L = np.empty(n * 128, np.float64)
+    tok = np.empty(n * 128, np.int32)
+    _load().oracle_attention(_ptr(q), _ptr(k), _ptr(v), B, H, N, D, _ptr(kv_idx), _ptr(kv_cnt),
+                             max_kv, _ptr(log_w), _ptr(q_map), _ptr(kv_map), float(scale),
+                             _ptr(sel), n, _ptr(O), _ptr(L), _ptr(tok))
+    return O, L, tok
+
+
+def _as_u16(t):
+    if hasattr(t, "view") and hasattr(t, "dtype") and "bfloat16" in str(t.dtype):
+        t = t.contiguous().view(__import__("torch").int16).numpy()
+    return np.ascontiguousarray(t).view(np.uint16)

@@ -1,0 +1,352 @@
+/*
+ * Block-sparse attention oracle: plain, slow, obviously-correct CPU code.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file; only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code, header, table or helper with the
+ * CUDA library.  Floating point is IEEE binary64 throughout; the inputs that
+ * arrive as bf16 or fp32 are widened exactly.  Build with
+ * -ffp-contract=off so that no multiply-add is fused: the sampler below
+ * takes integer decisions from fp64 sums and must round exactly as written.
+ *
+ * What each function follows (page title, then the passage):
+ *   oracle_index_mask_u8   WaveAlign, "B. Sparse Attention for Long-Video
+ *                          Generation": a mask row per query block, a kept
+ *                          entry per executed (query block, KV block) pair.
+ *   oracle_index_threshold ScalingAttention, section 5.2 eq. (2):
+ *                          M_p = I(T <= p), compared in fp32.
+ *   oracle_index_topk      MC-Sparse, "The MC-Sparse Architecture" (keep the
+ *                          highest-scoring KV blocks of a query block) and
+ *                          InstaGen section 3.2.1 (top-k = the heavy set).
+ *   oracle_reorder_rows    WaveAlign, section IV-D "NNZ-Guided Intra-Wave
+ *                          Temporal Alignment": consecutive buckets of at
+ *                          most W rows, each sorted by descending NNZ.
+ *   oracle_sample_blocks   InstaGen, section 3.2.1 eq. (4) (inclusion
+ *                          probabilities, cap at 1 and renormalise), the
+ *                          promotion of pi = 1 keys, systematic PPS sampling,
+ *                          and Algorithm 1 step 13 (w = 1/pi).
+ *   oracle_attention       InstaGen, section 3.1 eqs. (1)-(3) and Algorithm 1
+ *                          step 14 (softmax of l_ij + log w_j over the kept
+ *                          keys); INTRA, "CQS-Aware Token-Sparse
+ *                          FlashAttention Kernel" (keys and queries reached
+ *                          through index maps, outputs scattered back).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_BLOCK 128 /* query and key block edge (ScalingAttention 5.1, B = 128) */
+
+/* bf16 bit pattern -> exact double (bf16 is the top half of an fp32). */
+static double bf16_to_double(uint16_t h) {
+    uint32_t bits = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Index lists from a mask or a threshold map.                               */
+/* A row keeps the KV blocks whose predicate holds, in ascending block       */
+/* order.  A row with more than max_kv kept blocks is truncated to its first */
+/* max_kv entries and counted as an overflow; the return value is the number */
+/* of overflowing rows.                                                      */
+/* ------------------------------------------------------------------------- */
+static int32_t emit_row(const uint8_t* keep, int32_t nKB, int32_t* idx_row,
+                        int32_t max_kv, int32_t* cnt_out) {
+    int32_t n = 0, total = 0;
+    for (int32_t kb = 0; kb < nKB; ++kb) {
+        if (!keep[kb]) continue;
+        if (n < max_kv) idx_row[n++] = kb;
+        ++total;
+    }
+    for (int32_t e = n; e < max_kv; ++e) idx_row[e] = -1;
+    *cnt_out = n;
+    return total > max_kv;
+}
+
+int64_t oracle_index_mask_u8(const uint8_t* mask, int64_t rows, int32_t nKB,
+                             int32_t* kv_idx, int32_t* kv_cnt, int32_t max_kv) {
+    int64_t overflow = 0;
+    uint8_t* keep = (uint8_t*)malloc((size_t)nKB);
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int32_t kb = 0; kb < nKB; ++kb) keep[kb] = mask[r * nKB + kb] != 0;
+        overflow += emit_row(keep, nKB, kv_idx + r * max_kv, max_kv, kv_cnt + r);
+    }
+    free(keep);
+    return overflow;
+}
+
+int64_t oracle_index_threshold(const float* T, int64_t rows, int32_t nKB, float p,
+                               int32_t* kv_idx, int32_t* kv_cnt, int32_t max_kv) {
+    int64_t overflow = 0;
+    uint8_t* keep = (uint8_t*)malloc((size_t)nKB);
+    for (int64_t r = 0; r < rows; ++r) {
+        /* M_p = I(T <= p): inclusive, both operands fp32. */
+        for (int32_t kb = 0; kb < nKB; ++kb) keep[kb] = T[r * nKB + kb] <= p;
+        overflow += emit_row(keep, nKB, kv_idx + r * max_kv, max_kv, kv_cnt + r);
+    }
+    free(keep);
+    return overflow;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Top-k per row: a full sort by (score descending, block ascending), keep   */
+/* the first k, then list the kept blocks in ascending block order.          */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+    float s;
+    int32_t kb;
+} scored_t;
+
+static int by_score_desc_then_kb(const void* a, const void* b) {
+    const scored_t* x = (const scored_t*)a;
+    const scored_t* y = (const scored_t*)b;
+    if (x->s > y->s) return -1;
+    if (x->s < y->s) return 1;
+    return (x->kb > y->kb) - (x->kb < y->kb);
+}
+
+int64_t oracle_index_topk(const float* scores, int64_t rows, int32_t nKB,
+                          const int32_t* k_per_row, int32_t k_const,
+                          int32_t* kv_idx, int32_t* kv_cnt, int32_t max_kv) {
+    int64_t overflow = 0;
+    scored_t* tmp = (scored_t*)malloc(sizeof(scored_t) * (size_t)nKB);
+    uint8_t* keep = (uint8_t*)malloc((size_t)nKB);
+    for (int64_t r = 0; r < rows; ++r) {
+        int32_t k = k_per_row ? k_per_row[r] : k_const;
+        if (k > nKB) k = nKB;
+        if (k < 0) k = 0;
+        for (int32_t kb = 0; kb < nKB; ++kb) {
+            tmp[kb].s = scores[r * nKB + kb];
+            tmp[kb].kb = kb;
+        }
+        qsort(tmp, (size_t)nKB, sizeof(scored_t), by_score_desc_then_kb);
+        memset(keep, 0, (size_t)nKB);
+        for (int32_t i = 0; i < k; ++i) keep[tmp[i].kb] = 1;
+        overflow += emit_row(keep, nKB, kv_idx + r * max_kv, max_kv, kv_cnt + r);
+    }
+    free(keep);
+    free(tmp);
+    return overflow;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Query-row reordering, stage 2 of WaveAlign.  For each head the input     */
+/* order (identity when order_in is NULL) is cut into consecutive buckets of */
+/* `wave` slots; each bucket is stably sorted by descending KV-block count.  */
+/* row_perm[h][slot] is the query block that runs in that execution slot.    */
+/* ------------------------------------------------------------------------- */
+void oracle_reorder_rows(const int32_t* kv_cnt, const int32_t* order_in, int64_t heads,
+                         int32_t nQB, int32_t wave, int32_t* row_perm) {
+    int32_t* ord = (int32_t*)malloc(sizeof(int32_t) * (size_t)nQB);
+    for (int64_t h = 0; h < heads; ++h) {
+        const int32_t* cnt = kv_cnt + h * nQB;
+        for (int32_t i = 0; i < nQB; ++i) ord[i] = order_in ? order_in[h * nQB + i] : i;
+        for (int32_t b0 = 0; b0 < nQB; b0 += wave) {
+            int32_t b1 = b0 + wave < nQB ? b0 + wave : nQB;
+            /* stable insertion sort on descending count */
+            for (int32_t i = b0 + 1; i < b1; ++i) {
+                int32_t q = ord[i];
+                int32_t j = i - 1;
+                while (j >= b0 && cnt[ord[j]] < cnt[q]) {
+                    ord[j + 1] = ord[j];
+                    --j;
+                }
+                ord[j + 1] = q;
+            }
+        }
+        memcpy(row_perm + h * nQB, ord, sizeof(int32_t) * (size_t)nQB);
+    }
+    free(ord);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Exact set + PPSWOR sample of the residual, InstaGen section 3.2.1.        */
+/*                                                                           */
+/* Per row: the residual R is every KV block not in the exact list.  The     */
+/* inclusion probabilities are pi_j = min(1, lambda s_j) with                */
+/* sum_R pi_j = m (eq. 4), found by capping at 1 and renormalising until the */
+/* capped set stops growing.  Capped blocks (pi = 1) are promoted: always    */
+/* kept, weight 1.  The other m' = m - |capped| blocks are drawn by          */
+/* systematic PPS: with one uniform u in [0,1) the points u, u+1, ...,       */
+/* u+m'-1 are laid on the running sum C_j of pi over the uncapped residual   */
+/* in ascending block order, and block j is drawn when a point falls in      */
+/* [C_{j-1}, C_j), i.e. when ceil(C_j - u) > ceil(C_{j-1} - u).  Every drawn */
+/* block gets log-weight -log(pi_j) (Algorithm 1 step 13, w = 1/pi).        */
+/*                                                                           */
+/* Output list: exact, promoted and sampled blocks merged in ascending block */
+/* order, with log_w 0 for exact and promoted entries.  Returns the number   */
+/* of rows whose merged list did not fit in max_kv (truncated).              */
+/* Summation order is ascending block order; the file is built without      */
+/* fused multiply-adds.                                                      */
+/* ------------------------------------------------------------------------- */
+int64_t oracle_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
+                             const int32_t* exact_idx, const int32_t* exact_cnt,
+                             int32_t exact_stride, int32_t m, const double* u,
+                             int32_t* kv_idx, int32_t* kv_cnt, float* log_w,
+                             int32_t max_kv) {
+    int64_t overflow = 0;
+    uint8_t* state = (uint8_t*)malloc((size_t)nKB); /* 0 residual, 1 exact, 2 promoted, 3 sampled */
+    double* pi = (double*)malloc(sizeof(double) * (size_t)nKB);
+    for (int64_t r = 0; r < rows; ++r) {
+        const float* s = scores + r * nKB;
+        memset(state, 0, (size_t)nKB);
+        for (int32_t e = 0; e < exact_cnt[r]; ++e) state[exact_idx[r * exact_stride + e]] = 1;
+        int32_t n_res = 0;
+        for (int32_t kb = 0; kb < nKB; ++kb) n_res += state[kb] == 0;
+
+        if (n_res <= m) {
+            /* the budget covers the whole residual: every block has pi = 1 */
+            for (int32_t kb = 0; kb < nKB; ++kb)
+                if (state[kb] == 0) state[kb] = 2;
+        } else {
+            /* eq. (4): cap at 1 and renormalise until the capped set is stable */
+            int32_t n_cap = 0;
+            double lambda = 0.0;
+            for (;;) {
+                double sum = 0.0;
+                for (int32_t kb = 0; kb < nKB; ++kb)
+                    if (state[kb] == 0) sum += (double)s[kb];
+                lambda = (double)(m - n_cap) / sum;
+                int32_t grew = 0;
+                for (int32_t kb = 0; kb < nKB; ++kb) {
+                    if (state[kb] == 0 && lambda * (double)s[kb] >= 1.0) {
+                        state[kb] = 2;
+                        ++n_cap;
+                        grew = 1;
+                    }
+                }
+                if (!grew) break;
+            }
+            /* systematic PPS over the uncapped residual */
+            const int32_t m_rest = m - n_cap;
+            const double ur = u[r];
+            double C = 0.0;
+            int32_t drawn = 0;
+            for (int32_t kb = 0; kb < nKB; ++kb) {
+                if (state[kb] != 0) continue;
+                const double p = lambda * (double)s[kb];
+                const double C_prev = C;
+                C = C + p;
+                if (drawn < m_rest && ceil(C - ur) > ceil(C_prev - ur)) {
+                    state[kb] = 3;
+                    pi[kb] = p;
+                    ++drawn;
+                }
+            }
+        }
+        /* merge in ascending block order */
+        int32_t n = 0, total = 0;
+        for (int32_t kb = 0; kb < nKB; ++kb) {
+            if (state[kb] == 0) continue;
+            if (n < max_kv) {
+                kv_idx[r * max_kv + n] = kb;
+                log_w[r * max_kv + n] = state[kb] == 3 ? (float)(-log(pi[kb])) : 0.0f;
+                ++n;
+            }
+            ++total;
+        }
+        for (int32_t e = n; e < max_kv; ++e) {
+            kv_idx[r * max_kv + e] = -1;
+            log_w[r * max_kv + e] = 0.0f;
+        }
+        kv_cnt[r] = n;
+        overflow += total > max_kv;
+    }
+    free(pi);
+    free(state);
+    return overflow;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Masked, log-weighted softmax attention from its definition.               */
+/*                                                                           */
+/* Tensors q, k, v are bf16 bit patterns laid out [B*H, N, D].  Gathered    */
+/* position p of head bh holds query token q_map[bh][p] (p itself when       */
+/* q_map is NULL) and key/value token kv_map[bh][p] (likewise).  The query   */
+/* block of p is p / 128; its KV list is kv_idx[row][0..kv_cnt[row]) with   */
+/* row = bh * nQB + qb, and list entry e covers gathered key positions       */
+/* 128*kb .. 128*kb+127, all with log-weight log_w[row][e] (0 when NULL).    */
+/*                                                                           */
+/* For each selected query block (sel[i] = bh * nQB + qb) and each of its    */
+/* 128 positions p, with i = q_map(p):                                       */
+/*     s_j   = (q_i . k_j) * scale + lw          over every listed key j     */
+/*     LSE_i = ln sum_j exp(s_j)                 (max-shifted)               */
+/*     O_i   = sum_j exp(s_j - LSE_i) v_j                                    */
+/* An empty list gives O_i = 0 and LSE_i = -inf.  Results go to              */
+/* O[(i_sel*128 + r) * D + d], LSE[i_sel*128 + r], and tok[...] = i, the     */
+/* original token the row belongs to (the scatter-back target).             */
+/* scale <= 0 selects 1/sqrt(D).                                             */
+/* ------------------------------------------------------------------------- */
+void oracle_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                      int32_t B, int32_t H, int32_t N, int32_t D,
+                      const int32_t* kv_idx, const int32_t* kv_cnt, int32_t max_kv,
+                      const float* log_w, const int32_t* q_map, const int32_t* kv_map,
+                      double scale, const int64_t* sel, int64_t nsel,
+                      double* O, double* LSE, int32_t* tok) {
+    const int32_t nQB = N / ORACLE_BLOCK;
+    if (scale <= 0.0) scale = 1.0 / sqrt((double)D);
+    (void)B;
+    (void)H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t w = 0; w < nsel * ORACLE_BLOCK; ++w) {
+        const int64_t i_sel = w / ORACLE_BLOCK;
+        const int32_t r = (int32_t)(w % ORACLE_BLOCK);
+        const int64_t row = sel[i_sel];
+        const int64_t bh = row / nQB;
+        const int32_t qb = (int32_t)(row % nQB);
+        const int32_t p = qb * ORACLE_BLOCK + r;
+        const int32_t i = q_map ? q_map[bh * N + p] : p;
+        const int32_t cnt = kv_cnt[row];
+        double* o = O + w * D;
+        tok[w] = i;
+        for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
+        if (cnt <= 0) {
+            LSE[w] = -INFINITY;
+            continue;
+        }
+        const int64_t nkeys = (int64_t)cnt * ORACLE_BLOCK;
+        double* s = (double*)malloc(sizeof(double) * (size_t)nkeys);
+        int32_t* key = (int32_t*)malloc(sizeof(int32_t) * (size_t)nkeys);
+        double* qi = (double*)malloc(sizeof(double) * (size_t)D);
+        for (int32_t d = 0; d < D; ++d) qi[d] = bf16_to_double(q[(bh * N + i) * D + d]);
+        for (int32_t e = 0; e < cnt; ++e) {
+            const int32_t kb = kv_idx[row * max_kv + e];
+            const double lw = log_w ? (double)log_w[row * max_kv + e] : 0.0;
+            for (int32_t t = 0; t < ORACLE_BLOCK; ++t) {
+                const int32_t pos = kb * ORACLE_BLOCK + t;
+                const int32_t j = kv_map ? kv_map[bh * N + pos] : pos;
+                double dot = 0.0;
+                for (int32_t d = 0; d < D; ++d) dot += qi[d] * bf16_to_double(k[(bh * N + j) * D + d]);
+                s[e * ORACLE_BLOCK + t] = dot * scale + lw;
+                key[e * ORACLE_BLOCK + t] = j;
+            }
+        }
+        double mx = -INFINITY;
+        for (int64_t x = 0; x < nkeys; ++x) mx = s[x] > mx ? s[x] : mx;
+        double z = 0.0;
+        for (int64_t x = 0; x < nkeys; ++x) z += exp(s[x] - mx);
+        const double lse = mx + log(z);
+        for (int64_t x = 0; x < nkeys; ++x) {
+            const double a = exp(s[x] - lse);
+            const uint16_t* vj = v + (bh * N + key[x]) * D;
+            for (int32_t d = 0; d < D; ++d) o[d] += a * bf16_to_double(vj[d]);
+        }
+        LSE[w] = lse;
+        free(qi);
+        free(key);
+        free(s);
+    }
+}
+
+/* Number of threads the OpenMP runtime will use (reported by the timer). */
+int32_t oracle_num_threads(void) {
+#ifdef _OPENMP
+    extern int omp_get_max_threads(void);
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
