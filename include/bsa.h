@@ -1,0 +1,208 @@
+/*
+ * bsa.h - C ABI of libbsa.so, GB300-native (sm_103a) forward block-sparse
+ * attention over 128 x 128 blocks.
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - The caller owns every buffer.  Array arguments are DEVICE pointers
+ *    unless stated otherwise; the library allocates no device memory.
+ *  - All launches are asynchronous on `stream` (a cudaStream_t passed as
+ *    void*; NULL is the legacy default stream).  Results are ready when the
+ *    stream is synchronised.
+ *  - Errors the host can see (null or misaligned pointers, bad sizes, an
+ *    unsupported head dimension) are returned immediately and nothing is
+ *    launched.  Conditions only the device can see (an index list longer
+ *    than max_kv, an index or map entry out of range, a wait that timed out)
+ *    are recorded in a per-device status word: the first such code wins and
+ *    bsa_device_status() reads and clears it.  No kernel traps.
+ *  - Tensors are row-major and contiguous.  "rows" of an index list are the
+ *    (batch, head, query block) triples in that nesting order:
+ *    row = (b * H + h) * nQB + qb.
+ *  - Block edge is 128 tokens for queries and keys (nQB = nKB = N / 128).
+ */
+#ifndef BSA_H
+#define BSA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BSA_OK = 0,
+    BSA_ERR_INVALID_ARG = 1, /* host-detected: bad pointer, size or alignment   */
+    BSA_ERR_UNSUPPORTED = 2, /* host-detected: e.g. D not in {64, 128}         */
+    BSA_ERR_OVERFLOW = 3,    /* device: a list longer than max_kv (truncated)  */
+    BSA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed               */
+    BSA_ERR_TIMEOUT = 5,     /* device: a bounded wait gave up                  */
+    BSA_ERR_BOUNDS = 6       /* device: an index/map/perm entry out of range    */
+} bsa_status;
+
+typedef enum {
+    BSA_IDX_MASK_U8 = 0,       /* src: uint8 [rows, nKB], keep entries != 0             */
+    BSA_IDX_THRESHOLD_F32 = 1, /* src: fp32 threshold map [rows, nKB], keep T <= p     */
+    BSA_IDX_TOPK_F32 = 2       /* src: fp32 block scores [rows, nKB], keep the k largest */
+} bsa_idx_mode;
+
+/*
+ * bsa_build_index - compact a mask / threshold map / score matrix into
+ * per-row KV-block index lists.
+ *
+ * Defined by: ScalingAttention, section 5.2 eq. (2) (the mask M_p = I(T <= p)
+ * instantiated from a threshold map) and section 7.2 (index-based row
+ * format); WaveAlign, "B. Sparse Attention for Long-Video Generation" (one
+ * mask row per query block, one kept entry per executed block product);
+ * MC-Sparse, "The MC-Sparse Architecture" and InstaGen section 3.2.1 (keep
+ * the top-k blocks by score).
+ *
+ *  mode      which predicate selects a block (see bsa_idx_mode).
+ *  src       device, [rows, nKB] uint8 (MASK) or fp32 (THRESHOLD, TOPK).
+ *  rows      number of (b, h, qb) rows, >= 0.
+ *  nKB       KV blocks per row, 1 .. 65536.
+ *  p         THRESHOLD: keep src <= p, compared in fp32 (inclusive).
+ *  k_per_row TOPK: device int32 [rows] or NULL to use k_const for every row.
+ *  k_const   TOPK: k when k_per_row is NULL.  k is clamped to [0, nKB].
+ *            Ties in score go to the lower block index; -0.0 equals +0.0.
+ *            Scores must not be NaN.
+ *  kv_idx    device int32 [rows, max_kv] out: the kept blocks of each row in
+ *            ascending block order, unused tail entries set to -1.
+ *  kv_cnt    device int32 [rows] out: number of valid entries.
+ *  max_kv    list capacity, 1 .. nKB.  A row with more kept blocks keeps its
+ *            first max_kv (ascending) and raises BSA_ERR_OVERFLOW on the
+ *            device status word.
+ *  Pointers must be 4-byte aligned (src of MASK: any alignment).
+ */
+bsa_status bsa_build_index(bsa_idx_mode mode, const void* src, int64_t rows, int32_t nKB,
+                           float p, const int32_t* k_per_row, int32_t k_const,
+                           int32_t* kv_idx, int32_t* kv_cnt, int32_t max_kv, void* stream);
+
+/*
+ * bsa_reorder_rows - query-row execution order, NNZ-guided within waves.
+ *
+ * Defined by: WaveAlign, section IV-B (waves of at most W rows per head) and
+ * section IV-D "NNZ-Guided Intra-Wave Temporal Alignment" (consecutive
+ * buckets of at most W rows, each sorted by descending KV-block count).
+ * Ties keep their input order.  Buckets restart at every head.
+ *
+ *  kv_cnt    device int32 [heads, nQB]: KV-block count of each query block.
+ *  order_in  device int32 [heads, nQB] input order (each row a permutation
+ *            of 0..nQB-1, e.g. a spatial ordering), or NULL for identity.
+ *  heads     B * H, >= 0.
+ *  nQB       query blocks per head, 1 .. 65536.
+ *  wave      W, 1 .. 65536: typically bsa_resident_ctas(D).
+ *  row_perm  device int32 [heads, nQB] out: row_perm[h][slot] = query block
+ *            executed in that slot; pass it to bsa_forward.
+ *  An order_in entry outside [0, nQB) raises BSA_ERR_BOUNDS on the device.
+ */
+bsa_status bsa_reorder_rows(const int32_t* kv_cnt, const int32_t* order_in, int64_t heads,
+                            int32_t nQB, int32_t wave, int32_t* row_perm, void* stream);
+
+/*
+ * bsa_sample_blocks - exact set plus an importance-weighted PPSWOR sample of
+ * the remaining KV blocks, with Horvitz-Thompson log-weights.
+ *
+ * Defined by: InstaGen, section 3.2.1 eq. (4) (pi_j = min(1, lambda s_j),
+ * sum over the residual = m, by capping at 1 and renormalising), eq. (5)
+ * (Horvitz-Thompson), the promotion of blocks whose pi reaches 1, systematic
+ * PPS sampling, and Algorithm 1 step 13 (w = 1 / pi).
+ *
+ * Per row, the residual is every block not in the exact list.  Blocks with
+ * pi = 1 are promoted (kept, weight 1).  The other m - |promoted| blocks are
+ * drawn by systematic PPS in ascending block order with the row's uniform
+ * u: block j is drawn when a point u + i falls in [C_{j-1}, C_j), C the
+ * running sum of pi.  lambda, pi and C are fp64, summed in ascending block
+ * order without fused multiply-adds, so the drawn set is reproducible.
+ *
+ *  scores       device fp32 [rows, nKB], every entry > 0.
+ *  exact_idx    device int32 [rows, exact_stride]: exact blocks, ascending.
+ *  exact_cnt    device int32 [rows].
+ *  exact_stride row stride of exact_idx, >= 1.
+ *  m            blocks to draw per row (sampling budget), >= 0.
+ *  u            device fp64 [rows], each in [0, 1).
+ *  kv_idx       device int32 [rows, max_kv] out: exact, promoted and drawn
+ *               blocks merged in ascending order (tail -1).
+ *  kv_cnt       device int32 [rows] out.
+ *  log_w        device fp32 [rows, max_kv] out: 0 for exact and promoted
+ *               entries, -log(pi_j) for drawn ones (tail 0).
+ *  max_kv       capacity; a longer merged list is truncated and raises
+ *               BSA_ERR_OVERFLOW.
+ *  Outputs must not alias inputs.  nKB <= 4096.
+ */
+bsa_status bsa_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
+                             const int32_t* exact_idx, const int32_t* exact_cnt,
+                             int32_t exact_stride, int32_t m, const double* u,
+                             int32_t* kv_idx, int32_t* kv_cnt, float* log_w, int32_t max_kv,
+                             void* stream);
+
+/*
+ * bsa_forward - block-sparse attention forward, O and LSE.
+ *
+ * Defined by: InstaGen, section 3.1 eqs. (1)-(3) (scaled dot-product
+ * attention) and Algorithm 1 step 14 (softmax over the kept keys of
+ * l_ij + log w_j, w the block's Horvitz-Thompson weight); INTRA,
+ * "CQS-Aware Token-Sparse FlashAttention Kernel" (query and key tokens
+ * reached through index maps, packed into dense tiles, outputs scattered
+ * back through the query map); WaveAlign, section V (rows run in a
+ * permuted order, outputs land in their original rows).
+ *
+ * For head bh = b*H + h, gathered position p holds query token q_map[bh][p]
+ * and key/value token kv_map[bh][p] (p itself when the map is NULL).  Query
+ * block qb = p / 128 attends to the keys at gathered positions
+ * 128*kb .. 128*kb+127 for every kb in its list, each block with log-weight
+ * lw = log_w[row][e] (0 when log_w is NULL):
+ *     s_ij  = (q_i . k_j) * scale + lw
+ *     LSE_i = ln sum_j exp(s_ij)           (natural log, of the weighted sum)
+ *     O_i   = sum_j exp(s_ij - LSE_i) v_j
+ * written to O[bh][i] and LSE[bh][i] with i = q_map[bh][p].  An empty list
+ * gives O_i = 0 and LSE_i = -inf.  Execution slot s of head bh computes
+ * query block row_perm[bh][s] (s when NULL); the order changes only the
+ * schedule, never the result.
+ *
+ *  q, k, v   device bf16 [B, H, N, D] contiguous, 16-byte aligned.
+ *  B, H, N   N a multiple of 128, 128 .. 2^24; B*H*N < 2^31.
+ *  D         head dimension, 64 or 128.
+ *  kv_idx    device int32 [B*H*nQB, max_kv]; kv_cnt device int32 [B*H*nQB].
+ *            Entries must be distinct within a row.  An entry outside
+ *            [0, nKB) is skipped and raises BSA_ERR_BOUNDS; a count above
+ *            max_kv is clamped and raises BSA_ERR_OVERFLOW.
+ *  max_kv    list capacity, 1 .. nKB.
+ *  log_w     device fp32 [B*H*nQB, max_kv] or NULL.
+ *  q_map, kv_map  device int32 [B*H, N] or NULL; each row must be a
+ *            permutation of 0..N-1 (a q_map entry outside [0, N) skips that
+ *            output row and raises BSA_ERR_BOUNDS).
+ *  row_perm  device int32 [B*H, nQB] or NULL (see bsa_reorder_rows).
+ *  scale     logit scale; <= 0 selects 1/sqrt(D).
+ *  o         device bf16 [B, H, N, D] out, 16-byte aligned.
+ *  lse       device fp32 [B, H, N] out.
+ */
+bsa_status bsa_forward(const void* q, const void* k, const void* v, int32_t B, int32_t H,
+                       int32_t N, int32_t D, const int32_t* kv_idx, const int32_t* kv_cnt,
+                       int32_t max_kv, const float* log_w, const int32_t* q_map,
+                       const int32_t* kv_map, const int32_t* row_perm, float scale, void* o,
+                       float* lse, void* stream);
+
+/*
+ * bsa_device_status - read and clear the status word of the current device.
+ * Synchronises `stream` first.  *first_error (host pointer) receives the
+ * first device-side bsa_status code raised since the last read (BSA_OK if
+ * none).  Returns BSA_ERR_CUDA if the synchronisation or copy failed.
+ */
+bsa_status bsa_device_status(void* stream, int32_t* first_error);
+
+/*
+ * bsa_resident_ctas - how many bsa_forward thread blocks the current device
+ * runs at once for head dimension D (SM count x resident blocks per SM):
+ * the wave size W that WaveAlign's scheduling model uses.  Returns a value
+ * <= 0 on error (no device, bad D).
+ */
+int32_t bsa_resident_ctas(int32_t D);
+
+/* Human-readable name of a status code (static string). */
+const char* bsa_status_string(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSA_H */

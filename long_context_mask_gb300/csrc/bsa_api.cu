@@ -1,0 +1,161 @@
+// C-ABI entry points of libbsa.so: argument validation, the per-device
+// status word, and dispatch to the kernels.  Every check here runs on the
+// host before anything is launched, so a rejected call touches no device.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "bsa.h"
+#include "bsa_internal.h"
+
+namespace bsa {
+namespace {
+
+// First device-side error since the last bsa_device_status(); one per device.
+__device__ int32_t g_status_word = 0;
+
+constexpr int kMaxDevices = 64;
+int32_t* g_status_ptr[kMaxDevices] = {nullptr};
+std::mutex g_status_mu;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+int32_t* status_word_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_status_mu);
+    if (g_status_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int32_t*>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+}  // namespace bsa
+
+using bsa::aligned;
+
+extern "C" {
+
+const char* bsa_status_string(int32_t s) {
+    switch (s) {
+        case BSA_OK: return "BSA_OK";
+        case BSA_ERR_INVALID_ARG: return "BSA_ERR_INVALID_ARG";
+        case BSA_ERR_UNSUPPORTED: return "BSA_ERR_UNSUPPORTED";
+        case BSA_ERR_OVERFLOW: return "BSA_ERR_OVERFLOW";
+        case BSA_ERR_CUDA: return "BSA_ERR_CUDA";
+        case BSA_ERR_TIMEOUT: return "BSA_ERR_TIMEOUT";
+        case BSA_ERR_BOUNDS: return "BSA_ERR_BOUNDS";
+        default: return "BSA_ERR_UNKNOWN";
+    }
+}
+
+bsa_status bsa_build_index(bsa_idx_mode mode, const void* src, int64_t rows, int32_t nKB, float p,
+                           const int32_t* k_per_row, int32_t k_const, int32_t* kv_idx,
+                           int32_t* kv_cnt, int32_t max_kv, void* stream) {
+    if (mode != BSA_IDX_MASK_U8 && mode != BSA_IDX_THRESHOLD_F32 && mode != BSA_IDX_TOPK_F32)
+        return BSA_ERR_INVALID_ARG;
+    if (rows < 0 || nKB < 1 || nKB > 65536 || max_kv < 1 || max_kv > nKB) return BSA_ERR_INVALID_ARG;
+    if (rows > ((int64_t)1 << 40)) return BSA_ERR_INVALID_ARG;
+    if (rows == 0) return BSA_OK;
+    if (!src || !kv_idx || !kv_cnt) return BSA_ERR_INVALID_ARG;
+    if (!aligned(kv_idx, 4) || !aligned(kv_cnt, 4)) return BSA_ERR_INVALID_ARG;
+    if (mode != BSA_IDX_MASK_U8 && !aligned(src, 4)) return BSA_ERR_INVALID_ARG;
+    if (mode == BSA_IDX_TOPK_F32) {
+        if (k_per_row && !aligned(k_per_row, 4)) return BSA_ERR_INVALID_ARG;
+        if (!k_per_row && k_const < 0) return BSA_ERR_INVALID_ARG;
+    }
+    int32_t* status = bsa::status_word_ptr();
+    if (!status) return BSA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (mode == BSA_IDX_TOPK_F32)
+        e = bsa::launch_index_topk(static_cast<const float*>(src), rows, nKB, k_per_row, k_const,
+                                   kv_idx, kv_cnt, max_kv, status, st);
+    else
+        e = bsa::launch_index_predicate(mode, src, rows, nKB, p, kv_idx, kv_cnt, max_kv, status, st);
+    return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
+bsa_status bsa_reorder_rows(const int32_t* kv_cnt, const int32_t* order_in, int64_t heads,
+                            int32_t nQB, int32_t wave, int32_t* row_perm, void* stream) {
+    if (heads < 0 || heads > 65535 || nQB < 1 || nQB > 65536 || wave < 1 || wave > 8192)
+        return BSA_ERR_INVALID_ARG;
+    if (heads == 0) return BSA_OK;
+    if (!kv_cnt || !row_perm) return BSA_ERR_INVALID_ARG;
+    if (!aligned(kv_cnt, 4) || !aligned(row_perm, 4) || (order_in && !aligned(order_in, 4)))
+        return BSA_ERR_INVALID_ARG;
+    int32_t* status = bsa::status_word_ptr();
+    if (!status) return BSA_ERR_CUDA;
+    cudaError_t e = bsa::launch_reorder_rows(kv_cnt, order_in, heads, nQB, wave, row_perm, status,
+                                             static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
+bsa_status bsa_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
+                             const int32_t* exact_idx, const int32_t* exact_cnt,
+                             int32_t exact_stride, int32_t m, const double* u, int32_t* kv_idx,
+                             int32_t* kv_cnt, float* log_w, int32_t max_kv, void* stream) {
+    if (rows < 0 || nKB < 1 || nKB > 4096 || exact_stride < 1 || m < 0 || max_kv < 1)
+        return BSA_ERR_INVALID_ARG;
+    if (rows == 0) return BSA_OK;
+    if (!scores || !exact_idx || !exact_cnt || !u || !kv_idx || !kv_cnt || !log_w)
+        return BSA_ERR_INVALID_ARG;
+    if (!aligned(scores, 4) || !aligned(exact_idx, 4) || !aligned(exact_cnt, 4) || !aligned(u, 8) ||
+        !aligned(kv_idx, 4) || !aligned(kv_cnt, 4) || !aligned(log_w, 4))
+        return BSA_ERR_INVALID_ARG;
+    int32_t* status = bsa::status_word_ptr();
+    if (!status) return BSA_ERR_CUDA;
+    cudaError_t e = bsa::launch_sample_blocks(scores, rows, nKB, exact_idx, exact_cnt, exact_stride,
+                                              m, u, kv_idx, kv_cnt, log_w, max_kv, status,
+                                              static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
+bsa_status bsa_forward(const void* q, const void* k, const void* v, int32_t B, int32_t H, int32_t N,
+                       int32_t D, const int32_t* kv_idx, const int32_t* kv_cnt, int32_t max_kv,
+                       const float* log_w, const int32_t* q_map, const int32_t* kv_map,
+                       const int32_t* row_perm, float scale, void* o, float* lse, void* stream) {
+    if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+    if (B < 1 || H < 1 || N < 128 || (N % 128) != 0 || N > (1 << 24)) return BSA_ERR_INVALID_ARG;
+    const int64_t total_rows = (int64_t)B * H * N;
+    if (total_rows >= ((int64_t)1 << 31) || (int64_t)B * H > 65535) return BSA_ERR_INVALID_ARG;
+    const int32_t nKB = N / 128;
+    if (max_kv < 1 || max_kv > nKB) return BSA_ERR_INVALID_ARG;
+    if (!q || !k || !v || !kv_idx || !kv_cnt || !o || !lse) return BSA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+        return BSA_ERR_INVALID_ARG;
+    if (!aligned(kv_idx, 4) || !aligned(kv_cnt, 4) || !aligned(lse, 4)) return BSA_ERR_INVALID_ARG;
+    if ((log_w && !aligned(log_w, 4)) || (row_perm && !aligned(row_perm, 4)))
+        return BSA_ERR_INVALID_ARG;
+    if ((q_map && !aligned(q_map, 16)) || (kv_map && !aligned(kv_map, 16)))
+        return BSA_ERR_INVALID_ARG;
+    int32_t* status = bsa::status_word_ptr();
+    if (!status) return BSA_ERR_CUDA;
+    bsa::ForwardArgs a{q,      k,     v,     B,       H,      N,        D,     kv_idx,
+                       kv_cnt, max_kv, log_w, q_map, kv_map, row_perm, scale, o,     lse};
+    return bsa::launch_forward(a, status, static_cast<cudaStream_t>(stream));
+}
+
+bsa_status bsa_device_status(void* stream, int32_t* first_error) {
+    if (!first_error) return BSA_ERR_INVALID_ARG;
+    int32_t* status = bsa::status_word_ptr();
+    if (!status) return BSA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return BSA_ERR_CUDA;
+    if (cudaMemcpyAsync(&v, status, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return BSA_ERR_CUDA;
+    if (cudaMemsetAsync(status, 0, sizeof(v), st) != cudaSuccess) return BSA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return BSA_ERR_CUDA;
+    *first_error = v;
+    return BSA_OK;
+}
+
+int32_t bsa_resident_ctas(int32_t D) { return bsa::forward_resident_ctas(D); }
+
+}  // extern "C"

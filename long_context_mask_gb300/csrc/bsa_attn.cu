@@ -1,0 +1,581 @@
+// Block-sparse attention forward for sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes (InstaGen, section 3.1 eqs. (1)-(3) and Algorithm 1
+// step 14; INTRA, "CQS-Aware Token-Sparse FlashAttention Kernel"): for every
+// (head, 128-row query block) the online softmax over the 128-key blocks in
+// its list, each block's scores shifted by the block's log-weight, and
+// O = P V / l, LSE = ln l + max, written back through the query map.
+//
+// One thread block owns one (head, query block) work item; blockIdx.x is the
+// execution slot within the head (query block row_perm[head][slot]) and
+// blockIdx.y the head, so blocks are issued head-major in slot order (the
+// sequential-head, wave-ordered schedule of WaveAlign section V).
+//
+// Warp roles (6 warps):
+//   warp 0      TMA producer: Q once, then K_j and V_j of every listed block
+//               into a ring of kStages shared-memory slots (tile loads, or
+//               tile::gather4 row gathers when index maps are given).
+//   warp 1      allocates tensor memory; one lane issues tcgen05.mma:
+//               S_j = Q K_j^T into one of two TMEM score buffers, and
+//               O += P_{j-1} V_{j-1} with P read from TMEM.
+//   warps 2..5  softmax: one thread per query row (TMEM lane); reads S_j,
+//               updates the running max / sum, writes P_j (bf16) back over
+//               S_j, rescales O in TMEM when the max grows by more than
+//               2^8, and runs the epilogue (O / l -> bf16, LSE).
+//
+// Tensor memory (512 columns): S0 = [0,128), S1 = [128,256), O = [256,256+D).
+// Shared memory: Q tile + kStages K/V tiles, each tile stored as D/64 boxes
+// of 128 rows x 128 bytes with the 128-byte swizzle (canonical K-major
+// layout for Q and K, MN-major for V).
+//
+// Every mbarrier wait is bounded (1 s of wall time); on expiry the status
+// word gets BSA_ERR_TIMEOUT, the roles stop, in-flight copies and MMAs are
+// drained (again bounded) and tensor memory is freed before exit.  Blocks
+// that start, or are waiting, while the status word holds BSA_ERR_TIMEOUT
+// give up at once, so a broken launch ends within about a second per wave
+// instead of a second per block.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "bsa_internal.h"
+#include "bsa_ptx.cuh"
+
+namespace bsa {
+namespace {
+
+using namespace ptx;
+
+constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // rescale O only when the max grows by > 2^8
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 256;
+
+template <int D>
+struct Cfg {
+    static constexpr int kBoxBytes = 128 * 128;  // 128 rows x 64 bf16
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kTile = kBoxBytes * kBoxes;
+    static constexpr int kStages = D == 128 ? 5 : 10;
+    static constexpr int kData = kTile * (1 + kStages);
+    static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
+    static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
+};
+
+struct Barriers {
+    uint64_t full[16];
+    uint64_t empty[16];
+    uint64_t q_full;
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t o_done;
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int32_t abort;
+};
+
+struct Params {
+    CUtensorMap map_q, map_k, map_v;     // box 64 x 128 rows
+    CUtensorMap gmap_q, gmap_k, gmap_v;  // box 64 x 1 row (gather4)
+    const int32_t* kv_idx;
+    const int32_t* kv_cnt;
+    const float* log_w;
+    const int32_t* q_map;
+    const int32_t* kv_map;
+    const int32_t* row_perm;
+    __nv_bfloat16* o;
+    float* lse;
+    int32_t* status;
+    int32_t N, nQB, max_kv;
+    float scale_log2;
+};
+
+__device__ __forceinline__ void raise_status(int32_t* status, int32_t code) {
+    atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Shared (warp-uniform) abort check.
+__device__ __forceinline__ bool aborted(const Barriers* b) {
+    return *reinterpret_cast<const volatile int32_t*>(&b->abort) != 0;
+}
+__device__ __forceinline__ void set_abort(Barriers* b, int32_t* status) {
+    *reinterpret_cast<volatile int32_t*>(&b->abort) = 1;
+    raise_status(status, BSA_ERR_TIMEOUT);
+}
+
+// Token rows of a 128-row tile gathered through a map: lane l covers rows 4l..4l+3.
+__device__ __forceinline__ int4 map_rows(const int32_t* map, int64_t base, int32_t N, int lane,
+                                         int32_t* status) {
+    int4 t = *reinterpret_cast<const int4*>(map + base + 4 * lane);
+    int32_t* v = reinterpret_cast<int32_t*>(&t);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (v[i] < 0 || v[i] >= N) {
+            raise_status(status, BSA_ERR_BOUNDS);
+            v[i] = 0;
+        }
+    }
+    return t;
+}
+
+template <int D>
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* tile_map,
+                                          const CUtensorMap* gather_map, const int32_t* map,
+                                          int64_t bh, int32_t N, int32_t blk, uint32_t bar,
+                                          int lane, int32_t* status) {
+    using C = Cfg<D>;
+    const int32_t row0 = (int32_t)(bh * N) + blk * 128;
+    if (map == nullptr) {
+        if (lane == 0) {
+#pragma unroll
+            for (int b = 0; b < C::kBoxes; ++b) tma_load_2d(dst + b * C::kBoxBytes, tile_map, 64 * b, row0, bar);
+        }
+    } else {
+        const int4 t = map_rows(map, bh * N + (int64_t)blk * 128, N, lane, status);
+        const int32_t base = (int32_t)(bh * N);
+#pragma unroll
+        for (int b = 0; b < C::kBoxes; ++b)
+            tma_gather4(dst + b * C::kBoxBytes + lane * 512, gather_map, 64 * b, base + t.x,
+                        base + t.y, base + t.z, base + t.w, bar);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_constant__ Params P) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s_q = smem_u32(smem);
+    const uint32_t s_ring = s_q + C::kTile;
+    Barriers* bars = reinterpret_cast<Barriers*>(smem + C::kData);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t bh = blockIdx.y;
+    const int32_t N = P.N, nQB = P.nQB, max_kv = P.max_kv;
+    const int32_t nKB = nQB;
+
+    // A block of this launch (or an unread earlier one) timed out: abandon.
+    if (*reinterpret_cast<const volatile int32_t*>(P.status) == BSA_ERR_TIMEOUT) return;
+
+    int32_t qb = blockIdx.x;
+    if (P.row_perm != nullptr) {
+        qb = P.row_perm[bh * nQB + blockIdx.x];
+        if (qb < 0 || qb >= nQB) {
+            if (threadIdx.x == 0) raise_status(P.status, BSA_ERR_BOUNDS);
+            return;
+        }
+    }
+    const int64_t row = bh * nQB + qb;
+    int32_t cnt = P.kv_cnt[row];
+    if (cnt > max_kv) {
+        if (threadIdx.x == 0) raise_status(P.status, BSA_ERR_OVERFLOW);
+        cnt = max_kv;
+    }
+    if (cnt < 0) {
+        if (threadIdx.x == 0) raise_status(P.status, BSA_ERR_BOUNDS);
+        cnt = 0;
+    }
+    const int32_t* list = P.kv_idx + row * max_kv;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(smem_u32(&bars->full[s]), 1);
+            mbar_init(smem_u32(&bars->empty[s]), 1);
+        }
+        mbar_init(smem_u32(&bars->q_full), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(smem_u32(&bars->s_full[s]), 1);
+            mbar_init(smem_u32(&bars->p_full[s]), 128);
+        }
+        mbar_init(smem_u32(&bars->o_done), 1);
+        mbar_init(smem_u32(&bars->mma_done), 1);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(P.kv_map ? &P.gmap_k : &P.map_k);
+        prefetch_tensormap(P.kv_map ? &P.gmap_v : &P.map_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        int32_t issued = 0;
+        if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bars->q_full), C::kTile);
+        __syncwarp();
+        load_tile<D>(s_q, &P.map_q, &P.gmap_q, P.q_map, bh, N, qb, smem_u32(&bars->q_full), lane,
+                     P.status);
+        for (int32_t e = 0; e < cnt; ++e) {
+            const int32_t kb = list[e];
+            if (kb < 0 || kb >= nKB) {
+                if (lane == 0) raise_status(P.status, BSA_ERR_BOUNDS);
+                continue;
+            }
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const int32_t slot = issued % C::kStages;
+                const uint32_t phase = (uint32_t)(issued / C::kStages) & 1u;
+                int ok = 1;
+                if (lane == 0) ok = mbar_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok || aborted(bars)) {
+                    if (lane == 0) set_abort(bars, P.status);
+                    goto producer_done;
+                }
+                const uint32_t fb = smem_u32(&bars->full[slot]);
+                if (lane == 0) mbar_arrive_expect_tx(fb, C::kTile);
+                __syncwarp();
+                load_tile<D>(s_ring + slot * C::kTile, which ? &P.map_v : &P.map_k,
+                             which ? &P.gmap_v : &P.gmap_k, P.kv_map, bh, N, kb, fb, lane,
+                             P.status);
+                ++issued;
+            }
+        }
+    producer_done:
+        // Drain: every issued copy must land before the block exits.
+        if (lane == 0) {
+            if (!mbar_wait(smem_u32(&bars->q_full), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT)) raise_status(P.status, BSA_ERR_TIMEOUT);
+            const int32_t first = issued > C::kStages ? issued - C::kStages : 0;
+            for (int32_t i = first; i < issued; ++i)
+                if (!mbar_wait(smem_u32(&bars->full[i % C::kStages]), (uint32_t)(i / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT))
+                    raise_status(P.status, BSA_ERR_TIMEOUT);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int32_t j = 0;
+            bool ok = mbar_wait(smem_u32(&bars->q_full), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+            tc_fence_after();
+            auto issue_pv = [&](int32_t i) -> bool {
+                if (!mbar_wait(smem_u32(&bars->p_full[i & 1]), (uint32_t)(i >> 1) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT)) return false;
+                const int32_t item = 2 * i + 1;
+                const int32_t slot = item % C::kStages;
+                if (!mbar_wait(smem_u32(&bars->full[slot]), (uint32_t)(item / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT)) return false;
+                tc_fence_after();
+                const uint32_t sv = s_ring + slot * C::kTile;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t bdesc = smem_desc_sw128(sv + kk * 2048, C::kBoxBytes, 1024);
+                    mma_ts(tmem + kColO, tmem + (uint32_t)(i & 1) * 128u + kk * 8, bdesc, C::kIdescPV,
+                           (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(smem_u32(&bars->empty[slot]));
+                mma_commit(smem_u32(&bars->o_done));
+                return true;
+            };
+            for (int32_t e = 0; ok && e < cnt; ++e) {
+                const int32_t kb = list[e];
+                if (kb < 0 || kb >= nKB) continue;
+                if (aborted(bars)) {
+                    ok = false;
+                    break;
+                }
+                const int32_t item = 2 * j;
+                const int32_t slot = item % C::kStages;
+                if (!mbar_wait(smem_u32(&bars->full[slot]), (uint32_t)(item / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sk = s_ring + slot * C::kTile;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+                    const uint64_t adesc = smem_desc_sw128(s_q + off, 16, 1024);
+                    const uint64_t bdesc = smem_desc_sw128(sk + off, 16, 1024);
+                    mma_ss(tmem + (uint32_t)(j & 1) * 128u, adesc, bdesc, C::kIdescQK, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(smem_u32(&bars->empty[slot]));
+                mma_commit(smem_u32(&bars->s_full[j & 1]));
+                if (j > 0 && !issue_pv(j - 1)) {
+                    ok = false;
+                    break;
+                }
+                ++j;
+            }
+            if (ok && j > 0 && !aborted(bars)) ok = issue_pv(j - 1);
+            if (!ok) set_abort(bars, P.status);
+            // Drain: nothing of ours may still be running when TMEM is freed.
+            mma_commit(smem_u32(&bars->mma_done));
+            if (!mbar_wait(smem_u32(&bars->mma_done), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT)) raise_status(P.status, BSA_ERR_TIMEOUT);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int qd = warp & 3;                 // TMEM lane quadrant of this warp
+        const int r = qd * 32 + lane;            // row within the query tile
+        const uint32_t t_lane = tmem + ((uint32_t)(qd * 32) << 16);
+        const int32_t p = qb * 128 + r;
+        int32_t tok = p;
+        bool tok_ok = true;
+        if (P.q_map != nullptr) {
+            tok = P.q_map[bh * N + p];
+            if (tok < 0 || tok >= N) {
+                raise_status(P.status, BSA_ERR_BOUNDS);
+                tok_ok = false;
+            }
+        }
+        const float sl2 = P.scale_log2;
+        float m = -INFINITY, l = 0.0f;
+        int32_t j = 0;
+        bool ok = true;
+        for (int32_t e = 0; e < cnt; ++e) {
+            const int32_t kb = list[e];
+            if (kb < 0 || kb >= nKB) continue;
+            const float lw2 = P.log_w ? P.log_w[row * max_kv + e] * kLog2e : 0.0f;
+            const uint32_t sbuf = (uint32_t)(j & 1) * 128u;
+            bool w = mbar_wait(smem_u32(&bars->s_full[j & 1]), (uint32_t)(j >> 1) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+            if (__any_sync(0xffffffffu, !w || aborted(bars))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t s[128];
+            tmem_ld32(t_lane + sbuf + 0, &s[0]);
+            tmem_ld32(t_lane + sbuf + 32, &s[32]);
+            tmem_ld32(t_lane + sbuf + 64, &s[64]);
+            tmem_ld32(t_lane + sbuf + 96, &s[96]);
+            tmem_wait_ld();
+            float mx0 = __uint_as_float(s[0]), mx1 = __uint_as_float(s[1]);
+            float mx2 = __uint_as_float(s[2]), mx3 = __uint_as_float(s[3]);
+#pragma unroll
+            for (int c = 4; c < 128; c += 4) {
+                mx0 = fmaxf(mx0, __uint_as_float(s[c + 0]));
+                mx1 = fmaxf(mx1, __uint_as_float(s[c + 1]));
+                mx2 = fmaxf(mx2, __uint_as_float(s[c + 2]));
+                mx3 = fmaxf(mx3, __uint_as_float(s[c + 3]));
+            }
+            const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2 + lw2;
+            if (j == 0) {
+                m = mt;
+            } else if (__any_sync(0xffffffffu, mt > m + kRescaleThreshold)) {
+                const float m_new = fmaxf(m, mt);
+                const float alpha = ex2(m - m_new);
+                l *= alpha;
+                m = m_new;
+                // O holds P_0..P_{j-2} V: wait for P_{j-1} V_{j-1} before touching it.
+                w = mbar_wait(smem_u32(&bars->o_done), (uint32_t)(j - 1) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                if (__any_sync(0xffffffffu, !w)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(t_lane + kColO + c, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(t_lane + kColO + c, o);
+                }
+            }
+            const float bias = lw2 - m;
+            float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+            for (int c = 0; c < 128; c += 4) {
+                const float p0 = ex2(fmaf(__uint_as_float(s[c + 0]), sl2, bias));
+                const float p1 = ex2(fmaf(__uint_as_float(s[c + 1]), sl2, bias));
+                const float p2 = ex2(fmaf(__uint_as_float(s[c + 2]), sl2, bias));
+                const float p3 = ex2(fmaf(__uint_as_float(s[c + 3]), sl2, bias));
+                l0 += p0;
+                l1 += p1;
+                l2 += p2;
+                l3 += p3;
+                s[c / 2] = pack_bf16(p0, p1);
+                s[c / 2 + 1] = pack_bf16(p2, p3);
+            }
+            l += (l0 + l1) + (l2 + l3);
+            tmem_st32(t_lane + sbuf + 0, &s[0]);
+            tmem_st32(t_lane + sbuf + 32, &s[32]);
+            tmem_wait_st();
+            if (j > 0) {
+                // keeps this thread at most one O phase behind (unambiguous parity waits)
+                w = mbar_wait(smem_u32(&bars->o_done), (uint32_t)(j - 1) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                if (__any_sync(0xffffffffu, !w)) {
+                    ok = false;
+                    break;
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars->p_full[j & 1]));
+            ++j;
+        }
+        if (!ok) {
+            if (lane == 0) set_abort(bars, P.status);
+        } else {
+            __nv_bfloat16* orow = P.o + (bh * N + tok) * D;
+            if (j == 0) {
+                if (tok_ok) {
+                    uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(orow + c) = z;
+                    P.lse[bh * N + tok] = -INFINITY;
+                }
+            } else {
+                const bool w = mbar_wait(smem_u32(&bars->o_done), (uint32_t)(j - 1) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                if (__any_sync(0xffffffffu, !w)) {
+                    if (lane == 0) set_abort(bars, P.status);
+                } else {
+                    tc_fence_after();
+                    const float inv_l = 1.0f / l;
+#pragma unroll
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(t_lane + kColO + c, o);
+                        tmem_wait_ld();
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l,
+                                              __uint_as_float(o[2 * i + 1]) * inv_l);
+                        if (tok_ok) {
+                            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        }
+                    }
+                    if (tok_ok) P.lse[bh * N + tok] = (m + log2f(l)) * kLn2;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool encode_map(CUtensorMap* map, const void* base, uint64_t rows, int D, uint32_t box_rows) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D>
+size_t smem_bytes() {
+    return 1024 + Cfg<D>::kData + sizeof(Barriers);
+}
+
+template <int D>
+cudaError_t prepare_kernel() {
+    // Per device: opt in to the large dynamic shared-memory carve-out.
+    static int done[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && done[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(k_bsa_forward<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_bytes<D>());
+    if (e == cudaSuccess && dev < 64) done[dev] = 1;
+    return e;
+}
+
+template <int D>
+bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) {
+    if (prepare_kernel<D>() != cudaSuccess) return BSA_ERR_CUDA;
+    Params P;
+    memset(&P, 0, sizeof(P));
+    const uint64_t rows = (uint64_t)a.B * a.H * a.N;
+    bool ok = encode_map(&P.map_q, a.q, rows, D, 128) && encode_map(&P.map_k, a.k, rows, D, 128) &&
+              encode_map(&P.map_v, a.v, rows, D, 128) && encode_map(&P.gmap_q, a.q, rows, D, 1) &&
+              encode_map(&P.gmap_k, a.k, rows, D, 1) && encode_map(&P.gmap_v, a.v, rows, D, 1);
+    if (!ok) return BSA_ERR_CUDA;
+    P.kv_idx = a.kv_idx;
+    P.kv_cnt = a.kv_cnt;
+    P.log_w = a.log_w;
+    P.q_map = a.q_map;
+    P.kv_map = a.kv_map;
+    P.row_perm = a.row_perm;
+    P.o = static_cast<__nv_bfloat16*>(a.o);
+    P.lse = a.lse;
+    P.status = status;
+    P.N = a.N;
+    P.nQB = a.N / 128;
+    P.max_kv = a.max_kv;
+    const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
+    P.scale_log2 = scale * kLog2e;
+    const dim3 grid((unsigned)P.nQB, (unsigned)(a.B * a.H));
+    k_bsa_forward<D><<<grid, kThreads, smem_bytes<D>(), stream>>>(P);
+    return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
+}  // namespace
+
+bsa_status launch_forward(const ForwardArgs& a, int32_t* status, cudaStream_t stream) {
+    if (a.D == 128) return launch_d<128>(a, status, stream);
+    if (a.D == 64) return launch_d<64>(a, status, stream);
+    return BSA_ERR_UNSUPPORTED;
+}
+
+int32_t forward_resident_ctas(int32_t D) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    cudaError_t e;
+    if (D == 128) {
+        if (prepare_kernel<128>() != cudaSuccess) return -1;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bsa_forward<128>, kThreads, smem_bytes<128>());
+    } else if (D == 64) {
+        if (prepare_kernel<64>() != cudaSuccess) return -1;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bsa_forward<64>, kThreads, smem_bytes<64>());
+    } else {
+        return -1;
+    }
+    if (e != cudaSuccess) return -1;
+    return sms * per_sm;
+}
+
+}  // namespace bsa

@@ -1,0 +1,315 @@
+// Index-list construction, row reordering and block sampling kernels.
+//
+//  * Predicate compaction (mask / threshold map -> ascending KV-block lists):
+//    one warp per row; each 32-block chunk is one __ballot_sync word, and a
+//    block's slot is its prefix popcount.  ScalingAttention, section 5.2
+//    eq. (2) (M_p = I(T <= p)) and section 7.2 (a 32-block bitmask word per
+//    load); WaveAlign, "B. Sparse Attention for Long-Video Generation".
+//  * Top-k (MC-Sparse, "The MC-Sparse Architecture"; InstaGen 3.2.1): one
+//    warp per row, a 1-bit-per-pass radix select of the k-th largest
+//    order-preserving key, ties resolved toward the lower block index with a
+//    ballot scan, then the same ballot compaction.
+//  * Row reordering (WaveAlign section IV-D): one thread block per
+//    (head, bucket of W slots); each row's slot in its bucket is its rank
+//    under (count descending, input position ascending).
+//  * Block sampling (InstaGen section 3.2.1 eq. (4), systematic PPS,
+//    Algorithm 1 step 13): one thread per row, fp64, fixed summation order,
+//    explicit round-to-nearest arithmetic (never fused).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "bsa_internal.h"
+
+namespace bsa {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ void raise_status(int32_t* status, int32_t code) {
+    atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// ------------------------------------------------------------ compaction
+template <int MODE>
+__device__ __forceinline__ bool keep_block(const void* src, int64_t off, float p) {
+    if (MODE == BSA_IDX_MASK_U8) return static_cast<const uint8_t*>(src)[off] != 0;
+    return static_cast<const float*>(src)[off] <= p;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(256) k_index_predicate(const void* __restrict__ src, int64_t rows,
+                                                         int32_t nKB, float p,
+                                                         int32_t* __restrict__ kv_idx,
+                                                         int32_t* __restrict__ kv_cnt,
+                                                         int32_t max_kv, int32_t* status) {
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const int64_t base_in = row * (int64_t)nKB;
+    int32_t* out = kv_idx + row * (int64_t)max_kv;
+    int32_t n = 0;
+    for (int32_t c = 0; c < nKB; c += 32) {
+        const int32_t kb = c + lane;
+        const bool keep = kb < nKB && keep_block<MODE>(src, base_in + kb, p);
+        const uint32_t word = __ballot_sync(kFull, keep);
+        const int32_t pos = n + __popc(word & lanemask_lt());
+        if (keep && pos < max_kv) out[pos] = kb;
+        n += __popc(word);
+    }
+    const int32_t kept = n < max_kv ? n : max_kv;
+    for (int32_t e = kept + lane; e < max_kv; e += 32) out[e] = -1;
+    if (lane == 0) {
+        kv_cnt[row] = kept;
+        if (n > max_kv) raise_status(status, BSA_ERR_OVERFLOW);
+    }
+}
+
+// ------------------------------------------------------------ top-k
+// Order-preserving map fp32 -> uint32 (larger float -> larger key); -0 == +0.
+__device__ __forceinline__ uint32_t order_key(float f) {
+    uint32_t b = __float_as_uint(f);
+    if (b == 0x80000000u) b = 0u;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(256) k_index_topk(const float* __restrict__ scores, int64_t rows,
+                                                    int32_t nKB, const int32_t* __restrict__ k_per_row,
+                                                    int32_t k_const, int32_t* __restrict__ kv_idx,
+                                                    int32_t* __restrict__ kv_cnt, int32_t max_kv,
+                                                    int32_t* status) {
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const float* s = scores + row * (int64_t)nKB;
+    int32_t* out = kv_idx + row * (int64_t)max_kv;
+    int32_t k = k_per_row ? k_per_row[row] : k_const;
+    k = k < 0 ? 0 : (k > nKB ? nKB : k);
+
+    int32_t n = 0;
+    if (k > 0) {
+        // Largest key value T with #{key >= T} >= k, one bit per pass.
+        uint32_t T = 0;
+        for (int bit = 31; bit >= 0; --bit) {
+            const uint32_t cand = T | (1u << bit);
+            int32_t c = 0;
+            for (int32_t kb = lane; kb < nKB; kb += 32) c += order_key(s[kb]) >= cand;
+            c = __reduce_add_sync(kFull, c);
+            if (c >= k) T = cand;
+        }
+        int32_t gt = 0;
+        for (int32_t kb = lane; kb < nKB; kb += 32) gt += order_key(s[kb]) > T;
+        gt = __reduce_add_sync(kFull, gt);
+        const int32_t need_eq = k - gt;  // >= 1: equal keys taken from the lowest block up
+        int32_t eq_seen = 0;
+        for (int32_t c = 0; c < nKB; c += 32) {
+            const int32_t kb = c + lane;
+            const uint32_t key = kb < nKB ? order_key(s[kb]) : 0u;
+            const bool eq = kb < nKB && key == T;
+            const uint32_t eq_word = __ballot_sync(kFull, eq);
+            const bool sel = kb < nKB && (key > T || (eq && eq_seen + __popc(eq_word & lanemask_lt()) < need_eq));
+            eq_seen += __popc(eq_word);
+            const uint32_t word = __ballot_sync(kFull, sel);
+            const int32_t pos = n + __popc(word & lanemask_lt());
+            if (sel && pos < max_kv) out[pos] = kb;
+            n += __popc(word);
+        }
+    }
+    const int32_t kept = n < max_kv ? n : max_kv;
+    for (int32_t e = kept + lane; e < max_kv; e += 32) out[e] = -1;
+    if (lane == 0) {
+        kv_cnt[row] = kept;
+        if (n > max_kv) raise_status(status, BSA_ERR_OVERFLOW);
+    }
+}
+
+// ------------------------------------------------------------ reorder
+// grid: (buckets per head, heads); dynamic smem: 2 * W int32.
+__global__ void __launch_bounds__(256) k_reorder_rows(const int32_t* __restrict__ kv_cnt,
+                                                      const int32_t* __restrict__ order_in,
+                                                      int32_t nQB, int32_t wave,
+                                                      int32_t* __restrict__ row_perm,
+                                                      int32_t* status) {
+    extern __shared__ int32_t sm[];
+    const int64_t h = blockIdx.y;
+    const int32_t b0 = blockIdx.x * wave;
+    const int32_t len = min(wave, nQB - b0);
+    int32_t* s_qb = sm;
+    int32_t* s_cnt = sm + wave;
+    for (int32_t i = threadIdx.x; i < len; i += blockDim.x) {
+        int32_t qb = order_in ? order_in[h * nQB + b0 + i] : b0 + i;
+        if (qb < 0 || qb >= nQB) {
+            raise_status(status, BSA_ERR_BOUNDS);
+            qb = 0;
+        }
+        s_qb[i] = qb;
+        s_cnt[i] = kv_cnt[h * nQB + qb];
+    }
+    __syncthreads();
+    for (int32_t i = threadIdx.x; i < len; i += blockDim.x) {
+        const int32_t ci = s_cnt[i];
+        int32_t rank = 0;
+        for (int32_t j = 0; j < len; ++j) {
+            const int32_t cj = s_cnt[j];
+            rank += (cj > ci) | ((cj == ci) & (j < i));
+        }
+        row_perm[h * nQB + b0 + rank] = s_qb[i];
+    }
+}
+
+// ------------------------------------------------------------ sampling
+constexpr int kMaxSampleKB = 4096;
+constexpr int kWords = kMaxSampleKB / 32;
+
+__device__ __forceinline__ bool bit_get(const uint32_t* w, int32_t i) {
+    return (w[i >> 5] >> (i & 31)) & 1u;
+}
+__device__ __forceinline__ void bit_set(uint32_t* w, int32_t i) { w[i >> 5] |= 1u << (i & 31); }
+
+__global__ void __launch_bounds__(128) k_sample_blocks(
+    const float* __restrict__ scores, int64_t rows, int32_t nKB, const int32_t* __restrict__ exact_idx,
+    const int32_t* __restrict__ exact_cnt, int32_t exact_stride, int32_t m,
+    const double* __restrict__ u, int32_t* __restrict__ kv_idx, int32_t* __restrict__ kv_cnt,
+    float* __restrict__ log_w, int32_t max_kv, int32_t* status) {
+    const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (row >= rows) return;
+    const float* s = scores + row * (int64_t)nKB;
+    uint32_t ex[kWords], taken[kWords], drawn[kWords];  // exact / exact+promoted / drawn
+    const int32_t nw = (nKB + 31) >> 5;
+    for (int32_t w = 0; w < nw; ++w) ex[w] = taken[w] = drawn[w] = 0u;
+    const int32_t ec = exact_cnt[row];
+    for (int32_t e = 0; e < ec; ++e) {
+        const int32_t kb = exact_idx[row * (int64_t)exact_stride + e];
+        if (kb < 0 || kb >= nKB) {
+            raise_status(status, BSA_ERR_BOUNDS);
+            continue;
+        }
+        bit_set(ex, kb);
+        bit_set(taken, kb);
+    }
+    int32_t n_res = 0;
+    for (int32_t kb = 0; kb < nKB; ++kb) n_res += !bit_get(taken, kb);
+
+    double lambda = 0.0;
+    if (n_res <= m) {
+        for (int32_t w = 0; w < nw; ++w) taken[w] = 0xffffffffu;  // all residual blocks promoted
+    } else {
+        // eq. (4): cap at 1 and renormalise until the capped set is stable
+        int32_t n_cap = 0;
+        for (;;) {
+            double sum = 0.0;
+            for (int32_t kb = 0; kb < nKB; ++kb)
+                if (!bit_get(taken, kb)) sum = __dadd_rn(sum, (double)s[kb]);
+            lambda = __ddiv_rn((double)(m - n_cap), sum);
+            bool grew = false;
+            for (int32_t kb = 0; kb < nKB; ++kb) {
+                if (!bit_get(taken, kb) && __dmul_rn(lambda, (double)s[kb]) >= 1.0) {
+                    bit_set(taken, kb);
+                    ++n_cap;
+                    grew = true;
+                }
+            }
+            if (!grew) break;
+        }
+        // systematic PPS over the uncapped residual, ascending block order
+        const int32_t m_rest = m - n_cap;
+        const double ur = u[row];
+        double C = 0.0;
+        int32_t nd = 0;
+        for (int32_t kb = 0; kb < nKB; ++kb) {
+            if (bit_get(taken, kb)) continue;
+            const double pj = __dmul_rn(lambda, (double)s[kb]);
+            const double C_prev = C;
+            C = __dadd_rn(C, pj);
+            if (nd < m_rest && ceil(__dsub_rn(C, ur)) > ceil(__dsub_rn(C_prev, ur))) {
+                bit_set(drawn, kb);
+                ++nd;
+            }
+        }
+    }
+    int32_t n = 0, total = 0;
+    int32_t* out = kv_idx + row * (int64_t)max_kv;
+    float* lw = log_w + row * (int64_t)max_kv;
+    for (int32_t kb = 0; kb < nKB; ++kb) {
+        const bool t = bit_get(taken, kb), d = bit_get(drawn, kb);
+        if (!t && !d) continue;
+        if (n < max_kv) {
+            out[n] = kb;
+            lw[n] = d ? (float)(-log(__dmul_rn(lambda, (double)s[kb]))) : 0.0f;
+            ++n;
+        }
+        ++total;
+    }
+    for (int32_t e = n; e < max_kv; ++e) {
+        out[e] = -1;
+        lw[e] = 0.0f;
+    }
+    kv_cnt[row] = n;
+    if (total > max_kv) raise_status(status, BSA_ERR_OVERFLOW);
+    (void)ex;
+}
+
+}  // namespace
+
+cudaError_t launch_index_predicate(bsa_idx_mode mode, const void* src, int64_t rows, int32_t nKB,
+                                   float p, int32_t* kv_idx, int32_t* kv_cnt, int32_t max_kv,
+                                   int32_t* status, cudaStream_t stream) {
+    if (rows == 0) return cudaSuccess;
+    const int warps = 8;
+    const dim3 grid((unsigned)((rows + warps - 1) / warps));
+    if (mode == BSA_IDX_MASK_U8)
+        k_index_predicate<BSA_IDX_MASK_U8><<<grid, warps * 32, 0, stream>>>(src, rows, nKB, p, kv_idx,
+                                                                           kv_cnt, max_kv, status);
+    else
+        k_index_predicate<BSA_IDX_THRESHOLD_F32><<<grid, warps * 32, 0, stream>>>(
+            src, rows, nKB, p, kv_idx, kv_cnt, max_kv, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_index_topk(const float* scores, int64_t rows, int32_t nKB,
+                              const int32_t* k_per_row, int32_t k_const, int32_t* kv_idx,
+                              int32_t* kv_cnt, int32_t max_kv, int32_t* status,
+                              cudaStream_t stream) {
+    if (rows == 0) return cudaSuccess;
+    const int warps = 8;
+    const dim3 grid((unsigned)((rows + warps - 1) / warps));
+    k_index_topk<<<grid, warps * 32, 0, stream>>>(scores, rows, nKB, k_per_row, k_const, kv_idx,
+                                                  kv_cnt, max_kv, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reorder_rows(const int32_t* kv_cnt, const int32_t* order_in, int64_t heads,
+                                int32_t nQB, int32_t wave, int32_t* row_perm, int32_t* status,
+                                cudaStream_t stream) {
+    if (heads == 0) return cudaSuccess;
+    const int32_t w = wave < nQB ? wave : nQB;
+    const dim3 grid((unsigned)((nQB + w - 1) / w), (unsigned)heads);
+    const size_t smem = (size_t)2 * w * sizeof(int32_t);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k_reorder_rows,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    k_reorder_rows<<<grid, 256, smem, stream>>>(kv_cnt, order_in, nQB, w, row_perm, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
+                                 const int32_t* exact_idx, const int32_t* exact_cnt,
+                                 int32_t exact_stride, int32_t m, const double* u,
+                                 int32_t* kv_idx, int32_t* kv_cnt, float* log_w, int32_t max_kv,
+                                 int32_t* status, cudaStream_t stream) {
+    if (rows == 0) return cudaSuccess;
+    const dim3 grid((unsigned)((rows + 127) / 128));
+    k_sample_blocks<<<grid, 128, 0, stream>>>(scores, rows, nKB, exact_idx, exact_cnt, exact_stride,
+                                              m, u, kv_idx, kv_cnt, log_w, max_kv, status);
+    return cudaGetLastError();
+}
+
+}  // namespace bsa

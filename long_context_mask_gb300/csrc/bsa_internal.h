@@ -1,0 +1,55 @@
+// Internal declarations shared by the translation units of libbsa.so.
+// Host-side launchers; each takes the device address of the status word.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "bsa.h"
+
+namespace bsa {
+
+constexpr int kBlock = 128;  // query / key block edge
+
+// Status word helpers (defined in bsa_api.cu).
+int32_t* status_word_ptr();  // device address of the current device's status word
+
+// bsa_index.cu
+cudaError_t launch_index_predicate(bsa_idx_mode mode, const void* src, int64_t rows, int32_t nKB,
+                                   float p, int32_t* kv_idx, int32_t* kv_cnt, int32_t max_kv,
+                                   int32_t* status, cudaStream_t stream);
+cudaError_t launch_index_topk(const float* scores, int64_t rows, int32_t nKB,
+                              const int32_t* k_per_row, int32_t k_const, int32_t* kv_idx,
+                              int32_t* kv_cnt, int32_t max_kv, int32_t* status,
+                              cudaStream_t stream);
+cudaError_t launch_reorder_rows(const int32_t* kv_cnt, const int32_t* order_in, int64_t heads,
+                                int32_t nQB, int32_t wave, int32_t* row_perm, int32_t* status,
+                                cudaStream_t stream);
+cudaError_t launch_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
+                                 const int32_t* exact_idx, const int32_t* exact_cnt,
+                                 int32_t exact_stride, int32_t m, const double* u,
+                                 int32_t* kv_idx, int32_t* kv_cnt, float* log_w, int32_t max_kv,
+                                 int32_t* status, cudaStream_t stream);
+
+// bsa_attn.cu
+struct ForwardArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    int32_t B, H, N, D;
+    const int32_t* kv_idx;
+    const int32_t* kv_cnt;
+    int32_t max_kv;
+    const float* log_w;
+    const int32_t* q_map;
+    const int32_t* kv_map;
+    const int32_t* row_perm;
+    float scale;
+    void* o;
+    float* lse;
+};
+// Returns BSA_OK, BSA_ERR_CUDA (launch / descriptor failure) or BSA_ERR_UNSUPPORTED.
+bsa_status launch_forward(const ForwardArgs& a, int32_t* status, cudaStream_t stream);
+int32_t forward_resident_ctas(int32_t D);
+
+}  // namespace bsa

@@ -1,0 +1,100 @@
+"""The C-ABI library: it loads without a GPU, exports every symbol bsa.h
+declares, and rejects bad arguments on the host before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import long_context_mask_gb300 as bsa
+from long_context_mask_gb300 import build as bsa_build
+from long_context_mask_gb300.binding import EXPORTS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    bsa_build.build()
+    return bsa.load_library()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "bsa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"\b(bsa_[a-z_]+)\s*\(", src))
+
+
+def test_header_declarations_match_binding_exports():
+    assert _declared() == set(EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert lib.bsa_status_string(0) == b"BSA_OK"
+    assert lib.bsa_status_string(6) == b"BSA_ERR_BOUNDS"
+    assert lib.bsa_status_string(99) == b"BSA_ERR_UNKNOWN"
+
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: the calls below fail validation first
+FAKE_ODD = ctypes.c_void_p(0x10002)
+
+
+def _fwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, B=1, H=1, N=256, D=128, kv_idx=FAKE, kv_cnt=FAKE, max_kv=2,
+             log_w=None, q_map=None, kv_map=None, row_perm=None, scale=0.0, o=FAKE, lse=FAKE,
+             stream=None)
+    a.update(kw)
+    return lib.bsa_forward(*a.values())
+
+
+def test_forward_host_validation(lib):
+    assert _fwd(lib, D=96) == 2                    # unsupported head dim
+    assert _fwd(lib, N=200) == 1                   # not a multiple of 128
+    assert _fwd(lib, N=0) == 1
+    assert _fwd(lib, max_kv=3) == 1                # > nKB
+    assert _fwd(lib, max_kv=0) == 1
+    assert _fwd(lib, q=None) == 1                  # null required pointer
+    assert _fwd(lib, lse=None) == 1
+    assert _fwd(lib, k=FAKE_ODD) == 1              # 16-byte alignment
+    assert _fwd(lib, q_map=ctypes.c_void_p(0x10004)) == 1
+    assert _fwd(lib, B=70000, H=1) == 1            # grid limits
+    assert _fwd(lib, B=1, H=1, N=1 << 25) == 1
+
+
+def test_index_host_validation(lib):
+    f = lib.bsa_build_index
+    assert f(7, FAKE, 4, 8, 0.5, None, 1, FAKE, FAKE, 8, None) == 1     # bad mode
+    assert f(0, FAKE, 4, 8, 0.5, None, 1, FAKE, FAKE, 9, None) == 1     # max_kv > nKB
+    assert f(0, None, 4, 8, 0.5, None, 1, FAKE, FAKE, 8, None) == 1     # null src
+    assert f(1, FAKE_ODD, 4, 8, 0.5, None, 1, FAKE, FAKE, 8, None) == 1  # misaligned fp32 src
+    assert f(2, FAKE, 4, 8, 0.5, None, -1, FAKE, FAKE, 8, None) == 1    # negative k
+    assert f(0, None, 0, 8, 0.5, None, 1, None, None, 8, None) == 0     # empty: nothing to do
+
+
+def test_reorder_and_sample_host_validation(lib):
+    assert lib.bsa_reorder_rows(FAKE, None, 2, 16, 0, FAKE, None) == 1
+    assert lib.bsa_reorder_rows(FAKE, None, 2, 16, 9000, FAKE, None) == 1
+    assert lib.bsa_reorder_rows(None, None, 2, 16, 4, FAKE, None) == 1
+    assert lib.bsa_reorder_rows(None, None, 0, 16, 4, None, None) == 0
+    s = lib.bsa_sample_blocks
+    assert s(FAKE, 4, 5000, FAKE, FAKE, 1, 2, FAKE, FAKE, FAKE, FAKE, 4, None) == 1  # nKB > 4096
+    assert s(FAKE, 4, 16, FAKE, FAKE, 1, -1, FAKE, FAKE, FAKE, FAKE, 4, None) == 1   # m < 0
+    assert s(FAKE, 4, 16, FAKE, FAKE, 1, 2, ctypes.c_void_p(0x10004), FAKE, FAKE, FAKE, 4,
+             None) == 1                                                           # u not 8-aligned
+
+
+def test_device_status_rejects_null_output(lib):
+    assert lib.bsa_device_status(None, None) == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from long_context_mask_gb300 import binding
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="libbsa.so not found"):
+        binding.load_library()
