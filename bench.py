@@ -1,0 +1,456 @@
+#!/usr/bin/env python
+"""Benchmark: block-sparse attention forward on one GB300 (per rank).
+
+One step = one pass of the whole path over one synthetic workload resident
+in HBM: index-list construction (threshold map, mask or top-k scores, plus
+sampling where the workload has it) -> query-row reordering -> block-sparse
+attention forward.  The metric is effective TFLOP/s: 4 * 128 * 128 * D FLOPs
+per computed (query block, KV block) pair, divided by the step time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2]
+                    [--order reordered|identity] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (the reference arm of this comparison).  Under torchrun each rank
+runs its own copy of the workload on its own GPU (weak scaling); timing is
+the max over ranks.  One JSON line is printed by rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "block-sparse attn fwd effective TFLOP/s (% of GB300 BF16 TC peak); ms/call"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
+
+
+# ---------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("bsa_attn.cu", "bsa_ptx.cuh"):
+        with open(os.path.join(ROOT, "long_context_mask_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config_id):
+    """DRAM bytes per forward launch from a committed ncu capture, if it was
+    taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "forward_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"config{config_id}")
+    if not e or e.get("kernel_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the GPU is busy."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        busy = [s for s in sm if mx is None or s >= 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- the path
+class Path:
+    """Device buffers and the per-step launch sequence for one workload."""
+
+    def __init__(self, prob, dev, order: str):
+        import long_context_mask_gb300 as bsa
+        self.bsa = bsa
+        self.prob = prob
+        self.dev = dev
+        self.order = order
+        cu = lambda x: None if x is None else torch.from_numpy(np.ascontiguousarray(x)).to(dev)  # noqa: E731
+        self.q, self.k, self.v = (t.to(dev) for t in (prob.q, prob.k, prob.v))
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty(self.q.shape[:3], dtype=torch.float32, device=dev)
+        self.q_map, self.kv_map = cu(prob.q_map), cu(prob.kv_map)
+        rows, nqb = prob.rows, prob.nqb
+        self.heads = prob.B * prob.H
+        if prob.mask is not None:
+            self.mode, self.src, self.max_kv = bsa.IDX_MASK_U8, cu(prob.mask), nqb
+        elif prob.T is not None:
+            self.mode, self.src, self.max_kv = bsa.IDX_THRESHOLD_F32, cu(prob.T), nqb
+        elif prob.scores is not None:
+            self.mode, self.src = bsa.IDX_TOPK_F32, cu(prob.scores)
+            self.max_kv = int(prob.k_const if prob.k_per_row is None else prob.k_per_row.max())
+        else:
+            self.mode, self.src, self.max_kv = None, None, 1
+        self.k_per_row = cu(prob.k_per_row)
+        self.u = cu(prob.u)
+        self.idx = torch.empty((rows, self.max_kv), dtype=torch.int32, device=dev)
+        self.cnt = torch.empty(rows, dtype=torch.int32, device=dev)
+        if self.mode is None:  # one KV block per query block (Scatter / Gather layers)
+            self.idx.copy_(torch.arange(rows, device=dev, dtype=torch.int32).remainder(nqb)[:, None])
+            self.cnt.fill_(1)
+        self.lw = None
+        if prob.m_sample:
+            cap = self.max_kv + prob.m_sample
+            self.s_idx = torch.empty((rows, cap), dtype=torch.int32, device=dev)
+            self.s_cnt = torch.empty(rows, dtype=torch.int32, device=dev)
+            self.lw = torch.empty((rows, cap), dtype=torch.float32, device=dev)
+        self.row_perm = torch.empty((self.heads, nqb), dtype=torch.int32, device=dev)
+        self.wave = bsa.resident_ctas(prob.D)
+        self.launches_per_step = 1 + (self.mode is not None) + bool(prob.m_sample) + (order == "reordered")
+
+    def lists(self):
+        return (self.s_idx, self.s_cnt) if self.prob.m_sample else (self.idx, self.cnt)
+
+    def build_lists(self):
+        bsa, p = self.bsa, self.prob
+        if self.mode is not None:
+            bsa.build_index(self.mode, self.src, self.idx, self.cnt, p=p.p or 0.0,
+                            k_per_row=self.k_per_row, k_const=p.k_const or 0)
+        if p.m_sample:
+            bsa.sample_blocks(self.src, self.idx, self.cnt, p.m_sample, self.u, self.s_idx,
+                              self.s_cnt, self.lw)
+        if self.order == "reordered":
+            _, cnt = self.lists()
+            bsa.reorder_rows(cnt.reshape(self.heads, p.nqb), self.wave, self.row_perm)
+
+    def attend(self):
+        idx, cnt = self.lists()
+        self.bsa.forward(self.q, self.k, self.v, idx, cnt, self.o, self.lse, log_w=self.lw,
+                         q_map=self.q_map, kv_map=self.kv_map,
+                         row_perm=self.row_perm if self.order == "reordered" else None)
+
+    def step(self):
+        self.build_lists()
+        self.attend()
+
+    def effective_flops(self):
+        _, cnt = self.lists()
+        return self.bsa.effective_flops(cnt, self.prob.D)
+
+
+def make_problem(config: int, heads: int | None):
+    kw = {} if heads is None else {"H": heads}
+    return synth.CONFIGS[config](**kw)
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def time_oracle(prob, lists, budget_s: float, max_blocks: int | None = None, seed: int = 0):
+    """Oracle on a bounded sample of query blocks (spread over heads, seeded).
+    Returns (effective TFLOP/s, seconds, blocks, threads)."""
+    import oracle
+    idx, cnt, lw = lists
+    g = np.random.default_rng(seed)
+    order = g.permutation(prob.rows)
+    done, fl, t_total = 0, 0.0, 0.0
+    chunk = 8
+    while done < len(order):
+        sel = order[done:done + chunk]
+        t0 = time.perf_counter()
+        oracle.attention(prob.q, prob.k, prob.v, idx, cnt, log_w=lw, q_map=prob.q_map,
+                         kv_map=prob.kv_map, sel=sel)
+        t_total += time.perf_counter() - t0
+        fl += float(cnt[sel].sum()) * 4 * 128 * 128 * prob.D
+        done += len(sel)
+        if t_total >= budget_s or (max_blocks and done >= max_blocks):
+            break
+    return fl / t_total / 1e12, t_total, done, oracle.num_threads()
+
+
+def host_lists(prob):
+    """Index lists for the oracle, from the oracle (reference arm / CPU leg only)."""
+    import oracle
+    if prob.diag_list:
+        idx, cnt = synth.diag_lists(prob.rows, prob.nqb)
+        return idx, cnt, None
+    if prob.mask is not None:
+        idx, cnt, _ = oracle.index_mask(prob.mask)
+    elif prob.T is not None:
+        idx, cnt, _ = oracle.index_threshold(prob.T, prob.p)
+    else:
+        k = prob.k_per_row if prob.k_per_row is not None else prob.k_const
+        idx, cnt, _ = oracle.index_topk(prob.scores, k)
+    if prob.m_sample:
+        idx, cnt, lw, _ = oracle.sample_blocks(prob.scores, idx, cnt, prob.m_sample, prob.u,
+                                               idx.shape[1] + prob.m_sample)
+        return idx, cnt, lw
+    return idx, cnt, None
+
+
+# ---------------------------------------------------------------- main
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--heads", type=int, default=None, help="override H (smaller profiling case)")
+    ap.add_argument("--order", default="reordered", choices=["reordered", "identity"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle CPU time")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-once", action="store_true",
+                    help="build inputs, run one step, exit (for ncu captures)")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, dev) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def config_dict(prob, config, order, density, world):
+    return {"workload": synth.CONFIG_NAMES[config], "config_id": config, "B": prob.B, "H": prob.H,
+            "N": prob.N, "D": prob.D, "block": 128, "density": round(density, 4), "order": order,
+            "l2": "flushed between timed steps (256 MiB write)",
+            "parallelism": "one independent workload per GPU" if world > 1 else "single GPU"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    prob = make_problem(args.config, args.heads)
+    lists = host_lists(prob)
+    density = float(lists[1].sum()) / (prob.rows * prob.nqb)
+    # each step: the oracle on a bounded sample (about 1 s of CPU work)
+    budget = 1.0
+    for _ in range(args.warmup):
+        time_oracle(prob, lists, budget / 4, seed=1)
+    vals, secs, blocks = [], 0.0, 0
+    for k in range(args.steps):
+        v, s, b, threads = time_oracle(prob, lists, budget, seed=100 + k)
+        vals.append(v)
+        secs += s
+        blocks += b
+    value = statistics.median(vals)
+    ms = secs / args.steps * 1e3
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": config_dict(prob, args.config, args.order, density, 1),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{blocks} query blocks over {args.steps} steps "
+                                       f"(~{budget:.0f} s of oracle CPU time per step)"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py --impl ours needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    import long_context_mask_gb300 as bsa
+
+    prob = make_problem(args.config, args.heads)
+    path = Path(prob, dev, args.order)
+    path.step()
+    torch.cuda.synchronize()
+    if args.profile_once:
+        st = bsa.device_status()
+        print(json.dumps({"profile_once": True, "status": st}))
+        return
+
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(args.warmup, 3)):
+        path.step()
+    torch.cuda.synchronize()
+    flops = path.effective_flops()
+    density = float(path.lists()[1].sum()) / (prob.rows * prob.nqb)
+
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    gpu_id = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    fwd_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with ClockSampler(gpu_id) as clk:
+        # ---- timed region: K steps (L2 flushed before each, outside the events)
+        barrier(world)
+        torch.cuda.synchronize()
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            path.step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        step_ms = [a.elapsed_time(b) for a, b in ev]
+        # ---- the dominant kernel alone (same inputs, L2 flushed before each launch)
+        path.build_lists()
+        for i in range(K):
+            flush.zero_()
+            fwd_ev[i][0].record(stream)
+            path.attend()
+            fwd_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        fwd_ms = [a.elapsed_time(b) for a, b in fwd_ev]
+    status = bsa.device_status()
+    if status != 0:
+        raise SystemExit(f"device status {status} after the timed region")
+
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    ms_per_step = total_ms / K
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end: host (pinned) inputs -> device -> path -> host outputs
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    d_in = [t for t in (path.q, path.k, path.v, path.src, path.q_map, path.kv_map, path.k_per_row,
+                        path.u) if t is not None]
+    h_in = [pin(t) for t in d_in]
+    h_o, h_l = torch.empty_like(path.o, device="cpu").pin_memory(), torch.empty_like(path.lse, device="cpu").pin_memory()
+    bi = sum(t.numel() * t.element_size() for t in h_in)
+    bo = h_o.numel() * h_o.element_size() + h_l.numel() * h_l.element_size()
+    E = max(3, K // 4)
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e_start.record(stream)
+    for _ in range(E):
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        path.step()
+        h_o.copy_(path.o, non_blocking=True)
+        h_l.copy_(path.lse, non_blocking=True)
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / E, world, dev)
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    fwd_avg_ms = sum(fwd_ms) / len(fwd_ms)
+    achieved = flops / (fwd_avg_ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    traffic = recorded_traffic(args.config)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic, "kernel": "k_bsa_forward",
+                "peak_source": f"{peak_src} bf16 burst", "ms_per_launch": fwd_avg_ms,
+                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak))}
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, s, b, threads = time_oracle(prob, host_lists(prob), args.cpu_budget)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{b} of {prob.rows} query blocks (seeded), {s:.1f} s fp64 on host cores"}
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
+            "ms_per_step_median": statistics.median(step_ms) if world == 1 else None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": config_dict(prob, args.config, args.order, density, world),
+            "pct_of_peak": 100.0 * value / world / peak,
+            "roofline": roofline, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
+                    "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms},
+            "gpu_launches": K * path.launches_per_step,
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -23,4 +23,6 @@ from .binding import (  # noqa: F401
     reorder_rows,
     resident_ctas,
     sample_blocks,
+    selftest_exp2,
+    selftest_wait_timeout,
 )

@@ -21,7 +21,8 @@ STATUS_NAMES = {0: "BSA_OK", 1: "BSA_ERR_INVALID_ARG", 2: "BSA_ERR_UNSUPPORTED",
                 6: "BSA_ERR_BOUNDS"}
 
 EXPORTS = ("bsa_build_index", "bsa_reorder_rows", "bsa_sample_blocks", "bsa_forward",
-           "bsa_device_status", "bsa_resident_ctas", "bsa_status_string")
+           "bsa_device_status", "bsa_resident_ctas", "bsa_status_string", "bsa_selftest_exp2",
+           "bsa_selftest_wait_timeout")
 
 
 class BsaError(RuntimeError):
@@ -54,8 +55,11 @@ def load_library():
     lib.bsa_resident_ctas.argtypes = [i32]
     lib.bsa_status_string.argtypes = [i32]
     lib.bsa_status_string.restype = ctypes.c_char_p
+    lib.bsa_selftest_exp2.argtypes = [P, P, P, P, i64, P]
+    lib.bsa_selftest_wait_timeout.argtypes = [i64, P]
     for name in ("bsa_build_index", "bsa_reorder_rows", "bsa_sample_blocks", "bsa_forward",
-                 "bsa_device_status", "bsa_resident_ctas"):
+                 "bsa_device_status", "bsa_resident_ctas", "bsa_selftest_exp2",
+                 "bsa_selftest_wait_timeout"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -152,6 +156,22 @@ def device_status(stream=None) -> int:
     return out.value
 
 
+def selftest_exp2(x, *, stream=None):
+    """(y_fma, y_mufu, y_ref) = the three device 2^x of bsa_selftest.h for fp32 x."""
+    import torch
+    _dtype(x, "x", torch.float32)
+    outs = [torch.empty_like(x) for _ in range(3)]
+    _check("bsa_selftest_exp2", load_library().bsa_selftest_exp2(
+        _ptr(x), *(_ptr(o) for o in outs), x.numel(), _stream(stream)))
+    return tuple(outs)
+
+
+def selftest_wait_timeout(limit_ns: int, *, stream=None):
+    """Launch the bounded-wait self-test (records BSA_ERR_TIMEOUT on expiry)."""
+    _check("bsa_selftest_wait_timeout",
+           load_library().bsa_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
 def resident_ctas(D: int) -> int:
     n = load_library().bsa_resident_ctas(int(D))
     if n <= 0:
@@ -174,4 +194,4 @@ def dense_attention_flops(N: int, H: int, D: int, causal: bool = False, B: int =
 __all__ = ["BLOCK", "BsaError", "IDX_MASK_U8", "IDX_THRESHOLD_F32", "IDX_TOPK_F32", "build_index",
            "reorder_rows", "sample_blocks", "forward", "device_status", "resident_ctas",
            "effective_flops", "dense_attention_flops", "load_library", "lib_path", "EXPORTS",
-           "math"]
+           "selftest_exp2", "selftest_wait_timeout", "math"]

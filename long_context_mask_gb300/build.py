@@ -18,8 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbsa.so")
-SOURCES = ["bsa_api.cu", "bsa_index.cu", "bsa_attn.cu"]
-HEADERS = ["bsa_internal.h", "bsa_ptx.cuh"]
+SOURCES = ["bsa_api.cu", "bsa_index.cu", "bsa_attn.cu", "bsa_selftest.cu"]
+HEADERS = ["bsa_internal.h", "bsa_ptx.cuh", "bsa_math.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -42,7 +42,7 @@ def _stale(out: str, deps) -> bool:
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     os.makedirs(BUILD, exist_ok=True)
-    headers = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "bsa.h")]
+    headers = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, h) for h in ("bsa.h", "bsa_selftest.h")]
     jobs = []
     objs = []
     for s in SOURCES:

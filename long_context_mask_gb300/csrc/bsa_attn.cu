@@ -6,24 +6,35 @@
 // its list, each block's scores shifted by the block's log-weight, and
 // O = P V / l, LSE = ln l + max, written back through the query map.
 //
-// One thread block owns one (head, query block) work item; blockIdx.x is the
-// execution slot within the head (query block row_perm[head][slot]) and
-// blockIdx.y the head, so blocks are issued head-major in slot order (the
-// sequential-head, wave-ordered schedule of WaveAlign section V).
+// Work mapping.  One thread block owns one (head, query block) work item;
+// blockIdx.x is the execution slot within the head (query block
+// row_perm[head][slot]) and blockIdx.y the head, so blocks are issued
+// head-major in slot order: the sequential-head, wave-ordered schedule of
+// WaveAlign section V.
 //
 // Warp roles (6 warps):
 //   warp 0      TMA producer: Q once, then K_j and V_j of every listed block
 //               into a ring of kStages shared-memory slots (tile loads, or
-//               tile::gather4 row gathers when index maps are given).
-//   warp 1      allocates tensor memory; one lane issues tcgen05.mma:
-//               S_j = Q K_j^T into one of two TMEM score buffers, and
-//               O += P_{j-1} V_{j-1} with P read from TMEM.
+//               tile::gather4 row gathers when index maps are given).  The
+//               list is read 32 entries at a time by the whole warp.
+//   warp 1      allocates tensor memory; one lane issues tcgen05.mma in the
+//               order QK(0), QK(1), QK(2), then for i = 0..n-1: PV(i),
+//               QK(i+3): S_j = Q K_j^T into TMEM score buffer j % 3 (QK runs
+//               up to three blocks ahead of the softmax), O += P_i V_i with P
+//               read from TMEM.  This lane touches no global memory; it waits
+//               only for P_i and for data, and keeps the tensor core's
+//               instruction queue fed.
 //   warps 2..5  softmax: one thread per query row (TMEM lane); reads S_j,
-//               updates the running max / sum, writes P_j (bf16) back over
-//               S_j, rescales O in TMEM when the max grows by more than
-//               2^8, and runs the epilogue (O / l -> bf16, LSE).
+//               updates the running max (log2 domain) and sum, rescales O in
+//               TMEM when the max grows by more than 2^8, writes P_j (bf16)
+//               over S_j, and runs the epilogue (O / l -> bf16 through the
+//               query map, LSE).
 //
-// Tensor memory (512 columns): S0 = [0,128), S1 = [128,256), O = [256,256+D).
+// The producer loads K/V tiles in exactly the MMA's consumption order
+// (K_0, K_1, K_2, then V_i, K_{i+3}), so the ring is a plain FIFO.
+//
+// Tensor memory (512 columns): S_0, S_1, S_2 = [0,384) in 128-column
+// buffers, O = [384, 384+D).
 // Shared memory: Q tile + kStages K/V tiles, each tile stored as D/64 boxes
 // of 128 rows x 128 bytes with the 128-byte swizzle (canonical K-major
 // layout for Q and K, MN-major for V).
@@ -40,11 +51,13 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
 
 #include "bsa_internal.h"
+#include "bsa_math.cuh"
 #include "bsa_ptx.cuh"
 
 namespace bsa {
@@ -55,17 +68,22 @@ using namespace ptx;
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kDefaultPoly = 0;            // exponentials per 8 on the FMA pipe
 constexpr float kRescaleThreshold = 8.0f;  // rescale O only when the max grows by > 2^8
+constexpr int kProducerWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kFirstSoftmaxWarp = 2;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kColO = 384;
+constexpr int kSBuf = 3;  // TMEM score buffers
 
 template <int D>
 struct Cfg {
     static constexpr int kBoxBytes = 128 * 128;  // 128 rows x 64 bf16
     static constexpr int kBoxes = D / 64;
     static constexpr int kTile = kBoxBytes * kBoxes;
-    static constexpr int kStages = D == 128 ? 5 : 10;
+    static constexpr int kStages = D == 128 ? 6 : 12;
     static constexpr int kData = kTile * (1 + kStages);
     static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);
     static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 0, 1);
@@ -75,9 +93,10 @@ struct Barriers {
     uint64_t full[16];
     uint64_t empty[16];
     uint64_t q_full;
-    uint64_t s_full[2];
-    uint64_t p_full[2];
-    uint64_t o_done;
+    uint64_t s_full[kSBuf];
+    uint64_t p_full[kSBuf];
+    uint64_t o_done[2];  // PV_i commits o_done[i % 2]
+    uint64_t o_final;    // after the last PV
     uint64_t mma_done;
     uint32_t tmem_base;
     int32_t abort;
@@ -103,18 +122,11 @@ __device__ __forceinline__ void raise_status(int32_t* status, int32_t code) {
     atomicCAS(status, 0, code);
 }
 
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Shared (warp-uniform) abort check.
 __device__ __forceinline__ bool aborted(const Barriers* b) {
     return *reinterpret_cast<const volatile int32_t*>(&b->abort) != 0;
 }
@@ -160,7 +172,7 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* tile_
     }
 }
 
-template <int D>
+template <int D, int kPoly>
 __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_constant__ Params P) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -187,14 +199,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
         }
     }
     const int64_t row = bh * nQB + qb;
-    int32_t cnt = P.kv_cnt[row];
-    if (cnt > max_kv) {
+    int32_t n = P.kv_cnt[row];
+    if (n > max_kv) {
         if (threadIdx.x == 0) raise_status(P.status, BSA_ERR_OVERFLOW);
-        cnt = max_kv;
+        n = max_kv;
     }
-    if (cnt < 0) {
+    if (n < 0) {
         if (threadIdx.x == 0) raise_status(P.status, BSA_ERR_BOUNDS);
-        cnt = 0;
+        n = 0;
     }
     const int32_t* list = P.kv_idx + row * max_kv;
 
@@ -204,20 +216,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
             mbar_init(smem_u32(&bars->empty[s]), 1);
         }
         mbar_init(smem_u32(&bars->q_full), 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kSBuf; ++s) {
             mbar_init(smem_u32(&bars->s_full[s]), 1);
             mbar_init(smem_u32(&bars->p_full[s]), 128);
         }
-        mbar_init(smem_u32(&bars->o_done), 1);
+        mbar_init(smem_u32(&bars->o_done[0]), 1);
+        mbar_init(smem_u32(&bars->o_done[1]), 1);
+        mbar_init(smem_u32(&bars->o_final), 1);
         mbar_init(smem_u32(&bars->mma_done), 1);
         bars->abort = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 0 && lane == 0) {
+    if (warp == kProducerWarp && lane == 0) {
         prefetch_tensormap(P.kv_map ? &P.gmap_k : &P.map_k);
         prefetch_tensormap(P.kv_map ? &P.gmap_v : &P.map_v);
     }
@@ -226,40 +240,57 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == 0) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
         int32_t issued = 0;
         if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bars->q_full), C::kTile);
         __syncwarp();
         load_tile<D>(s_q, &P.map_q, &P.gmap_q, P.q_map, bh, N, qb, smem_u32(&bars->q_full), lane,
                      P.status);
-        for (int32_t e = 0; e < cnt; ++e) {
-            const int32_t kb = list[e];
-            if (kb < 0 || kb >= nKB) {
-                if (lane == 0) raise_status(P.status, BSA_ERR_BOUNDS);
-                continue;
-            }
-#pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                const int32_t slot = issued % C::kStages;
-                const uint32_t phase = (uint32_t)(issued / C::kStages) & 1u;
-                int ok = 1;
-                if (lane == 0) ok = mbar_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok || aborted(bars)) {
-                    if (lane == 0) set_abort(bars, P.status);
-                    goto producer_done;
+        // Load order = MMA consumption order: K_0, K_1, K_2, then V_i, K_{i+3}.
+        // Tile t of that sequence is V_i for t = 3 + 2i (i < n - 3) etc.; it is
+        // generated below as (block, is_v) pairs.  The list is read 32 entries
+        // at a time with one coalesced load and broadcast by shuffles.
+        bool ok = true;
+        int32_t chunk_base = -64, kb_lane = 0;
+        auto block_kb = [&](int32_t e) -> int32_t {
+            if (e - chunk_base >= 32 || e < chunk_base) {
+                chunk_base = e & ~31;
+                kb_lane = chunk_base + lane < n ? list[chunk_base + lane] : 0;
+                if (kb_lane < 0 || kb_lane >= nKB) {
+                    raise_status(P.status, BSA_ERR_BOUNDS);
+                    kb_lane = 0;  // keeps the pipeline in step; this row's result is unspecified
                 }
-                const uint32_t fb = smem_u32(&bars->full[slot]);
-                if (lane == 0) mbar_arrive_expect_tx(fb, C::kTile);
-                __syncwarp();
-                load_tile<D>(s_ring + slot * C::kTile, which ? &P.map_v : &P.map_k,
-                             which ? &P.gmap_v : &P.gmap_k, P.kv_map, bh, N, kb, fb, lane,
-                             P.status);
-                ++issued;
             }
+            return __shfl_sync(0xffffffffu, kb_lane, e - chunk_base);
+        };
+        auto put = [&](int32_t e, bool is_v) -> bool {
+            const int32_t kb = block_kb(e);
+            const int32_t slot = issued % C::kStages;
+            const uint32_t phase = (uint32_t)(issued / C::kStages) & 1u;
+            int w = 1;
+            if (lane == 0) w = mbar_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+            w = __shfl_sync(0xffffffffu, w, 0);
+            if (!w || aborted(bars)) {
+                if (lane == 0) set_abort(bars, P.status);
+                return false;
+            }
+            const uint32_t fb = smem_u32(&bars->full[slot]);
+            if (lane == 0) mbar_arrive_expect_tx(fb, C::kTile);
+            __syncwarp();
+            load_tile<D>(s_ring + slot * C::kTile, is_v ? &P.map_v : &P.map_k,
+                         is_v ? &P.gmap_v : &P.gmap_k, P.kv_map, bh, N, kb, fb, lane, P.status);
+            ++issued;
+            return true;
+        };
+        // K blocks are fetched in increasing order (lookahead 3), V blocks trail;
+        // both read the list through the same 32-entry window when close enough,
+        // so block_kb may refetch a chunk when the two cross a chunk boundary.
+        for (int32_t e = 0; ok && e < n && e < kSBuf; ++e) ok = put(e, false);
+        for (int32_t i = 0; ok && i < n; ++i) {
+            ok = put(i, true);
+            if (ok && i + kSBuf < n) ok = put(i + kSBuf, false);
         }
-    producer_done:
         // Drain: every issued copy must land before the block exits.
         if (lane == 0) {
             if (!mbar_wait(smem_u32(&bars->q_full), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT)) raise_status(P.status, BSA_ERR_TIMEOUT);
@@ -268,60 +299,55 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
                 if (!mbar_wait(smem_u32(&bars->full[i % C::kStages]), (uint32_t)(i / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT))
                     raise_status(P.status, BSA_ERR_TIMEOUT);
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int32_t j = 0;
+            // descriptors of the K-major Q tile and of ring slot 0; a slot / k-step
+            // offset is added to the start-address field (bits 0..13, 16-byte units)
+            const uint64_t dq = smem_desc_sw128(s_q, 16, 1024);
+            const uint64_t dk = smem_desc_sw128(s_ring, 16, 1024);
+            const uint64_t dv = smem_desc_sw128(s_ring, C::kBoxBytes, 1024);
             bool ok = mbar_wait(smem_u32(&bars->q_full), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT);
             tc_fence_after();
-            auto issue_pv = [&](int32_t i) -> bool {
-                if (!mbar_wait(smem_u32(&bars->p_full[i & 1]), (uint32_t)(i >> 1) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT)) return false;
-                const int32_t item = 2 * i + 1;
+            int32_t item = 0;  // ring position of the next tile (same order as the producer)
+            auto issue_qk = [&](int32_t j) -> bool {
                 const int32_t slot = item % C::kStages;
                 if (!mbar_wait(smem_u32(&bars->full[slot]), (uint32_t)(item / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT)) return false;
                 tc_fence_after();
-                const uint32_t sv = s_ring + slot * C::kTile;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t bdesc = smem_desc_sw128(sv + kk * 2048, C::kBoxBytes, 1024);
-                    mma_ts(tmem + kColO, tmem + (uint32_t)(i & 1) * 128u + kk * 8, bdesc, C::kIdescPV,
-                           (i > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(smem_u32(&bars->empty[slot]));
-                mma_commit(smem_u32(&bars->o_done));
-                return true;
-            };
-            for (int32_t e = 0; ok && e < cnt; ++e) {
-                const int32_t kb = list[e];
-                if (kb < 0 || kb >= nKB) continue;
-                if (aborted(bars)) {
-                    ok = false;
-                    break;
-                }
-                const int32_t item = 2 * j;
-                const int32_t slot = item % C::kStages;
-                if (!mbar_wait(smem_u32(&bars->full[slot]), (uint32_t)(item / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t sk = s_ring + slot * C::kTile;
+                const uint64_t ks = dk + (uint64_t)((slot * C::kTile) >> 4);
+                const uint32_t d_col = (uint32_t)(j % kSBuf) * 128u;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-                    const uint64_t adesc = smem_desc_sw128(s_q + off, 16, 1024);
-                    const uint64_t bdesc = smem_desc_sw128(sk + off, 16, 1024);
-                    mma_ss(tmem + (uint32_t)(j & 1) * 128u, adesc, bdesc, C::kIdescQK, kk > 0 ? 1u : 0u);
+                    const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+                    mma_ss(tmem + d_col, dq + off, ks + off, C::kIdescQK, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(smem_u32(&bars->empty[slot]));
-                mma_commit(smem_u32(&bars->s_full[j & 1]));
-                if (j > 0 && !issue_pv(j - 1)) {
-                    ok = false;
-                    break;
-                }
-                ++j;
+                mma_commit(smem_u32(&bars->s_full[j % kSBuf]));
+                ++item;
+                return true;
+            };
+            for (int32_t j = 0; ok && j < n && j < kSBuf; ++j) ok = issue_qk(j);
+            for (int32_t i = 0; ok && i < n; ++i) {
+                // O += P_i V_i once the softmax has written P_i (and rescaled O)
+                ok = mbar_wait(smem_u32(&bars->p_full[i % kSBuf]), (uint32_t)(i / kSBuf) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                if (!ok) break;
+                const int32_t slot = item % C::kStages;
+                ok = mbar_wait(smem_u32(&bars->full[slot]), (uint32_t)(item / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t vs = dv + (uint64_t)((slot * C::kTile) >> 4);
+                const uint32_t p_col = (uint32_t)(i % kSBuf) * 128u;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tmem + kColO, tmem + p_col + kk * 8, vs + (uint64_t)(kk * 2048 >> 4),
+                           C::kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(smem_u32(&bars->empty[slot]));
+                mma_commit(smem_u32(&bars->o_done[i & 1]));
+                if (i + 1 == n) mma_commit(smem_u32(&bars->o_final));
+                ++item;
+                // S buffer i % 3 is free again once PV_i (issued above) has read P_i
+                if (i + kSBuf < n) ok = issue_qk(i + kSBuf);
             }
-            if (ok && j > 0 && !aborted(bars)) ok = issue_pv(j - 1);
             if (!ok) set_abort(bars, P.status);
             // Drain: nothing of ours may still be running when TMEM is freed.
             mma_commit(smem_u32(&bars->mma_done));
@@ -344,15 +370,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
             }
         }
         const float sl2 = P.scale_log2;
+        const float* lw_row = P.log_w ? P.log_w + row * max_kv : nullptr;
         float m = -INFINITY, l = 0.0f;
-        int32_t j = 0;
         bool ok = true;
-        for (int32_t e = 0; e < cnt; ++e) {
-            const int32_t kb = list[e];
-            if (kb < 0 || kb >= nKB) continue;
-            const float lw2 = P.log_w ? P.log_w[row * max_kv + e] * kLog2e : 0.0f;
-            const uint32_t sbuf = (uint32_t)(j & 1) * 128u;
-            bool w = mbar_wait(smem_u32(&bars->s_full[j & 1]), (uint32_t)(j >> 1) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+        float lw_next = (lw_row && n > 0) ? lw_row[0] : 0.0f;
+        for (int32_t j = 0; j < n; ++j) {
+            const float lw2 = lw_next * kLog2e;
+            lw_next = (lw_row && j + 1 < n) ? lw_row[j + 1] : 0.0f;
+            const uint32_t sbuf = (uint32_t)(j % kSBuf) * 128u;
+            bool w = mbar_wait(smem_u32(&bars->s_full[j % kSBuf]), (uint32_t)(j / kSBuf) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
             if (__any_sync(0xffffffffu, !w || aborted(bars))) {
                 ok = false;
                 break;
@@ -374,15 +400,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
                 mx3 = fmaxf(mx3, __uint_as_float(s[c + 3]));
             }
             const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2 + lw2;
+            // warp-uniform: the tcgen05 loads/stores of the rescale are warp-wide
+            const bool rescale = j > 0 && __any_sync(0xffffffffu, mt > m + kRescaleThreshold);
+            float alpha = 1.0f;
             if (j == 0) {
                 m = mt;
-            } else if (__any_sync(0xffffffffu, mt > m + kRescaleThreshold)) {
+            } else if (rescale) {
                 const float m_new = fmaxf(m, mt);
-                const float alpha = ex2(m - m_new);
+                alpha = ex2(m - m_new);
                 l *= alpha;
                 m = m_new;
-                // O holds P_0..P_{j-2} V: wait for P_{j-1} V_{j-1} before touching it.
-                w = mbar_wait(smem_u32(&bars->o_done), (uint32_t)(j - 1) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+            }
+            const float bias = lw2 - m;
+            float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+            for (int c = 0; c < 128; c += 4) {
+                const float x0 = fmaf(__uint_as_float(s[c + 0]), sl2, bias);
+                const float x1 = fmaf(__uint_as_float(s[c + 1]), sl2, bias);
+                const float x2 = fmaf(__uint_as_float(s[c + 2]), sl2, bias);
+                const float x3 = fmaf(__uint_as_float(s[c + 3]), sl2, bias);
+                const float p0 = ((c + 0) % 8) < kPoly ? exp2_fma(x0) : ex2(x0);
+                const float p1 = ((c + 1) % 8) < kPoly ? exp2_fma(x1) : ex2(x1);
+                const float p2 = ((c + 2) % 8) < kPoly ? exp2_fma(x2) : ex2(x2);
+                const float p3 = ((c + 3) % 8) < kPoly ? exp2_fma(x3) : ex2(x3);
+                l0 += p0;
+                l1 += p1;
+                l2 += p2;
+                l3 += p3;
+                s[c / 2] = pack_bf16(p0, p1);
+                s[c / 2 + 1] = pack_bf16(p2, p3);
+            }
+            l += (l0 + l1) + (l2 + l3);
+            tmem_st32(t_lane + sbuf + 0, &s[0]);
+            tmem_st32(t_lane + sbuf + 32, &s[32]);
+            if (rescale) {
+                // O must hold P_0..P_{j-1} V: wait for PV_{j-1}.  S_j complete
+                // implies PV_{j-3} complete (QK_j was issued after it), so the
+                // parity wait on o_done[(j-1) % 2] is unambiguous.
+                w = mbar_wait(smem_u32(&bars->o_done[(j - 1) & 1]), (uint32_t)((j - 1) >> 1) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
                 if (__any_sync(0xffffffffu, !w)) {
                     ok = false;
                     break;
@@ -398,50 +453,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
                     tmem_st32(t_lane + kColO + c, o);
                 }
             }
-            const float bias = lw2 - m;
-            float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-#pragma unroll
-            for (int c = 0; c < 128; c += 4) {
-                const float p0 = ex2(fmaf(__uint_as_float(s[c + 0]), sl2, bias));
-                const float p1 = ex2(fmaf(__uint_as_float(s[c + 1]), sl2, bias));
-                const float p2 = ex2(fmaf(__uint_as_float(s[c + 2]), sl2, bias));
-                const float p3 = ex2(fmaf(__uint_as_float(s[c + 3]), sl2, bias));
-                l0 += p0;
-                l1 += p1;
-                l2 += p2;
-                l3 += p3;
-                s[c / 2] = pack_bf16(p0, p1);
-                s[c / 2 + 1] = pack_bf16(p2, p3);
-            }
-            l += (l0 + l1) + (l2 + l3);
-            tmem_st32(t_lane + sbuf + 0, &s[0]);
-            tmem_st32(t_lane + sbuf + 32, &s[32]);
             tmem_wait_st();
-            if (j > 0) {
-                // keeps this thread at most one O phase behind (unambiguous parity waits)
-                w = mbar_wait(smem_u32(&bars->o_done), (uint32_t)(j - 1) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
-                if (__any_sync(0xffffffffu, !w)) {
-                    ok = false;
-                    break;
-                }
-            }
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars->p_full[j & 1]));
-            ++j;
+            mbar_arrive(smem_u32(&bars->p_full[j % kSBuf]));
         }
         if (!ok) {
             if (lane == 0) set_abort(bars, P.status);
         } else {
             __nv_bfloat16* orow = P.o + (bh * N + tok) * D;
-            if (j == 0) {
+            if (n == 0) {
                 if (tok_ok) {
-                    uint4 z = make_uint4(0, 0, 0, 0);
+                    const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
                     for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(orow + c) = z;
                     P.lse[bh * N + tok] = -INFINITY;
                 }
             } else {
-                const bool w = mbar_wait(smem_u32(&bars->o_done), (uint32_t)(j - 1) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                const bool w = mbar_wait(smem_u32(&bars->o_final), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT);
                 if (__any_sync(0xffffffffu, !w)) {
                     if (lane == 0) set_abort(bars, P.status);
                 } else {
@@ -473,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ------------------------------------------------------------------ host side
@@ -509,7 +537,7 @@ size_t smem_bytes() {
     return 1024 + Cfg<D>::kData + sizeof(Barriers);
 }
 
-template <int D>
+template <int D, int kPoly>
 cudaError_t prepare_kernel() {
     // Per device: opt in to the large dynamic shared-memory carve-out.
     static int done[64] = {0};
@@ -517,15 +545,33 @@ cudaError_t prepare_kernel() {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(k_bsa_forward<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k_bsa_forward<D, kPoly>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem_bytes<D>());
     if (e == cudaSuccess && dev < 64) done[dev] = 1;
     return e;
 }
 
+// Share of exponentials (out of every 8) computed by exp2_fma instead of
+// the MUFU unit.  BSA_EXP2_POLY=<0|2|3|4> overrides it (tuning).
+int poly_setting() {
+    static int v = -1;
+    if (v < 0) {
+        const char* s = getenv("BSA_EXP2_POLY");
+        v = kDefaultPoly;
+        if (s && (s[0] == '0' || s[0] == '2' || s[0] == '3' || s[0] == '4') && s[1] == 0) v = s[0] - '0';
+    }
+    return v;
+}
+
+template <int D, int kPoly>
+bsa_status launch_dp(const Params& P, unsigned grid_x, unsigned grid_y, cudaStream_t stream) {
+    if (prepare_kernel<D, kPoly>() != cudaSuccess) return BSA_ERR_CUDA;
+    k_bsa_forward<D, kPoly><<<dim3(grid_x, grid_y), kThreads, smem_bytes<D>(), stream>>>(P);
+    return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
 template <int D>
 bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) {
-    if (prepare_kernel<D>() != cudaSuccess) return BSA_ERR_CUDA;
     Params P;
     memset(&P, 0, sizeof(P));
     const uint64_t rows = (uint64_t)a.B * a.H * a.N;
@@ -547,9 +593,23 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
     P.max_kv = a.max_kv;
     const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
     P.scale_log2 = scale * kLog2e;
-    const dim3 grid((unsigned)P.nQB, (unsigned)(a.B * a.H));
-    k_bsa_forward<D><<<grid, kThreads, smem_bytes<D>(), stream>>>(P);
-    return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+    const unsigned gx = (unsigned)P.nQB, gy = (unsigned)(a.B * a.H);
+    switch (poly_setting()) {
+        case 0: return launch_dp<D, 0>(P, gx, gy, stream);
+        case 2: return launch_dp<D, 2>(P, gx, gy, stream);
+        case 3: return launch_dp<D, 3>(P, gx, gy, stream);
+        default: return launch_dp<D, 4>(P, gx, gy, stream);
+    }
+}
+
+template <int D>
+int32_t occupancy() {
+    int per_sm = 0;
+    if (prepare_kernel<D, kDefaultPoly>() != cudaSuccess) return -1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bsa_forward<D, kDefaultPoly>, kThreads,
+                                                      smem_bytes<D>()) != cudaSuccess)
+        return -1;
+    return per_sm;
 }
 
 }  // namespace
@@ -561,21 +621,11 @@ bsa_status launch_forward(const ForwardArgs& a, int32_t* status, cudaStream_t st
 }
 
 int32_t forward_resident_ctas(int32_t D) {
-    int dev = 0, sms = 0, per_sm = 0;
+    int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-    cudaError_t e;
-    if (D == 128) {
-        if (prepare_kernel<128>() != cudaSuccess) return -1;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bsa_forward<128>, kThreads, smem_bytes<128>());
-    } else if (D == 64) {
-        if (prepare_kernel<64>() != cudaSuccess) return -1;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bsa_forward<64>, kThreads, smem_bytes<64>());
-    } else {
-        return -1;
-    }
-    if (e != cudaSuccess) return -1;
-    return sms * per_sm;
+    const int32_t per_sm = D == 128 ? occupancy<128>() : (D == 64 ? occupancy<64>() : -1);
+    return per_sm > 0 ? sms * per_sm : -1;
 }
 
 }  // namespace bsa

@@ -20,9 +20,9 @@ def lib():
 
 
 def _declared():
-    src = open(os.path.join(ROOT, "include", "bsa.h")).read()
+    src = "".join(open(os.path.join(ROOT, "include", h)).read() for h in ("bsa.h", "bsa_selftest.h"))
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return set(re.findall(r"\b(bsa_[a-z_]+)\s*\(", src))
+    return set(re.findall(r"\b(bsa_[a-z_0-9]+)\s*\(", src))
 
 
 def test_header_declarations_match_binding_exports():
