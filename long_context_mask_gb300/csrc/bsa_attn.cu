@@ -31,7 +31,12 @@
 //               query map, LSE).
 //
 // The producer loads K/V tiles in exactly the MMA's consumption order
-// (K_0, K_1, K_2, then V_i, K_{i+3}), so the ring is a plain FIFO.
+// (K_0, K_1, K_2, then V_i, K_{i+3}), so the ring is a plain FIFO.  Each MMA
+// group ends with a single commit, on the empty barrier of the ring slot it
+// read; the softmax waits on that same barrier for S_j (slot of K_j) and,
+// before touching O, for PV_{j-1} (slot of V_{j-1}).  The next completion of
+// such a barrier needs a later P from this softmax, so parity waits on it
+// are unambiguous.
 //
 // Tensor memory (512 columns): S_0, S_1, S_2 = [0,384) in 128-column
 // buffers, O = [384, 384+D).
@@ -93,18 +98,18 @@ struct Barriers {
     uint64_t full[16];
     uint64_t empty[16];
     uint64_t q_full;
-    uint64_t s_full[kSBuf];
     uint64_t p_full[kSBuf];
-    uint64_t o_done[2];  // PV_i commits o_done[i % 2]
-    uint64_t o_final;    // after the last PV
     uint64_t mma_done;
     uint32_t tmem_base;
     int32_t abort;
 };
 
 struct Params {
-    CUtensorMap map_q, map_k, map_v;     // box 64 x 128 rows
-    CUtensorMap gmap_q, gmap_k, gmap_v;  // box 64 x 1 row (gather4)
+    // Tile maps view a [rows, D] bf16 tensor as 3D (64 columns, rows, D/64
+    // column halves) so that one copy brings a whole 128-row tile, reading
+    // each 2D-byte row in full, and lands it as D/64 swizzled 16 KB boxes.
+    CUtensorMap map_q, map_k, map_v;     // 3D box 64 x 128 rows x D/64
+    CUtensorMap gmap_q, gmap_k, gmap_v;  // 2D box 64 x 1 row (gather4)
     const int32_t* kv_idx;
     const int32_t* kv_cnt;
     const float* log_w;
@@ -158,10 +163,7 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* tile_
     using C = Cfg<D>;
     const int32_t row0 = (int32_t)(bh * N) + blk * 128;
     if (map == nullptr) {
-        if (lane == 0) {
-#pragma unroll
-            for (int b = 0; b < C::kBoxes; ++b) tma_load_2d(dst + b * C::kBoxBytes, tile_map, 64 * b, row0, bar);
-        }
+        if (lane == 0) tma_load_3d(dst, tile_map, 0, row0, 0, bar);
     } else {
         const int4 t = map_rows(map, bh * N + (int64_t)blk * 128, N, lane, status);
         const int32_t base = (int32_t)(bh * N);
@@ -170,6 +172,17 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* tile_
             tma_gather4(dst + b * C::kBoxBytes + lane * 512, gather_map, 64 * b, base + t.x,
                         base + t.y, base + t.z, base + t.w, bar);
     }
+}
+
+// Positions in the K/V load order K_0, K_1, K_2, then V_i, K_{i+3} (i < n):
+// K_j sits at j for j < 3 and at 2j - 2 after that (right behind V_{j-3});
+// V_i sits behind the min(n, 3) leading K tiles, the i earlier V tiles and
+// the min(i, n - 3) K tiles that follow them.
+__device__ __forceinline__ int32_t ring_pos_k(int32_t j) { return j < kSBuf ? j : 2 * j - 2; }
+__device__ __forceinline__ int32_t ring_pos_v(int32_t i, int32_t n) {
+    const int32_t lead = n < kSBuf ? n : kSBuf;
+    const int32_t mid = n - kSBuf > 0 ? (i < n - kSBuf ? i : n - kSBuf) : 0;
+    return lead + i + mid;
 }
 
 template <int D, int kPoly>
@@ -216,13 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
             mbar_init(smem_u32(&bars->empty[s]), 1);
         }
         mbar_init(smem_u32(&bars->q_full), 1);
-        for (int s = 0; s < kSBuf; ++s) {
-            mbar_init(smem_u32(&bars->s_full[s]), 1);
-            mbar_init(smem_u32(&bars->p_full[s]), 128);
-        }
-        mbar_init(smem_u32(&bars->o_done[0]), 1);
-        mbar_init(smem_u32(&bars->o_done[1]), 1);
-        mbar_init(smem_u32(&bars->o_final), 1);
+        for (int s = 0; s < kSBuf; ++s) mbar_init(smem_u32(&bars->p_full[s]), 128);
         mbar_init(smem_u32(&bars->mma_done), 1);
         bars->abort = 0;
         fence_mbar_init();
@@ -321,8 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
                     const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
                     mma_ss(tmem + d_col, dq + off, ks + off, C::kIdescQK, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(smem_u32(&bars->empty[slot]));
-                mma_commit(smem_u32(&bars->s_full[j % kSBuf]));
+                mma_commit(smem_u32(&bars->empty[slot]));  // also signals S_j to the softmax
                 ++item;
                 return true;
             };
@@ -341,9 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ts(tmem + kColO, tmem + p_col + kk * 8, vs + (uint64_t)(kk * 2048 >> 4),
                            C::kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(smem_u32(&bars->empty[slot]));
-                mma_commit(smem_u32(&bars->o_done[i & 1]));
-                if (i + 1 == n) mma_commit(smem_u32(&bars->o_final));
+                mma_commit(smem_u32(&bars->empty[slot]));  // also signals PV_i to the softmax
                 ++item;
                 // S buffer i % 3 is free again once PV_i (issued above) has read P_i
                 if (i + kSBuf < n) ok = issue_qk(i + kSBuf);
@@ -378,7 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
             const float lw2 = lw_next * kLog2e;
             lw_next = (lw_row && j + 1 < n) ? lw_row[j + 1] : 0.0f;
             const uint32_t sbuf = (uint32_t)(j % kSBuf) * 128u;
-            bool w = mbar_wait(smem_u32(&bars->s_full[j % kSBuf]), (uint32_t)(j / kSBuf) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+            const int32_t pk = ring_pos_k(j);
+            bool w = mbar_wait(smem_u32(&bars->empty[pk % C::kStages]), (uint32_t)(pk / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
             if (__any_sync(0xffffffffu, !w || aborted(bars))) {
                 ok = false;
                 break;
@@ -434,10 +439,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
             tmem_st32(t_lane + sbuf + 0, &s[0]);
             tmem_st32(t_lane + sbuf + 32, &s[32]);
             if (rescale) {
-                // O must hold P_0..P_{j-1} V: wait for PV_{j-1}.  S_j complete
-                // implies PV_{j-3} complete (QK_j was issued after it), so the
-                // parity wait on o_done[(j-1) % 2] is unambiguous.
-                w = mbar_wait(smem_u32(&bars->o_done[(j - 1) & 1]), (uint32_t)((j - 1) >> 1) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                // O must hold P_0..P_{j-1} V: wait for PV_{j-1}
+                const int32_t pv = ring_pos_v(j - 1, n);
+                w = mbar_wait(smem_u32(&bars->empty[pv % C::kStages]), (uint32_t)(pv / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
                 if (__any_sync(0xffffffffu, !w)) {
                     ok = false;
                     break;
@@ -469,7 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
                     P.lse[bh * N + tok] = -INFINITY;
                 }
             } else {
-                const bool w = mbar_wait(smem_u32(&bars->o_final), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                const int32_t pv = ring_pos_v(n - 1, n);
+                const bool w = mbar_wait(smem_u32(&bars->empty[pv % C::kStages]), (uint32_t)(pv / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
                 if (__any_sync(0xffffffffu, !w)) {
                     if (lane == 0) set_abort(bars, P.status);
                 } else {
@@ -517,6 +522,20 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
     });
     return fn;
+}
+
+// [rows, D] as (64 columns, rows, D/64 halves) with a 64 x 128 x D/64 box.
+bool encode_tile_map(CUtensorMap* map, const void* base, uint64_t rows, int D) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(D / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128};
+    cuuint32_t box[3] = {64, 128, (cuuint32_t)(D / 64)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 bool encode_map(CUtensorMap* map, const void* base, uint64_t rows, int D, uint32_t box_rows) {
@@ -575,8 +594,8 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
     Params P;
     memset(&P, 0, sizeof(P));
     const uint64_t rows = (uint64_t)a.B * a.H * a.N;
-    bool ok = encode_map(&P.map_q, a.q, rows, D, 128) && encode_map(&P.map_k, a.k, rows, D, 128) &&
-              encode_map(&P.map_v, a.v, rows, D, 128) && encode_map(&P.gmap_q, a.q, rows, D, 1) &&
+    bool ok = encode_tile_map(&P.map_q, a.q, rows, D) && encode_tile_map(&P.map_k, a.k, rows, D) &&
+              encode_tile_map(&P.map_v, a.v, rows, D) && encode_map(&P.gmap_q, a.q, rows, D, 1) &&
               encode_map(&P.gmap_k, a.k, rows, D, 1) && encode_map(&P.gmap_v, a.v, rows, D, 1);
     if (!ok) return BSA_ERR_CUDA;
     P.kv_idx = a.kv_idx;
