@@ -202,9 +202,15 @@ class Path:
         return self.bsa.effective_flops(cnt, self.prob.D)
 
 
-def make_problem(config: int, heads: int | None):
+def make_problem(config: int, heads: int | None, dense: bool = False):
     kw = {} if heads is None else {"H": heads}
-    return synth.CONFIGS[config](**kw)
+    prob = synth.CONFIGS[config](**kw)
+    if dense:
+        prob.mask = np.ones((prob.rows, prob.nqb), np.uint8)
+        prob.T = prob.scores = prob.k_per_row = prob.k_const = prob.m_sample = prob.u = None
+        prob.diag_list = False
+        prob.name += "+dense"
+    return prob
 
 
 # ---------------------------------------------------------------- CPU oracle timing
@@ -259,6 +265,8 @@ def parse():
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller profiling case)")
     ap.add_argument("--order", default="reordered", choices=["reordered", "identity"])
+    ap.add_argument("--dense", action="store_true",
+                    help="every query block attends to every KV block (the in-build dense ceiling)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle CPU time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -294,7 +302,8 @@ def max_over_ranks(x: float, world: int, dev) -> float:
 
 
 def config_dict(prob, config, order, density, world):
-    return {"workload": synth.CONFIG_NAMES[config], "config_id": config, "B": prob.B, "H": prob.H,
+    name = synth.CONFIG_NAMES[config] + (" [dense: all blocks listed]" if prob.name.endswith("+dense") else "")
+    return {"workload": name, "config_id": config, "B": prob.B, "H": prob.H,
             "N": prob.N, "D": prob.D, "block": 128, "density": round(density, 4), "order": order,
             "l2": "flushed between timed steps (256 MiB write)",
             "parallelism": "one independent workload per GPU" if world > 1 else "single GPU"}
@@ -303,7 +312,7 @@ def config_dict(prob, config, order, density, world):
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    prob = make_problem(args.config, args.heads)
+    prob = make_problem(args.config, args.heads, args.dense)
     lists = host_lists(prob)
     density = float(lists[1].sum()) / (prob.rows * prob.nqb)
     # each step: the oracle on a bounded sample (about 1 s of CPU work)
@@ -345,7 +354,7 @@ def main():
     __graft_entry__.build()
     import long_context_mask_gb300 as bsa
 
-    prob = make_problem(args.config, args.heads)
+    prob = make_problem(args.config, args.heads, args.dense)
     path = Path(prob, dev, args.order)
     path.step()
     torch.cuda.synchronize()
