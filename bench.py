@@ -170,7 +170,11 @@ class Path:
             self.lw = torch.empty((rows, cap), dtype=torch.float32, device=dev)
         self.row_perm = torch.empty((self.heads, nqb), dtype=torch.int32, device=dev)
         self.wave = bsa.resident_ctas(prob.D)
-        self.launches_per_step = 1 + (self.mode is not None) + bool(prob.m_sample) + (order == "reordered")
+        if order == "spectral":
+            self.x0 = torch.from_numpy(synth.spectral_start(7, self.heads, nqb)).float().to(dev)
+            self.spec = torch.empty((self.heads, nqb), dtype=torch.int32, device=dev)
+        self.launches_per_step = (1 + (self.mode is not None) + bool(prob.m_sample)
+                                  + (order != "identity") + (order == "spectral"))
 
     def lists(self):
         return (self.s_idx, self.s_cnt) if self.prob.m_sample else (self.idx, self.cnt)
@@ -183,7 +187,12 @@ class Path:
         if p.m_sample:
             bsa.sample_blocks(self.src, self.idx, self.cnt, p.m_sample, self.u, self.s_idx,
                               self.s_cnt, self.lw)
-        if self.order == "reordered":
+        if self.order == "spectral":
+            idx, cnt = self.lists()
+            bsa.spectral_order(idx, cnt, p.nqb, self.x0, self.spec, iters=10)
+            bsa.reorder_rows(cnt.reshape(self.heads, p.nqb), self.wave, self.row_perm,
+                             order_in=self.spec)
+        elif self.order == "reordered":
             _, cnt = self.lists()
             bsa.reorder_rows(cnt.reshape(self.heads, p.nqb), self.wave, self.row_perm)
 
@@ -191,7 +200,7 @@ class Path:
         idx, cnt = self.lists()
         self.bsa.forward(self.q, self.k, self.v, idx, cnt, self.o, self.lse, log_w=self.lw,
                          q_map=self.q_map, kv_map=self.kv_map,
-                         row_perm=self.row_perm if self.order == "reordered" else None)
+                         row_perm=None if self.order == "identity" else self.row_perm)
 
     def step(self):
         self.build_lists()
@@ -262,9 +271,10 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6])
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller profiling case)")
-    ap.add_argument("--order", default="reordered", choices=["reordered", "identity"])
+    ap.add_argument("--order", default="reordered", choices=["reordered", "identity", "spectral"],
+                    help="row order: NNZ-guided wave sort, identity, or spectral (stage 1) + wave sort")
     ap.add_argument("--dense", action="store_true",
                     help="every query block attends to every KV block (the in-build dense ceiling)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

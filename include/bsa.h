@@ -90,13 +90,42 @@ bsa_status bsa_build_index(bsa_idx_mode mode, const void* src, int64_t rows, int
  *            of 0..nQB-1, e.g. a spatial ordering), or NULL for identity.
  *  heads     B * H, >= 0.
  *  nQB       query blocks per head, 1 .. 65536.
- *  wave      W, 1 .. 65536: typically bsa_resident_ctas(D).
+ *  wave      W, 1 .. 8192: typically bsa_resident_ctas(D).
  *  row_perm  device int32 [heads, nQB] out: row_perm[h][slot] = query block
  *            executed in that slot; pass it to bsa_forward.
  *  An order_in entry outside [0, nQB) raises BSA_ERR_BOUNDS on the device.
  */
 bsa_status bsa_reorder_rows(const int32_t* kv_cnt, const int32_t* order_in, int64_t heads,
                             int32_t nQB, int32_t wave, int32_t* row_perm, void* stream);
+
+/*
+ * bsa_spectral_order - spatial row order from the rank-2 embedding of each
+ * head's centered block mask (the first stage of row reordering).
+ *
+ * Defined by: WaveAlign, section IV-C "SVD-Based Global Spatial Ordering"
+ * (polar spectral ordering; matrix-free centered subspace iteration with
+ * the rank-1 centering correction, 5-15 iterations suffice because the
+ * angular sort ignores in-plane rotations and sign flips).
+ *
+ * Per head the mask A (row = query block, column = KV block listed in that
+ * row) is centered by its mean row mu.  Starting from x0 (orthonormalised),
+ * `iters` times: Z = A^T X - mu (1^T X); X = Gram-Schmidt(A Z - 1 (mu^T Z)).
+ * Rows are then sorted by atan2(X[r][1], X[r][0]) ascending, ties to the lower
+ * query block.  fp32; pass the result as order_in to bsa_reorder_rows.
+ *
+ *  kv_idx, kv_cnt, max_kv  the index lists of B*H*nQB rows (as bsa_forward).
+ *  heads     B * H.        nQB  query blocks per head, 2 .. 4096.
+ *  nKB       KV blocks per head, 1 .. 8192.   iters  0 .. 1000.
+ *  x0        device fp32 [heads, nQB, 2]: starting vectors (e.g. random).
+ *  x_out     device fp32 [heads, nQB, 2] or NULL: the final embedding.
+ *  angle     device fp32 [heads, nQB] or NULL: the polar angles.
+ *  order     device int32 [heads, nQB] out: order[h][s] = query block.
+ *  A list entry outside [0, nKB) is ignored and raises BSA_ERR_BOUNDS.
+ */
+bsa_status bsa_spectral_order(const int32_t* kv_idx, const int32_t* kv_cnt, int32_t max_kv,
+                              int64_t heads, int32_t nQB, int32_t nKB, int32_t iters,
+                              const float* x0, float* x_out, float* angle, int32_t* order,
+                              void* stream);
 
 /*
  * bsa_sample_blocks - exact set plus an importance-weighted PPSWOR sample of

@@ -20,9 +20,11 @@ from .binding import (  # noqa: F401
     forward,
     lib_path,
     load_library,
+    reorder_guard,
     reorder_rows,
     resident_ctas,
     sample_blocks,
     selftest_exp2,
     selftest_wait_timeout,
+    spectral_order,
 )

@@ -20,7 +20,8 @@ STATUS_NAMES = {0: "BSA_OK", 1: "BSA_ERR_INVALID_ARG", 2: "BSA_ERR_UNSUPPORTED",
                 3: "BSA_ERR_OVERFLOW", 4: "BSA_ERR_CUDA", 5: "BSA_ERR_TIMEOUT",
                 6: "BSA_ERR_BOUNDS"}
 
-EXPORTS = ("bsa_build_index", "bsa_reorder_rows", "bsa_sample_blocks", "bsa_forward",
+EXPORTS = ("bsa_build_index", "bsa_reorder_rows", "bsa_spectral_order", "bsa_sample_blocks",
+           "bsa_forward",
            "bsa_device_status", "bsa_resident_ctas", "bsa_status_string", "bsa_selftest_exp2",
            "bsa_selftest_wait_timeout")
 
@@ -50,6 +51,7 @@ def load_library():
     lib.bsa_build_index.argtypes = [i32, P, i64, i32, f32, P, i32, P, P, i32, P]
     lib.bsa_reorder_rows.argtypes = [P, P, i64, i32, i32, P, P]
     lib.bsa_sample_blocks.argtypes = [P, i64, i32, P, P, i32, i32, P, P, P, P, i32, P]
+    lib.bsa_spectral_order.argtypes = [P, P, i32, i64, i32, i32, i32, P, P, P, P, P]
     lib.bsa_forward.argtypes = [P, P, P, i32, i32, i32, i32, P, P, i32, P, P, P, P, f32, P, P, P]
     lib.bsa_device_status.argtypes = [P, ctypes.POINTER(i32)]
     lib.bsa_resident_ctas.argtypes = [i32]
@@ -57,7 +59,8 @@ def load_library():
     lib.bsa_status_string.restype = ctypes.c_char_p
     lib.bsa_selftest_exp2.argtypes = [P, P, P, P, i64, P]
     lib.bsa_selftest_wait_timeout.argtypes = [i64, P]
-    for name in ("bsa_build_index", "bsa_reorder_rows", "bsa_sample_blocks", "bsa_forward",
+    for name in ("bsa_build_index", "bsa_reorder_rows", "bsa_spectral_order", "bsa_sample_blocks",
+                 "bsa_forward",
                  "bsa_device_status", "bsa_resident_ctas", "bsa_selftest_exp2",
                  "bsa_selftest_wait_timeout"):
         getattr(lib, name).restype = i32
@@ -116,6 +119,29 @@ def reorder_rows(kv_cnt, wave: int, row_perm, *, order_in=None, stream=None):
     code = load_library().bsa_reorder_rows(_ptr(kv_cnt), _ptr(order_in), heads, nqb, int(wave),
                                            _ptr(row_perm), _stream(stream))
     _check("bsa_reorder_rows", code)
+
+
+def spectral_order(kv_idx, kv_cnt, n_kb: int, x0, order, *, x_out=None, angle=None,
+                   iters: int = 10, stream=None):
+    """Row order from the rank-2 centered-mask embedding (WaveAlign section IV-C).
+
+    kv_idx [heads*nQB, max_kv], kv_cnt [heads*nQB]; x0 fp32 [heads, nQB, 2];
+    order int32 [heads, nQB] out (optional x_out like x0, angle [heads, nQB])."""
+    import torch
+    _dtype(x0, "x0", torch.float32)
+    _dtype(order, "order", torch.int32)
+    heads, nqb = order.shape
+    code = load_library().bsa_spectral_order(_ptr(kv_idx), _ptr(kv_cnt), kv_idx.shape[1], heads,
+                                             nqb, int(n_kb), int(iters), _ptr(x0), _ptr(x_out),
+                                             _ptr(angle), _ptr(order), _stream(stream))
+    _check("bsa_spectral_order", code)
+
+
+def reorder_guard(N: int, D: int, l2_bytes: int) -> bool:
+    """Whether row reordering can pay on this GPU: only when one head's K/V
+    (2 * N * D bf16 values) exceeds the L2, since heads run one after another
+    and a working set that fits in L2 is already reused in any row order."""
+    return 2 * N * D * 2 > l2_bytes
 
 
 def sample_blocks(scores, exact_idx, exact_cnt, m: int, u, kv_idx, kv_cnt, log_w, *, stream=None):
@@ -194,4 +220,5 @@ def dense_attention_flops(N: int, H: int, D: int, causal: bool = False, B: int =
 __all__ = ["BLOCK", "BsaError", "IDX_MASK_U8", "IDX_THRESHOLD_F32", "IDX_TOPK_F32", "build_index",
            "reorder_rows", "sample_blocks", "forward", "device_status", "resident_ctas",
            "effective_flops", "dense_attention_flops", "load_library", "lib_path", "EXPORTS",
+           "spectral_order", "reorder_guard",
            "selftest_exp2", "selftest_wait_timeout", "math"]

@@ -96,6 +96,26 @@ bsa_status bsa_reorder_rows(const int32_t* kv_cnt, const int32_t* order_in, int6
     return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
+bsa_status bsa_spectral_order(const int32_t* kv_idx, const int32_t* kv_cnt, int32_t max_kv,
+                              int64_t heads, int32_t nQB, int32_t nKB, int32_t iters,
+                              const float* x0, float* x_out, float* angle, int32_t* order,
+                              void* stream) {
+    if (heads < 0 || heads > 65535 || nQB < 2 || nQB > 4096 || nKB < 1 || nKB > 8192 ||
+        max_kv < 1 || max_kv > nKB || iters < 0 || iters > 1000)
+        return BSA_ERR_INVALID_ARG;
+    if (heads == 0) return BSA_OK;
+    if (!kv_idx || !kv_cnt || !x0 || !order) return BSA_ERR_INVALID_ARG;
+    if (!aligned(kv_idx, 4) || !aligned(kv_cnt, 4) || !aligned(x0, 8) || !aligned(order, 4) ||
+        (x_out && !aligned(x_out, 8)) || (angle && !aligned(angle, 4)))
+        return BSA_ERR_INVALID_ARG;
+    int32_t* status = bsa::status_word_ptr();
+    if (!status) return BSA_ERR_CUDA;
+    cudaError_t e = bsa::launch_spectral_order(kv_idx, kv_cnt, max_kv, heads, nQB, nKB, iters, x0,
+                                               x_out, angle, order, status,
+                                               static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
 bsa_status bsa_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
                              const int32_t* exact_idx, const int32_t* exact_cnt,
                              int32_t exact_stride, int32_t m, const double* u, int32_t* kv_idx,

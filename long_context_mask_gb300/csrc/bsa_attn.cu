@@ -77,7 +77,6 @@ constexpr int kDefaultPoly = 0;            // exponentials per 8 on the FMA pipe
 constexpr float kRescaleThreshold = 8.0f;  // rescale O only when the max grows by > 2^8
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
-constexpr int kFirstSoftmaxWarp = 2;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 384;

@@ -56,6 +56,8 @@ def _load():
         lib.oracle_attention.argtypes = [P, P, P, i32, i32, i32, i32, P, P, i32, P, P, P,
                                          f64, P, i64, P, P, P]
         lib.oracle_attention.restype = None
+        lib.oracle_spectral_order.argtypes = [P, P, i32, i64, i32, i32, i32, P, P, P, P]
+        lib.oracle_spectral_order.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i32
         _lib = lib
@@ -142,6 +144,23 @@ def sample_blocks(scores, exact_idx, exact_cnt, m, u, max_kv):
                                       exact_idx.shape[1], int(m), _ptr(u), _ptr(idx), _ptr(cnt),
                                       _ptr(lw), int(max_kv))
     return idx, cnt, lw, int(ov)
+
+
+def spectral_order(kv_idx, kv_cnt, n_kb, x0, iters):
+    """WaveAlign stage 1 per head: (X [heads, nQB, 2], angle [heads, nQB], order [heads, nQB]).
+
+    kv_idx [heads*nQB, max_kv], kv_cnt [heads*nQB]; x0 fp64 [heads, nQB, 2]."""
+    kv_idx = _c(kv_idx, np.int32)
+    kv_cnt = _c(kv_cnt, np.int32)
+    x0 = _c(x0, np.float64)
+    heads, nqb = x0.shape[0], x0.shape[1]
+    X = np.empty((heads, nqb, 2), np.float64)
+    ang = np.empty((heads, nqb), np.float64)
+    order = np.empty((heads, nqb), np.int32)
+    _load().oracle_spectral_order(_ptr(kv_idx), _ptr(kv_cnt), kv_idx.shape[1], heads, nqb,
+                                  int(n_kb), int(iters), _ptr(x0), _ptr(X), _ptr(ang),
+                                  _ptr(order))
+    return X, ang, order
 
 
 def attention(q, k, v, kv_idx, kv_cnt, log_w=None, q_map=None, kv_map=None, scale=0.0,

@@ -25,6 +25,9 @@
  *                          probabilities, cap at 1 and renormalise), the
  *                          promotion of pi = 1 keys, systematic PPS sampling,
  *                          and Algorithm 1 step 13 (w = 1/pi).
+ *   oracle_spectral_order  WaveAlign, section IV-C (rank-2 embedding of the
+ *                          centered mask by matrix-free subspace iteration,
+ *                          rows ordered by polar angle).
  *   oracle_attention       InstaGen, section 3.1 eqs. (1)-(3) and Algorithm 1
  *                          step 14 (softmax of l_ij + log w_j over the kept
  *                          keys); INTRA, "CQS-Aware Token-Sparse
@@ -349,4 +352,112 @@ int32_t oracle_num_threads(void) {
 #else
     return 1;
 #endif
+}
+
+/* ------------------------------------------------------------------------- */
+/* Spectral row order, WaveAlign section IV-C ("SVD-Based Global Spatial    */
+/* Ordering": polar spectral ordering and matrix-free centered subspace      */
+/* iteration).                                                               */
+/*                                                                           */
+/* Per head the mask A (rows = query blocks, columns = KV blocks, A[r][c] = */
+/* 1 when c is in row r's list) is centered by its mean row mu, so that     */
+/* pairwise row distances are kept and the all-ones direction gets a zero   */
+/* singular value.  The top-2 left singular subspace of the centered mask   */
+/* is found by subspace iteration that never forms it:                      */
+/*     Z = A^T X - mu (1^T X)          (the rank-1 centering correction)     */
+/*     Y = A Z   - 1 (mu^T Z)                                                */
+/*     X = Gram-Schmidt(Y)                                                   */
+/* starting from the given X0 (orthonormalised first).  Each row's polar    */
+/* angle atan2(X[r][1], X[r][0]) then orders the rows (ascending, ties to   */
+/* the lower query block).  Outputs: X [heads, nQB, 2], the angle           */
+/* [heads, nQB] and the order [heads, nQB] (order[h][s] = query block).     */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+    double a;
+    int32_t r;
+} angled_t;
+
+static int by_angle_then_row(const void* x, const void* y) {
+    const angled_t* p = (const angled_t*)x;
+    const angled_t* q = (const angled_t*)y;
+    if (p->a < q->a) return -1;
+    if (p->a > q->a) return 1;
+    return (p->r > q->r) - (p->r < q->r);
+}
+
+static void gram_schmidt2(double* X, int32_t n) {
+    double n0 = 0.0;
+    for (int32_t r = 0; r < n; ++r) n0 += X[2 * r] * X[2 * r];
+    n0 = sqrt(n0);
+    for (int32_t r = 0; r < n; ++r) X[2 * r] /= n0;
+    double d = 0.0;
+    for (int32_t r = 0; r < n; ++r) d += X[2 * r] * X[2 * r + 1];
+    for (int32_t r = 0; r < n; ++r) X[2 * r + 1] -= d * X[2 * r];
+    double n1 = 0.0;
+    for (int32_t r = 0; r < n; ++r) n1 += X[2 * r + 1] * X[2 * r + 1];
+    n1 = sqrt(n1);
+    for (int32_t r = 0; r < n; ++r) X[2 * r + 1] /= n1;
+}
+
+void oracle_spectral_order(const int32_t* kv_idx, const int32_t* kv_cnt, int32_t max_kv,
+                           int64_t heads, int32_t nQB, int32_t nKB, int32_t iters,
+                           const double* x0, double* x_out, double* angle, int32_t* order) {
+    double* mu = (double*)malloc(sizeof(double) * (size_t)nKB);
+    double* Z = (double*)malloc(sizeof(double) * 2 * (size_t)nKB);
+    double* X = (double*)malloc(sizeof(double) * 2 * (size_t)nQB);
+    angled_t* srt = (angled_t*)malloc(sizeof(angled_t) * (size_t)nQB);
+    for (int64_t h = 0; h < heads; ++h) {
+        const int32_t* idx = kv_idx + h * nQB * (int64_t)max_kv;
+        const int32_t* cnt = kv_cnt + h * nQB;
+        for (int32_t c = 0; c < nKB; ++c) mu[c] = 0.0;
+        for (int32_t r = 0; r < nQB; ++r)
+            for (int32_t e = 0; e < cnt[r]; ++e) mu[idx[r * (int64_t)max_kv + e]] += 1.0;
+        for (int32_t c = 0; c < nKB; ++c) mu[c] /= (double)nQB;
+        memcpy(X, x0 + h * 2 * (int64_t)nQB, sizeof(double) * 2 * (size_t)nQB);
+        gram_schmidt2(X, nQB);
+        for (int32_t it = 0; it < iters; ++it) {
+            double s0 = 0.0, s1 = 0.0; /* 1^T X */
+            for (int32_t r = 0; r < nQB; ++r) {
+                s0 += X[2 * r];
+                s1 += X[2 * r + 1];
+            }
+            for (int32_t c = 0; c < 2 * nKB; ++c) Z[c] = 0.0;
+            for (int32_t r = 0; r < nQB; ++r)
+                for (int32_t e = 0; e < cnt[r]; ++e) {
+                    const int32_t c = idx[r * (int64_t)max_kv + e];
+                    Z[2 * c] += X[2 * r];
+                    Z[2 * c + 1] += X[2 * r + 1];
+                }
+            double m0 = 0.0, m1 = 0.0; /* mu^T Z (after centering) */
+            for (int32_t c = 0; c < nKB; ++c) {
+                Z[2 * c] -= mu[c] * s0;
+                Z[2 * c + 1] -= mu[c] * s1;
+                m0 += mu[c] * Z[2 * c];
+                m1 += mu[c] * Z[2 * c + 1];
+            }
+            for (int32_t r = 0; r < nQB; ++r) {
+                double y0 = 0.0, y1 = 0.0;
+                for (int32_t e = 0; e < cnt[r]; ++e) {
+                    const int32_t c = idx[r * (int64_t)max_kv + e];
+                    y0 += Z[2 * c];
+                    y1 += Z[2 * c + 1];
+                }
+                X[2 * r] = y0 - m0;
+                X[2 * r + 1] = y1 - m1;
+            }
+            gram_schmidt2(X, nQB);
+        }
+        for (int32_t r = 0; r < nQB; ++r) {
+            srt[r].a = atan2(X[2 * r + 1], X[2 * r]);
+            srt[r].r = r;
+            angle[h * nQB + r] = srt[r].a;
+        }
+        memcpy(x_out + h * 2 * (int64_t)nQB, X, sizeof(double) * 2 * (size_t)nQB);
+        qsort(srt, (size_t)nQB, sizeof(angled_t), by_angle_then_row);
+        for (int32_t s = 0; s < nQB; ++s) order[h * nQB + s] = srt[s].r;
+    }
+    free(srt);
+    free(X);
+    free(Z);
+    free(mu);
 }

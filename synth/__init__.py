@@ -28,6 +28,8 @@ structure the pages describe):
                  per-block offsets so that query blocks fall into 8 shuffled
                  low-rank access clusters; block scores are mean-pooled QK^T;
                  per-row k ~ U{ceil(0.10 nB) .. floor(0.20 nB)}.
+* ``long_video`` the same at N401408 (401 latent frames), H2: one head's K/V
+                 exceeds the L2 (WaveAlign's longest Wan2.1 workload).
 """
 from __future__ import annotations
 
@@ -181,17 +183,33 @@ def dynamic(seed: int = 5, B: int = 1, H: int = 24, N: int = 118784, D: int = 12
     return prob
 
 
+def long_video(seed: int = 6, B: int = 1, H: int = 2, N: int = 401408, D: int = 128) -> Problem:
+    """The dynamic workload at 401K tokens (3136 blocks per head): one head's
+    K/V (205 MB) no longer fits in a 129 MB L2, the regime where the order in
+    which query rows run decides K/V reuse (WaveAlign's 401-frame Wan2.1 case)."""
+    p = dynamic(seed=seed, B=B, H=H, N=N, D=D)
+    p.name = "long_video"
+    return p
+
+
+def spectral_start(seed: int, heads: int, nqb: int) -> np.ndarray:
+    """Random starting vectors [heads, nQB, 2] for the subspace iteration."""
+    g = _gen(seed)
+    return torch.randn((heads, nqb, 2), generator=g, dtype=torch.float64).numpy()
+
+
 def diag_lists(rows: int, nqb: int):
     """kv_idx [rows, 1] = qb, kv_cnt = 1: each query block attends to its own block."""
     idx = (np.arange(rows) % nqb).astype(np.int32)[:, None]
     return idx, np.ones(rows, np.int32)
 
 
-CONFIGS = {1: tiny, 2: threshold, 3: scatter, 4: sampled, 5: dynamic}
+CONFIGS = {1: tiny, 2: threshold, 3: scatter, 4: sampled, 5: dynamic, 6: long_video}
 CONFIG_NAMES = {
     1: "tiny B1 H2 N2048 D64, Bernoulli(0.25) block mask + diagonal",
     2: "threshold-map mask B1 H12 N32768 D128, T~U(0,1) + frame band, p=0.15",
     3: "Scatter/Gather maps B1 H24 N16384 D128, T=R=128, one block per query block",
     4: "permuted exact top-16 + 8 PPS-sampled blocks B1 H40 N75776 D128",
     5: "dynamic top-k (10-20%) of mean-pooled scores, 8 shuffled clusters, B1 H24 N118784 D128",
+    6: "dynamic top-k (10-20%), 8 shuffled clusters, long video B1 H2 N401408 D128",
 }

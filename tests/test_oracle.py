@@ -423,3 +423,75 @@ def test_flop_formula_reproduces_printed_gflops():
         f = dense_attention_flops(int(N), int(H), int(D), causal=bool(int(causal)))
         f /= int(groups)
         assert abs(f / 1e9 - float(gf)) <= 0.05, (l, f / 1e9)
+
+
+# --------------------------------------------------------------------------
+# Spectral row order (WaveAlign section IV-C): matrix-free centered subspace
+# iteration, checked against numpy's SVD of the explicitly centered mask.
+# --------------------------------------------------------------------------
+def _lists_from_mask(mask):
+    idx, cnt, _ = oracle.index_mask(mask)
+    return idx, cnt
+
+
+def _planted_mask(rng, heads, nqb, nkb, clusters, p_in=0.6, p_out=0.03):
+    mask = np.zeros((heads, nqb, nkb), np.uint8)
+    lab = np.zeros((heads, nqb), np.int64)
+    for h in range(heads):
+        cols = rng.permutation(nkb)
+        support = np.array_split(cols, clusters)
+        lab[h] = rng.integers(0, clusters, nqb)
+        for r in range(nqb):
+            row = rng.random(nkb) < p_out
+            row[support[lab[h, r]]] |= rng.random(len(support[lab[h, r]])) < p_in
+            row[r % nkb] = True
+            mask[h, r] = row
+    return mask, lab
+
+
+def test_spectral_subspace_matches_svd_of_centered_mask():
+    rng = np.random.default_rng(21)
+    heads, nqb, nkb = 2, 96, 80
+    mask, _ = _planted_mask(rng, heads, nqb, nkb, clusters=3)
+    idx, cnt = _lists_from_mask(mask.reshape(heads * nqb, nkb))
+    x0 = rng.standard_normal((heads, nqb, 2))
+    X, ang, order = oracle.spectral_order(idx, cnt, nkb, x0, iters=300)
+    for h in range(heads):
+        A = mask[h].astype(np.float64)
+        Ac = A - A.mean(0, keepdims=True)          # centered by the mean row
+        U, S, _ = np.linalg.svd(Ac, full_matrices=False)
+        assert S[1] > 1.05 * S[2]                  # a spectral gap to converge to
+        cos = np.linalg.svd(U[:, :2].T @ X[h], compute_uv=False)
+        assert cos.min() > 1 - 1e-8
+        np.testing.assert_allclose(X[h].T @ X[h], np.eye(2), atol=1e-12)   # orthonormal
+        np.testing.assert_allclose(X[h].sum(0), 0.0, atol=1e-9)            # orthogonal to 1
+
+
+def test_spectral_order_groups_planted_clusters_and_is_a_permutation():
+    rng = np.random.default_rng(5)
+    heads, nqb, nkb = 3, 120, 100
+    mask, lab = _planted_mask(rng, heads, nqb, nkb, clusters=3, p_in=0.7, p_out=0.01)
+    idx, cnt = _lists_from_mask(mask.reshape(heads * nqb, nkb))
+    x0 = rng.standard_normal((heads, nqb, 2))
+    X, ang, order = oracle.spectral_order(idx, cnt, nkb, x0, iters=15)  # the page's 5-15
+    for h in range(heads):
+        assert sorted(order[h]) == list(range(nqb))
+        seq = lab[h][order[h]]
+        # each cluster occupies one circular run of the order
+        changes = int(np.sum(seq != np.roll(seq, 1)))
+        assert changes <= 3, (h, changes)
+        assert np.all(np.diff(ang[h][order[h]]) >= 0)
+
+
+def test_spectral_order_is_equivariant_under_row_relabelling():
+    rng = np.random.default_rng(8)
+    nqb, nkb = 64, 50
+    mask, _ = _planted_mask(rng, 1, nqb, nkb, clusters=2)
+    perm = rng.permutation(nqb)
+    x0 = rng.standard_normal((1, nqb, 2))
+    idx, cnt = _lists_from_mask(mask[0])
+    X, ang, order = oracle.spectral_order(idx, cnt, nkb, x0, iters=10)
+    idx_p, cnt_p = _lists_from_mask(mask[0][perm])
+    Xp, angp, orderp = oracle.spectral_order(idx_p, cnt_p, nkb, x0[:, perm], iters=10)
+    np.testing.assert_allclose(Xp[0], X[0][perm], atol=1e-10)
+    np.testing.assert_allclose(angp[0], ang[0][perm], atol=1e-10)
