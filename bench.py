@@ -173,6 +173,8 @@ class Path:
         if order == "spectral":
             self.x0 = torch.from_numpy(synth.spectral_start(7, self.heads, nqb)).float().to(dev)
             self.spec = torch.empty((self.heads, nqb), dtype=torch.int32, device=dev)
+            self.spec_ws = torch.empty(bsa.spectral_order_workspace_size(self.heads, nqb, nqb),
+                                       dtype=torch.uint8, device=dev)
         self.launches_per_step = (1 + (self.mode is not None) + bool(prob.m_sample)
                                   + (order != "identity") + (order == "spectral"))
 
@@ -189,7 +191,7 @@ class Path:
                               self.s_cnt, self.lw)
         if self.order == "spectral":
             idx, cnt = self.lists()
-            bsa.spectral_order(idx, cnt, p.nqb, self.x0, self.spec, iters=10)
+            bsa.spectral_order(idx, cnt, p.nqb, self.x0, self.spec, workspace=self.spec_ws, iters=10)
             bsa.reorder_rows(cnt.reshape(self.heads, p.nqb), self.wave, self.row_perm,
                              order_in=self.spec)
         elif self.order == "reordered":

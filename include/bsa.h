@@ -23,6 +23,7 @@
 #ifndef BSA_H
 #define BSA_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -111,12 +112,19 @@ bsa_status bsa_reorder_rows(const int32_t* kv_cnt, const int32_t* order_in, int6
  * row) is centered by its mean row mu.  Starting from x0 (orthonormalised),
  * `iters` times: Z = A^T X - mu (1^T X); X = Gram-Schmidt(A Z - 1 (mu^T Z)).
  * Rows are then sorted by atan2(X[r][1], X[r][0]) ascending, ties to the lower
- * query block.  fp32; pass the result as order_in to bsa_reorder_rows.
+ * query block.  fp32, one warp per query block across the whole GPU; the
+ * sums are fp32 atomics, so the last bits of the embedding (and the order of
+ * rows whose angles nearly coincide) may differ between runs.  Pass the
+ * result as order_in to bsa_reorder_rows.
  *
  *  kv_idx, kv_cnt, max_kv  the index lists of B*H*nQB rows (as bsa_forward).
- *  heads     B * H.        nQB  query blocks per head, 2 .. 4096.
- *  nKB       KV blocks per head, 1 .. 8192.   iters  0 .. 1000.
+ *  heads     B * H.        nQB  query blocks per head, 2 .. 8192.
+ *  nKB       KV blocks per head, 1 .. 65536.   iters  0 .. 1000.
  *  x0        device fp32 [heads, nQB, 2]: starting vectors (e.g. random).
+ *  workspace device scratch of at least
+ *            bsa_spectral_order_workspace_size(heads, nQB, nKB) bytes,
+ *            8-byte aligned; its contents on entry do not matter.  Calls
+ *            that share a workspace must not overlap on the GPU.
  *  x_out     device fp32 [heads, nQB, 2] or NULL: the final embedding.
  *  angle     device fp32 [heads, nQB] or NULL: the polar angles.
  *  order     device int32 [heads, nQB] out: order[h][s] = query block.
@@ -124,8 +132,11 @@ bsa_status bsa_reorder_rows(const int32_t* kv_cnt, const int32_t* order_in, int6
  */
 bsa_status bsa_spectral_order(const int32_t* kv_idx, const int32_t* kv_cnt, int32_t max_kv,
                               int64_t heads, int32_t nQB, int32_t nKB, int32_t iters,
-                              const float* x0, float* x_out, float* angle, int32_t* order,
-                              void* stream);
+                              const float* x0, void* workspace, size_t workspace_bytes,
+                              float* x_out, float* angle, int32_t* order, void* stream);
+
+/* Bytes of workspace bsa_spectral_order needs (0 for sizes it rejects). */
+size_t bsa_spectral_order_workspace_size(int64_t heads, int32_t nQB, int32_t nKB);
 
 /*
  * bsa_sample_blocks - exact set plus an importance-weighted PPSWOR sample of

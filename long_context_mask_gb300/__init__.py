@@ -27,4 +27,5 @@ from .binding import (  # noqa: F401
     selftest_exp2,
     selftest_wait_timeout,
     spectral_order,
+    spectral_order_workspace_size,
 )

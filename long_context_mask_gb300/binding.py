@@ -20,7 +20,8 @@ STATUS_NAMES = {0: "BSA_OK", 1: "BSA_ERR_INVALID_ARG", 2: "BSA_ERR_UNSUPPORTED",
                 3: "BSA_ERR_OVERFLOW", 4: "BSA_ERR_CUDA", 5: "BSA_ERR_TIMEOUT",
                 6: "BSA_ERR_BOUNDS"}
 
-EXPORTS = ("bsa_build_index", "bsa_reorder_rows", "bsa_spectral_order", "bsa_sample_blocks",
+EXPORTS = ("bsa_build_index", "bsa_reorder_rows", "bsa_spectral_order",
+           "bsa_spectral_order_workspace_size", "bsa_sample_blocks",
            "bsa_forward",
            "bsa_device_status", "bsa_resident_ctas", "bsa_status_string", "bsa_selftest_exp2",
            "bsa_selftest_wait_timeout")
@@ -51,7 +52,10 @@ def load_library():
     lib.bsa_build_index.argtypes = [i32, P, i64, i32, f32, P, i32, P, P, i32, P]
     lib.bsa_reorder_rows.argtypes = [P, P, i64, i32, i32, P, P]
     lib.bsa_sample_blocks.argtypes = [P, i64, i32, P, P, i32, i32, P, P, P, P, i32, P]
-    lib.bsa_spectral_order.argtypes = [P, P, i32, i64, i32, i32, i32, P, P, P, P, P]
+    lib.bsa_spectral_order.argtypes = [P, P, i32, i64, i32, i32, i32, P, P, ctypes.c_size_t, P, P,
+                                       P, P]
+    lib.bsa_spectral_order_workspace_size.argtypes = [i64, i32, i32]
+    lib.bsa_spectral_order_workspace_size.restype = ctypes.c_size_t
     lib.bsa_forward.argtypes = [P, P, P, i32, i32, i32, i32, P, P, i32, P, P, P, P, f32, P, P, P]
     lib.bsa_device_status.argtypes = [P, ctypes.POINTER(i32)]
     lib.bsa_resident_ctas.argtypes = [i32]
@@ -121,19 +125,30 @@ def reorder_rows(kv_cnt, wave: int, row_perm, *, order_in=None, stream=None):
     _check("bsa_reorder_rows", code)
 
 
-def spectral_order(kv_idx, kv_cnt, n_kb: int, x0, order, *, x_out=None, angle=None,
-                   iters: int = 10, stream=None):
+def spectral_order_workspace_size(heads: int, nqb: int, nkb: int) -> int:
+    return int(load_library().bsa_spectral_order_workspace_size(heads, nqb, nkb))
+
+
+def spectral_order(kv_idx, kv_cnt, n_kb: int, x0, order, *, workspace=None, x_out=None,
+                   angle=None, iters: int = 10, stream=None):
     """Row order from the rank-2 centered-mask embedding (WaveAlign section IV-C).
 
     kv_idx [heads*nQB, max_kv], kv_cnt [heads*nQB]; x0 fp32 [heads, nQB, 2];
-    order int32 [heads, nQB] out (optional x_out like x0, angle [heads, nQB])."""
+    order int32 [heads, nQB] out (optional x_out like x0, angle [heads, nQB]).
+    ``workspace`` is a CUDA tensor of at least spectral_order_workspace_size()
+    bytes (allocated here through torch when omitted)."""
     import torch
     _dtype(x0, "x0", torch.float32)
     _dtype(order, "order", torch.int32)
     heads, nqb = order.shape
+    need = spectral_order_workspace_size(heads, nqb, n_kb)
+    if workspace is None:
+        workspace = torch.empty(max(need, 8), dtype=torch.uint8, device=order.device)
+    nbytes = workspace.numel() * workspace.element_size()
     code = load_library().bsa_spectral_order(_ptr(kv_idx), _ptr(kv_cnt), kv_idx.shape[1], heads,
-                                             nqb, int(n_kb), int(iters), _ptr(x0), _ptr(x_out),
-                                             _ptr(angle), _ptr(order), _stream(stream))
+                                             nqb, int(n_kb), int(iters), _ptr(x0),
+                                             _ptr(workspace), nbytes, _ptr(x_out), _ptr(angle),
+                                             _ptr(order), _stream(stream))
     _check("bsa_spectral_order", code)
 
 
@@ -220,5 +235,5 @@ def dense_attention_flops(N: int, H: int, D: int, causal: bool = False, B: int =
 __all__ = ["BLOCK", "BsaError", "IDX_MASK_U8", "IDX_THRESHOLD_F32", "IDX_TOPK_F32", "build_index",
            "reorder_rows", "sample_blocks", "forward", "device_status", "resident_ctas",
            "effective_flops", "dense_attention_flops", "load_library", "lib_path", "EXPORTS",
-           "spectral_order", "reorder_guard",
+           "spectral_order", "spectral_order_workspace_size", "reorder_guard",
            "selftest_exp2", "selftest_wait_timeout", "math"]

@@ -96,23 +96,34 @@ bsa_status bsa_reorder_rows(const int32_t* kv_cnt, const int32_t* order_in, int6
     return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
+static bool spectral_sizes_ok(int64_t heads, int32_t nQB, int32_t nKB) {
+    return heads >= 0 && heads <= 65535 && nQB >= 2 && nQB <= 8192 && nKB >= 1 && nKB <= 65536;
+}
+
+size_t bsa_spectral_order_workspace_size(int64_t heads, int32_t nQB, int32_t nKB) {
+    if (!spectral_sizes_ok(heads, nQB, nKB)) return 0;
+    return bsa::spectral_order_workspace_bytes(heads, nQB, nKB);
+}
+
 bsa_status bsa_spectral_order(const int32_t* kv_idx, const int32_t* kv_cnt, int32_t max_kv,
                               int64_t heads, int32_t nQB, int32_t nKB, int32_t iters,
-                              const float* x0, float* x_out, float* angle, int32_t* order,
-                              void* stream) {
-    if (heads < 0 || heads > 65535 || nQB < 2 || nQB > 4096 || nKB < 1 || nKB > 8192 ||
-        max_kv < 1 || max_kv > nKB || iters < 0 || iters > 1000)
+                              const float* x0, void* workspace, size_t workspace_bytes,
+                              float* x_out, float* angle, int32_t* order, void* stream) {
+    if (!spectral_sizes_ok(heads, nQB, nKB) || max_kv < 1 || max_kv > nKB || iters < 0 ||
+        iters > 1000)
         return BSA_ERR_INVALID_ARG;
     if (heads == 0) return BSA_OK;
-    if (!kv_idx || !kv_cnt || !x0 || !order) return BSA_ERR_INVALID_ARG;
+    if (!kv_idx || !kv_cnt || !x0 || !order || !workspace) return BSA_ERR_INVALID_ARG;
+    if (workspace_bytes < bsa::spectral_order_workspace_bytes(heads, nQB, nKB))
+        return BSA_ERR_INVALID_ARG;
     if (!aligned(kv_idx, 4) || !aligned(kv_cnt, 4) || !aligned(x0, 8) || !aligned(order, 4) ||
-        (x_out && !aligned(x_out, 8)) || (angle && !aligned(angle, 4)))
+        !aligned(workspace, 8) || (x_out && !aligned(x_out, 8)) || (angle && !aligned(angle, 4)))
         return BSA_ERR_INVALID_ARG;
     int32_t* status = bsa::status_word_ptr();
     if (!status) return BSA_ERR_CUDA;
     cudaError_t e = bsa::launch_spectral_order(kv_idx, kv_cnt, max_kv, heads, nQB, nKB, iters, x0,
-                                               x_out, angle, order, status,
-                                               static_cast<cudaStream_t>(stream));
+                                               static_cast<float*>(workspace), x_out, angle, order,
+                                               status, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 

@@ -32,11 +32,11 @@ cudaError_t launch_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
                                  int32_t* status, cudaStream_t stream);
 
 // bsa_order.cu
-size_t spectral_order_smem(int32_t nQB, int32_t nKB, int32_t* p2_out);
+size_t spectral_order_workspace_bytes(int64_t heads, int32_t nQB, int32_t nKB);
 cudaError_t launch_spectral_order(const int32_t* kv_idx, const int32_t* kv_cnt, int32_t max_kv,
                                   int64_t heads, int32_t nQB, int32_t nKB, int32_t iters,
-                                  const float* x0, float* x_out, float* angle, int32_t* order,
-                                  int32_t* status, cudaStream_t stream);
+                                  const float* x0, float* workspace, float* x_out, float* angle,
+                                  int32_t* order, int32_t* status, cudaStream_t stream);
 
 // bsa_attn.cu
 struct ForwardArgs {

@@ -88,6 +88,15 @@ def test_reorder_and_sample_host_validation(lib):
              None) == 1                                                           # u not 8-aligned
 
 
+def test_spectral_order_workspace_and_validation(lib):
+    ws = lib.bsa_spectral_order_workspace_size
+    assert ws(2, 100, 80) == 2 * (5 * 80 + 2 * 100 + 16) * 4
+    assert ws(2, 1, 80) == 0 and ws(2, 9000, 80) == 0
+    f = lib.bsa_spectral_order
+    assert f(FAKE, FAKE, 8, 2, 100, 80, 10, FAKE, FAKE, 10, None, None, FAKE, None) == 1  # too small
+    assert f(FAKE, FAKE, 8, 2, 100, 80, 10, FAKE, None, 1 << 20, None, None, FAKE, None) == 1
+
+
 def test_device_status_rejects_null_output(lib):
     assert lib.bsa_device_status(None, None) == 1
 
