@@ -138,6 +138,36 @@ bsa_status bsa_spectral_order(const int32_t* kv_idx, const int32_t* kv_cnt, int3
 /* Bytes of workspace bsa_spectral_order needs (0 for sizes it rejects). */
 size_t bsa_spectral_order_workspace_size(int64_t heads, int32_t nQB, int32_t nKB);
 
+/* Size of the fixed scratch array behind bsa_spectral_order_noalloc. */
+#define BSA_SPECTRAL_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * bsa_spectral_order_noalloc - bsa_spectral_order for callers that cannot
+ * allocate device memory.  The pages have no counterpart; it exists for
+ * programs that must not allocate while they run (for example a serving
+ * loop or host framework that owns the whole device memory pool, where an
+ * allocation could fail or stall in the middle of a step) or that cannot
+ * pass a workspace buffer down to this call.
+ *
+ * Same arguments and results as bsa_spectral_order, without the workspace:
+ * its scratch is a fixed array of BSA_SPECTRAL_NOALLOC_SCRATCH_BYTES inside
+ * the library, present on every device that loads it until the process
+ * exits.  Nothing in this call allocates memory.
+ *  - Sizes whose workspace (bsa_spectral_order_workspace_size) exceeds
+ *    BSA_SPECTRAL_NOALLOC_SCRATCH_BYTES are rejected with
+ *    BSA_ERR_UNSUPPORTED before anything is launched.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - All calls share the array.  Calls whose work overlaps on the GPU (other
+ *    streams, other host threads) race on it: serialise them.  Each call
+ *    clears what must start at zero, so leftovers of an earlier call do not
+ *    matter.
+ */
+bsa_status bsa_spectral_order_noalloc(const int32_t* kv_idx, const int32_t* kv_cnt,
+                                      int32_t max_kv, int64_t heads, int32_t nQB, int32_t nKB,
+                                      int32_t iters, const float* x0, float* x_out, float* angle,
+                                      int32_t* order, void* stream);
+
 /*
  * bsa_sample_blocks - exact set plus an importance-weighted PPSWOR sample of
  * the remaining KV blocks, with Horvitz-Thompson log-weights.

@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     IDX_MASK_U8,
     IDX_THRESHOLD_F32,
     IDX_TOPK_F32,
+    NOALLOC_SCRATCH_BYTES,
     build_index,
     dense_attention_flops,
     device_status,
@@ -27,5 +28,6 @@ from .binding import (  # noqa: F401
     selftest_exp2,
     selftest_wait_timeout,
     spectral_order,
+    spectral_order_noalloc,
     spectral_order_workspace_size,
 )

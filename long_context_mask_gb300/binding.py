@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "BSA_OK", 1: "BSA_ERR_INVALID_ARG", 2: "BSA_ERR_UNSUPPORTED",
                 6: "BSA_ERR_BOUNDS"}
 
 EXPORTS = ("bsa_build_index", "bsa_reorder_rows", "bsa_spectral_order",
-           "bsa_spectral_order_workspace_size", "bsa_sample_blocks",
+           "bsa_spectral_order_workspace_size", "bsa_spectral_order_noalloc", "bsa_sample_blocks",
            "bsa_forward",
            "bsa_device_status", "bsa_resident_ctas", "bsa_status_string", "bsa_selftest_exp2",
            "bsa_selftest_wait_timeout")
@@ -56,6 +56,8 @@ def load_library():
                                        P, P]
     lib.bsa_spectral_order_workspace_size.argtypes = [i64, i32, i32]
     lib.bsa_spectral_order_workspace_size.restype = ctypes.c_size_t
+    lib.bsa_spectral_order_noalloc.argtypes = [P, P, i32, i64, i32, i32, i32, P, P, P, P, P]
+    lib.bsa_spectral_order_noalloc.restype = i32
     lib.bsa_forward.argtypes = [P, P, P, i32, i32, i32, i32, P, P, i32, P, P, P, P, f32, P, P, P]
     lib.bsa_device_status.argtypes = [P, ctypes.POINTER(i32)]
     lib.bsa_resident_ctas.argtypes = [i32]
@@ -152,6 +154,24 @@ def spectral_order(kv_idx, kv_cnt, n_kb: int, x0, order, *, workspace=None, x_ou
     _check("bsa_spectral_order", code)
 
 
+NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def spectral_order_noalloc(kv_idx, kv_cnt, n_kb: int, x0, order, *, x_out=None, angle=None,
+                           iters: int = 10, stream=None):
+    """spectral_order for callers that cannot allocate device memory: the
+    library's own fixed scratch array replaces the workspace (see bsa.h)."""
+    import torch
+    _dtype(x0, "x0", torch.float32)
+    _dtype(order, "order", torch.int32)
+    heads, nqb = order.shape
+    code = load_library().bsa_spectral_order_noalloc(_ptr(kv_idx), _ptr(kv_cnt), kv_idx.shape[1],
+                                                     heads, nqb, int(n_kb), int(iters), _ptr(x0),
+                                                     _ptr(x_out), _ptr(angle), _ptr(order),
+                                                     _stream(stream))
+    _check("bsa_spectral_order_noalloc", code)
+
+
 def reorder_guard(N: int, D: int, l2_bytes: int) -> bool:
     """Whether row reordering can pay on this GPU: only when one head's K/V
     (2 * N * D bf16 values) exceeds the L2, since heads run one after another
@@ -235,5 +255,6 @@ def dense_attention_flops(N: int, H: int, D: int, causal: bool = False, B: int =
 __all__ = ["BLOCK", "BsaError", "IDX_MASK_U8", "IDX_THRESHOLD_F32", "IDX_TOPK_F32", "build_index",
            "reorder_rows", "sample_blocks", "forward", "device_status", "resident_ctas",
            "effective_flops", "dense_attention_flops", "load_library", "lib_path", "EXPORTS",
-           "spectral_order", "spectral_order_workspace_size", "reorder_guard",
+           "spectral_order", "spectral_order_workspace_size", "spectral_order_noalloc",
+           "NOALLOC_SCRATCH_BYTES", "reorder_guard",
            "selftest_exp2", "selftest_wait_timeout", "math"]
