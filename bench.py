@@ -133,7 +133,7 @@ class ClockSampler:
 class Path:
     """Device buffers and the per-step launch sequence for one workload."""
 
-    def __init__(self, prob, dev, order: str):
+    def __init__(self, prob, dev, order: str, scores_on_gpu: bool = False, crm: bool = False):
         import long_context_mask_gb300 as bsa
         self.bsa = bsa
         self.prob = prob
@@ -156,6 +156,11 @@ class Path:
         else:
             self.mode, self.src, self.max_kv = None, None, 1
         self.k_per_row = cu(prob.k_per_row)
+        self.scores_on_gpu = scores_on_gpu and prob.scores is not None
+        if self.scores_on_gpu:
+            self.score_mode = bsa.SCORE_CENTROID_EXP if prob.m_sample else bsa.SCORE_MEAN_DOT
+            self.score_ws = torch.empty(max(1, bsa.load_library().bsa_block_scores_workspace_size(
+                prob.B, prob.H, prob.N, prob.D)), dtype=torch.uint8, device=dev)
         self.u = cu(prob.u)
         self.idx = torch.empty((rows, self.max_kv), dtype=torch.int32, device=dev)
         self.cnt = torch.empty(rows, dtype=torch.int32, device=dev)
@@ -168,6 +173,10 @@ class Path:
             self.s_idx = torch.empty((rows, cap), dtype=torch.int32, device=dev)
             self.s_cnt = torch.empty(rows, dtype=torch.int32, device=dev)
             self.lw = torch.empty((rows, cap), dtype=torch.float32, device=dev)
+        self.crm = crm and self.mode in (bsa.IDX_MASK_U8, bsa.IDX_THRESHOLD_F32)
+        if self.crm:
+            self.words = torch.empty((rows, (nqb + 31) // 32), dtype=torch.int32, device=dev)
+            order = self.order = "identity"
         self.row_perm = torch.empty((self.heads, nqb), dtype=torch.int32, device=dev)
         self.wave = bsa.resident_ctas(prob.D)
         if order == "spectral":
@@ -176,13 +185,20 @@ class Path:
             self.spec_ws = torch.empty(bsa.spectral_order_workspace_size(self.heads, nqb, nqb),
                                        dtype=torch.uint8, device=dev)
         self.launches_per_step = (1 + (self.mode is not None) + bool(prob.m_sample)
-                                  + (order != "identity") + (order == "spectral"))
+                                  + (order != "identity") + (order == "spectral")
+                                  + 2 * self.scores_on_gpu)
 
     def lists(self):
         return (self.s_idx, self.s_cnt) if self.prob.m_sample else (self.idx, self.cnt)
 
     def build_lists(self):
         bsa, p = self.bsa, self.prob
+        if self.crm:
+            bsa.build_crm(self.mode, self.src, self.words, p=p.p or 0.0)
+            return
+        if self.scores_on_gpu:
+            bsa.block_scores(self.q, self.k, self.src, q_map=self.q_map, kv_map=self.kv_map,
+                             mode=self.score_mode, workspace=self.score_ws)
         if self.mode is not None:
             bsa.build_index(self.mode, self.src, self.idx, self.cnt, p=p.p or 0.0,
                             k_per_row=self.k_per_row, k_const=p.k_const or 0)
@@ -199,6 +215,10 @@ class Path:
             bsa.reorder_rows(cnt.reshape(self.heads, p.nqb), self.wave, self.row_perm)
 
     def attend(self):
+        if self.crm:
+            self.bsa.forward_crm(self.q, self.k, self.v, self.words, self.o, self.lse,
+                                 q_map=self.q_map, kv_map=self.kv_map)
+            return
         idx, cnt = self.lists()
         self.bsa.forward(self.q, self.k, self.v, idx, cnt, self.o, self.lse, log_w=self.lw,
                          q_map=self.q_map, kv_map=self.kv_map,
@@ -209,6 +229,8 @@ class Path:
         self.attend()
 
     def effective_flops(self):
+        if self.crm:
+            self.bsa.build_index(self.mode, self.src, self.idx, self.cnt, p=self.prob.p or 0.0)
         _, cnt = self.lists()
         return self.bsa.effective_flops(cnt, self.prob.D)
 
@@ -277,6 +299,11 @@ def parse():
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller profiling case)")
     ap.add_argument("--order", default="reordered", choices=["reordered", "identity", "spectral"],
                     help="row order: NNZ-guided wave sort, identity, or spectral (stage 1) + wave sort")
+    ap.add_argument("--crm", action="store_true",
+                    help="mask / threshold workloads: CRM bitmask rows instead of index lists "
+                         "(identity row order)")
+    ap.add_argument("--scores-on-gpu", action="store_true",
+                    help="score blocks from Q/K inside the step (mean-pooled; centroid for --config 4)")
     ap.add_argument("--dense", action="store_true",
                     help="every query block attends to every KV block (the in-build dense ceiling)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -318,7 +345,9 @@ def config_dict(prob, config, order, density, world):
     return {"workload": name, "config_id": config, "B": prob.B, "H": prob.H,
             "N": prob.N, "D": prob.D, "block": 128, "density": round(density, 4), "order": order,
             "l2": "flushed between timed steps (256 MiB write)",
-            "parallelism": "one independent workload per GPU" if world > 1 else "single GPU"}
+            "parallelism": "one independent workload per GPU" if world > 1 else "single GPU",
+            "scores": "from Q/K inside the step" if getattr(prob, "_scores_on_gpu", False) else "given",
+            "kv_sets": "CRM bitmask rows" if getattr(prob, "_crm", False) else "index lists"}
 
 
 def run_reference(args, world, rank):
@@ -367,7 +396,9 @@ def main():
     import long_context_mask_gb300 as bsa
 
     prob = make_problem(args.config, args.heads, args.dense)
-    path = Path(prob, dev, args.order)
+    prob._scores_on_gpu = args.scores_on_gpu and prob.scores is not None
+    prob._crm = args.crm and (prob.mask is not None or prob.T is not None)
+    path = Path(prob, dev, args.order, args.scores_on_gpu, args.crm)
     path.step()
     torch.cuda.synchronize()
     if args.profile_once:
@@ -382,6 +413,8 @@ def main():
     torch.cuda.synchronize()
     flops = path.effective_flops()
     density = float(path.lists()[1].sum()) / (prob.rows * prob.nqb)
+    if path.crm:
+        args.order = "identity"
 
     uuid = str(torch.cuda.get_device_properties(dev).uuid)
     gpu_id = uuid if uuid.startswith("GPU-") else "GPU-" + uuid

@@ -41,6 +41,11 @@ typedef enum {
 } bsa_status;
 
 typedef enum {
+    BSA_SCORE_MEAN_DOT = 0,     /* mean(Q_u) . mean(K_v) * scale                     */
+    BSA_SCORE_CENTROID_EXP = 1  /* exp(mean(Q_u) . mean(K_v) * scale): centroid score */
+} bsa_score_mode;
+
+typedef enum {
     BSA_IDX_MASK_U8 = 0,       /* src: uint8 [rows, nKB], keep entries != 0             */
     BSA_IDX_THRESHOLD_F32 = 1, /* src: fp32 threshold map [rows, nKB], keep T <= p     */
     BSA_IDX_TOPK_F32 = 2       /* src: fp32 block scores [rows, nKB], keep the k largest */
@@ -77,6 +82,35 @@ typedef enum {
 bsa_status bsa_build_index(bsa_idx_mode mode, const void* src, int64_t rows, int32_t nKB,
                            float p, const int32_t* k_per_row, int32_t k_const,
                            int32_t* kv_idx, int32_t* kv_cnt, int32_t max_kv, void* stream);
+
+/*
+ * bsa_block_scores - per-head score of every (query block, KV block) pair
+ * from the blocks' mean vectors, the input of top-k selection and of
+ * importance sampling.
+ *
+ * Defined by: MC-Sparse, "The MC-Sparse Architecture" (block-sparse attention
+ * scores blocks by mean-pooled similarity); InstaGen, section 3.3 and
+ * Algorithm 1 step 2 (centroid score s_gc = exp(q_g . k_c / sqrt d) of a
+ * query group and a key cluster).  A group / cluster is a 128-token block of
+ * the gathered order (q_map / kv_map, identity when NULL).
+ *
+ *  q, k      device bf16 [B, H, N, D]; N a multiple of 128, D 8 .. 256 (x8).
+ *  q_map, kv_map  device int32 [B*H, N] or NULL (as in bsa_forward).
+ *  scale     <= 0 selects 1/sqrt(D).
+ *  mode      BSA_SCORE_MEAN_DOT or BSA_SCORE_CENTROID_EXP.
+ *  workspace device scratch of at least bsa_block_scores_workspace_size()
+ *            bytes (the fp32 block means), 16-byte aligned.
+ *  scores    device fp32 [B*H*nQB, nKB] out.
+ *  fp32 means and dot products; a map entry outside [0, N) is read as row 0
+ *  and raises BSA_ERR_BOUNDS.
+ */
+bsa_status bsa_block_scores(const void* q, const void* k, int32_t B, int32_t H, int32_t N,
+                            int32_t D, const int32_t* q_map, const int32_t* kv_map, float scale,
+                            bsa_score_mode mode, void* workspace, size_t workspace_bytes,
+                            float* scores, void* stream);
+
+/* Bytes of workspace bsa_block_scores needs (0 for sizes it rejects). */
+size_t bsa_block_scores_workspace_size(int32_t B, int32_t H, int32_t N, int32_t D);
 
 /*
  * bsa_reorder_rows - query-row execution order, NNZ-guided within waves.
@@ -184,7 +218,9 @@ bsa_status bsa_spectral_order_noalloc(const int32_t* kv_idx, const int32_t* kv_c
  * running sum of pi.  lambda, pi and C are fp64, summed in ascending block
  * order without fused multiply-adds, so the drawn set is reproducible.
  *
- *  scores       device fp32 [rows, nKB], every entry > 0.
+ *  scores       device fp32 [rows, nKB], every entry > 0; or NULL for the
+ *               uniform sampler (InstaGen Algorithm 1 steps 6-8): every
+ *               residual block gets pi = m / |residual|.
  *  exact_idx    device int32 [rows, exact_stride]: exact blocks, ascending.
  *  exact_cnt    device int32 [rows].
  *  exact_stride row stride of exact_idx, >= 1.
@@ -251,6 +287,52 @@ bsa_status bsa_forward(const void* q, const void* k, const void* v, int32_t B, i
                        int32_t max_kv, const float* log_w, const int32_t* q_map,
                        const int32_t* kv_map, const int32_t* row_perm, float scale, void* o,
                        float* lse, void* stream);
+
+/*
+ * bsa_build_crm - the CRM (compressed row mask) form of a mask or threshold
+ * map: per row, uint32 words in which bit i of word w is set when KV block
+ * 32w + i is kept (ScalingAttention, section 7.2: one 32-bit load decodes 32
+ * block states).  Same selection as bsa_build_index (MASK / THRESHOLD);
+ * bits at or beyond nKB are 0.
+ *
+ *  words      device uint32 [rows, crm_words] out; crm_words >= ceil(nKB/32)
+ *             (words beyond ceil(nKB/32) are written as 0).
+ */
+bsa_status bsa_build_crm(bsa_idx_mode mode, const void* src, int64_t rows, int32_t nKB, float p,
+                         uint32_t* words, int32_t crm_words, void* stream);
+
+/*
+ * bsa_forward_crm - bsa_forward with the KV-block sets given as CRM rows.
+ *
+ * Defined by: ScalingAttention, sections 7.2-7.3 (CRM rows walked with bit
+ * scan and bit clear in place of the dense block iterator; Algorithm 2).
+ * The forward pass visits the set bits of each row in ascending block order
+ * (count trailing zeros, then clear the lowest bit); results equal
+ * bsa_forward on the equivalent index lists.  No per-block log-weights.
+ *
+ *  crm        device uint32 [B*H*nQB, crm_words], crm_words >= ceil(nKB/32);
+ *             bits at or beyond nKB must be 0 (else BSA_ERR_BOUNDS, row
+ *             unspecified).  Other arguments as bsa_forward.
+ */
+bsa_status bsa_forward_crm(const void* q, const void* k, const void* v, int32_t B, int32_t H,
+                           int32_t N, int32_t D, const uint32_t* crm, int32_t crm_words,
+                           const int32_t* q_map, const int32_t* kv_map, const int32_t* row_perm,
+                           float scale, void* o, float* lse, void* stream);
+
+/*
+ * bsa_upscale_threshold - carry a threshold map built at a base resolution
+ * to a target resolution (ScalingAttention, section 7.1 eq. (7),
+ * R_target(u, v) = ceil(Phi(R_base, u / s_h, v / s_w)), Phi bilinear).
+ *
+ * Target block u samples base coordinate u * Ub / Ut (likewise v); on every
+ * mask M_p = I(T <= p) the ceiling keeps a target block when any base block
+ * with a nonzero bilinear weight is active, so the target threshold is the
+ * minimum of T over those (one or two per axis, the upper index clamped).
+ *
+ *  T_base    device fp32 [heads, Ub, Vb];  T_target device fp32 [heads, Ut, Vt] out.
+ */
+bsa_status bsa_upscale_threshold(const float* T_base, int64_t heads, int32_t Ub, int32_t Vb,
+                                 int32_t Ut, int32_t Vt, float* T_target, void* stream);
 
 /*
  * bsa_device_status - read and clear the status word of the current device.

@@ -13,12 +13,17 @@ from .binding import (  # noqa: F401
     IDX_MASK_U8,
     IDX_THRESHOLD_F32,
     IDX_TOPK_F32,
+    SCORE_CENTROID_EXP,
+    SCORE_MEAN_DOT,
+    block_scores,
     NOALLOC_SCRATCH_BYTES,
+    build_crm,
     build_index,
     dense_attention_flops,
     device_status,
     effective_flops,
     forward,
+    forward_crm,
     lib_path,
     load_library,
     reorder_guard,
@@ -30,4 +35,5 @@ from .binding import (  # noqa: F401
     spectral_order,
     spectral_order_noalloc,
     spectral_order_workspace_size,
+    upscale_threshold,
 )

@@ -20,7 +20,9 @@ STATUS_NAMES = {0: "BSA_OK", 1: "BSA_ERR_INVALID_ARG", 2: "BSA_ERR_UNSUPPORTED",
                 3: "BSA_ERR_OVERFLOW", 4: "BSA_ERR_CUDA", 5: "BSA_ERR_TIMEOUT",
                 6: "BSA_ERR_BOUNDS"}
 
-EXPORTS = ("bsa_build_index", "bsa_reorder_rows", "bsa_spectral_order",
+EXPORTS = ("bsa_build_index", "bsa_build_crm", "bsa_forward_crm", "bsa_upscale_threshold",
+           "bsa_block_scores", "bsa_block_scores_workspace_size",
+           "bsa_reorder_rows", "bsa_spectral_order",
            "bsa_spectral_order_workspace_size", "bsa_spectral_order_noalloc", "bsa_sample_blocks",
            "bsa_forward",
            "bsa_device_status", "bsa_resident_ctas", "bsa_status_string", "bsa_selftest_exp2",
@@ -51,6 +53,17 @@ def load_library():
     P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
     lib.bsa_build_index.argtypes = [i32, P, i64, i32, f32, P, i32, P, P, i32, P]
     lib.bsa_reorder_rows.argtypes = [P, P, i64, i32, i32, P, P]
+    lib.bsa_build_crm.argtypes = [i32, P, i64, i32, f32, P, i32, P]
+    lib.bsa_build_crm.restype = i32
+    lib.bsa_forward_crm.argtypes = [P, P, P, i32, i32, i32, i32, P, i32, P, P, P, f32, P, P, P]
+    lib.bsa_forward_crm.restype = i32
+    lib.bsa_upscale_threshold.argtypes = [P, i64, i32, i32, i32, i32, P, P]
+    lib.bsa_upscale_threshold.restype = i32
+    lib.bsa_block_scores.argtypes = [P, P, i32, i32, i32, i32, P, P, f32, i32, P, ctypes.c_size_t,
+                                     P, P]
+    lib.bsa_block_scores.restype = i32
+    lib.bsa_block_scores_workspace_size.argtypes = [i32, i32, i32, i32]
+    lib.bsa_block_scores_workspace_size.restype = ctypes.c_size_t
     lib.bsa_sample_blocks.argtypes = [P, i64, i32, P, P, i32, i32, P, P, P, P, i32, P]
     lib.bsa_spectral_order.argtypes = [P, P, i32, i64, i32, i32, i32, P, P, ctypes.c_size_t, P, P,
                                        P, P]
@@ -113,6 +126,65 @@ def build_index(mode: int, src, kv_idx, kv_cnt, *, p: float = 0.0, k_per_row=Non
                                           int(k_const), _ptr(kv_idx), _ptr(kv_cnt),
                                           kv_idx.shape[1], _stream(stream))
     _check("bsa_build_index", code)
+
+
+SCORE_MEAN_DOT, SCORE_CENTROID_EXP = 0, 1
+
+
+def block_scores(q, k, scores, *, q_map=None, kv_map=None, scale: float = 0.0,
+                 mode: int = SCORE_MEAN_DOT, workspace=None, stream=None):
+    """scores [B*H*nQB, nKB] fp32 from the block means of Q and K (see bsa.h)."""
+    import torch
+    _dtype(q, "q", torch.bfloat16)
+    _dtype(k, "k", torch.bfloat16)
+    _dtype(scores, "scores", torch.float32)
+    B, H, N, D = q.shape
+    lib = load_library()
+    need = int(lib.bsa_block_scores_workspace_size(B, H, N, D))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    nbytes = workspace.numel() * workspace.element_size()
+    code = lib.bsa_block_scores(_ptr(q), _ptr(k), B, H, N, D, _ptr(q_map), _ptr(kv_map),
+                                float(scale), int(mode), _ptr(workspace), nbytes, _ptr(scores),
+                                _stream(stream))
+    _check("bsa_block_scores", code)
+
+
+def build_crm(mode: int, src, words, *, p: float = 0.0, stream=None):
+    """CRM rows (uint32 [rows, n_words], viewed as int32 in torch) from a mask /
+    threshold map [rows, nKB]."""
+    import torch
+    _dtype(src, "src", torch.uint8 if mode == IDX_MASK_U8 else torch.float32)
+    _dtype(words, "words", torch.int32)
+    rows, nkb = src.shape
+    _check("bsa_build_crm", load_library().bsa_build_crm(mode, _ptr(src), rows, nkb, float(p),
+                                                         _ptr(words), words.shape[1],
+                                                         _stream(stream)))
+
+
+def forward_crm(q, k, v, crm, o, lse, *, q_map=None, kv_map=None, row_perm=None,
+                scale: float = 0.0, stream=None):
+    """bsa_forward with CRM rows (int32-viewed uint32 [B*H*nQB, n_words])."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _dtype(t, n, torch.bfloat16)
+    _dtype(crm, "crm", torch.int32)
+    B, H, N, D = q.shape
+    code = load_library().bsa_forward_crm(_ptr(q), _ptr(k), _ptr(v), B, H, N, D, _ptr(crm),
+                                          crm.shape[1], _ptr(q_map), _ptr(kv_map), _ptr(row_perm),
+                                          float(scale), _ptr(o), _ptr(lse), _stream(stream))
+    _check("bsa_forward_crm", code)
+
+
+def upscale_threshold(T_base, T_target, *, stream=None):
+    """[heads, Ub, Vb] -> [heads, Ut, Vt] threshold maps (eq. 7)."""
+    import torch
+    _dtype(T_base, "T_base", torch.float32)
+    _dtype(T_target, "T_target", torch.float32)
+    heads, ub, vb = T_base.shape
+    _, ut, vt = T_target.shape
+    _check("bsa_upscale_threshold", load_library().bsa_upscale_threshold(
+        _ptr(T_base), heads, ub, vb, ut, vt, _ptr(T_target), _stream(stream)))
 
 
 def reorder_rows(kv_cnt, wave: int, row_perm, *, order_in=None, stream=None):
@@ -179,12 +251,17 @@ def reorder_guard(N: int, D: int, l2_bytes: int) -> bool:
     return 2 * N * D * 2 > l2_bytes
 
 
-def sample_blocks(scores, exact_idx, exact_cnt, m: int, u, kv_idx, kv_cnt, log_w, *, stream=None):
-    """Exact list + PPSWOR sample with log-weights (InstaGen section 3.2.1)."""
+def sample_blocks(scores, exact_idx, exact_cnt, m: int, u, kv_idx, kv_cnt, log_w, *, nkb=None,
+                  stream=None):
+    """Exact list + PPSWOR sample with log-weights (InstaGen section 3.2.1).
+    scores None selects the uniform sampler (then pass nkb)."""
     import torch
     _dtype(scores, "scores", torch.float32)
     _dtype(u, "u", torch.float64)
-    rows, nkb = scores.shape
+    if scores is None:
+        rows = exact_cnt.shape[0]
+    else:
+        rows, nkb = scores.shape
     code = load_library().bsa_sample_blocks(_ptr(scores), rows, nkb, _ptr(exact_idx),
                                             _ptr(exact_cnt), exact_idx.shape[1], int(m), _ptr(u),
                                             _ptr(kv_idx), _ptr(kv_cnt), _ptr(log_w),
@@ -255,6 +332,8 @@ def dense_attention_flops(N: int, H: int, D: int, causal: bool = False, B: int =
 __all__ = ["BLOCK", "BsaError", "IDX_MASK_U8", "IDX_THRESHOLD_F32", "IDX_TOPK_F32", "build_index",
            "reorder_rows", "sample_blocks", "forward", "device_status", "resident_ctas",
            "effective_flops", "dense_attention_flops", "load_library", "lib_path", "EXPORTS",
+           "block_scores", "SCORE_MEAN_DOT", "SCORE_CENTROID_EXP", "build_crm", "forward_crm",
+           "upscale_threshold",
            "spectral_order", "spectral_order_workspace_size", "spectral_order_noalloc",
            "NOALLOC_SCRATCH_BYTES", "reorder_guard",
            "selftest_exp2", "selftest_wait_timeout", "math"]

@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbsa.so")
-SOURCES = ["bsa_api.cu", "bsa_index.cu", "bsa_order.cu", "bsa_attn.cu", "bsa_selftest.cu",
+SOURCES = ["bsa_api.cu", "bsa_index.cu", "bsa_scores.cu", "bsa_order.cu", "bsa_attn.cu",
+           "bsa_selftest.cu",
            "bsa_noalloc.cu"]
 HEADERS = ["bsa_internal.h", "bsa_ptx.cuh", "bsa_math.cuh"]
 

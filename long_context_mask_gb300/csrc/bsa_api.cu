@@ -96,6 +96,37 @@ bsa_status bsa_reorder_rows(const int32_t* kv_cnt, const int32_t* order_in, int6
     return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
+static bool score_sizes_ok(int32_t B, int32_t H, int32_t N, int32_t D) {
+    return B >= 1 && H >= 1 && (int64_t)B * H <= 65535 && N >= 128 && (N % 128) == 0 &&
+           N <= (1 << 24) && (int64_t)B * H * N < ((int64_t)1 << 31) && D >= 8 && D <= 256 &&
+           (D % 8) == 0;
+}
+
+size_t bsa_block_scores_workspace_size(int32_t B, int32_t H, int32_t N, int32_t D) {
+    if (!score_sizes_ok(B, H, N, D)) return 0;
+    return bsa::block_scores_workspace_bytes((int64_t)B * H, N, D);
+}
+
+bsa_status bsa_block_scores(const void* q, const void* k, int32_t B, int32_t H, int32_t N,
+                            int32_t D, const int32_t* q_map, const int32_t* kv_map, float scale,
+                            bsa_score_mode mode, void* workspace, size_t workspace_bytes,
+                            float* scores, void* stream) {
+    if (!score_sizes_ok(B, H, N, D)) return BSA_ERR_INVALID_ARG;
+    if (mode != BSA_SCORE_MEAN_DOT && mode != BSA_SCORE_CENTROID_EXP) return BSA_ERR_INVALID_ARG;
+    if (!q || !k || !scores || !workspace) return BSA_ERR_INVALID_ARG;
+    if (workspace_bytes < bsa::block_scores_workspace_bytes((int64_t)B * H, N, D))
+        return BSA_ERR_INVALID_ARG;
+    if (!aligned(q, 2) || !aligned(k, 2) || !aligned(scores, 4) || !aligned(workspace, 16) ||
+        (q_map && !aligned(q_map, 4)) || (kv_map && !aligned(kv_map, 4)))
+        return BSA_ERR_INVALID_ARG;
+    int32_t* status = bsa::status_word_ptr();
+    if (!status) return BSA_ERR_CUDA;
+    cudaError_t e = bsa::launch_block_scores(q, k, B, H, N, D, q_map, kv_map, scale, (int32_t)mode,
+                                             static_cast<float*>(workspace), scores, status,
+                                             static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
 static bool spectral_sizes_ok(int64_t heads, int32_t nQB, int32_t nKB) {
     return heads >= 0 && heads <= 65535 && nQB >= 2 && nQB <= 8192 && nKB >= 1 && nKB <= 65536;
 }
@@ -134,9 +165,9 @@ bsa_status bsa_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
     if (rows < 0 || nKB < 1 || nKB > 4096 || exact_stride < 1 || m < 0 || max_kv < 1)
         return BSA_ERR_INVALID_ARG;
     if (rows == 0) return BSA_OK;
-    if (!scores || !exact_idx || !exact_cnt || !u || !kv_idx || !kv_cnt || !log_w)
-        return BSA_ERR_INVALID_ARG;
-    if (!aligned(scores, 4) || !aligned(exact_idx, 4) || !aligned(exact_cnt, 4) || !aligned(u, 8) ||
+    if (!exact_idx || !exact_cnt || !u || !kv_idx || !kv_cnt || !log_w)
+        return BSA_ERR_INVALID_ARG;  // scores may be NULL: the uniform sampler
+    if ((scores && !aligned(scores, 4)) || !aligned(exact_idx, 4) || !aligned(exact_cnt, 4) || !aligned(u, 8) ||
         !aligned(kv_idx, 4) || !aligned(kv_cnt, 4) || !aligned(log_w, 4))
         return BSA_ERR_INVALID_ARG;
     int32_t* status = bsa::status_word_ptr();
@@ -167,9 +198,57 @@ bsa_status bsa_forward(const void* q, const void* k, const void* v, int32_t B, i
         return BSA_ERR_INVALID_ARG;
     int32_t* status = bsa::status_word_ptr();
     if (!status) return BSA_ERR_CUDA;
-    bsa::ForwardArgs a{q,      k,     v,     B,       H,      N,        D,     kv_idx,
-                       kv_cnt, max_kv, log_w, q_map, kv_map, row_perm, scale, o,     lse};
+    bsa::ForwardArgs a{q,      k,      v,     B,     H,      N,        D,     kv_idx, kv_cnt,
+                       max_kv, log_w, q_map, kv_map, row_perm, scale, o,     lse,    nullptr, 0};
     return bsa::launch_forward(a, status, static_cast<cudaStream_t>(stream));
+}
+
+bsa_status bsa_forward_crm(const void* q, const void* k, const void* v, int32_t B, int32_t H,
+                           int32_t N, int32_t D, const uint32_t* crm, int32_t crm_words,
+                           const int32_t* q_map, const int32_t* kv_map, const int32_t* row_perm,
+                           float scale, void* o, float* lse, void* stream) {
+    if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+    if (B < 1 || H < 1 || N < 128 || (N % 128) != 0 || N > (1 << 24)) return BSA_ERR_INVALID_ARG;
+    const int64_t total_rows = (int64_t)B * H * N;
+    if (total_rows >= ((int64_t)1 << 31) || (int64_t)B * H > 65535) return BSA_ERR_INVALID_ARG;
+    const int32_t nKB = N / 128;
+    if (crm_words < (nKB + 31) / 32 || crm_words > (1 << 20)) return BSA_ERR_INVALID_ARG;
+    if (!q || !k || !v || !crm || !o || !lse) return BSA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+        !aligned(crm, 4) || !aligned(lse, 4) || (row_perm && !aligned(row_perm, 4)) ||
+        (q_map && !aligned(q_map, 16)) || (kv_map && !aligned(kv_map, 16)))
+        return BSA_ERR_INVALID_ARG;
+    int32_t* status = bsa::status_word_ptr();
+    if (!status) return BSA_ERR_CUDA;
+    bsa::ForwardArgs a{q,   k,      v,     B,     H,      N,        D,     nullptr, nullptr,
+                       nKB, nullptr, q_map, kv_map, row_perm, scale, o,     lse,     crm, crm_words};
+    return bsa::launch_forward(a, status, static_cast<cudaStream_t>(stream));
+}
+
+bsa_status bsa_build_crm(bsa_idx_mode mode, const void* src, int64_t rows, int32_t nKB, float p,
+                         uint32_t* words, int32_t crm_words, void* stream) {
+    if (mode != BSA_IDX_MASK_U8 && mode != BSA_IDX_THRESHOLD_F32) return BSA_ERR_INVALID_ARG;
+    if (rows < 0 || rows > ((int64_t)1 << 40) || nKB < 1 || nKB > 65536 ||
+        crm_words < (nKB + 31) / 32 || crm_words > (1 << 20))
+        return BSA_ERR_INVALID_ARG;
+    if (rows == 0) return BSA_OK;
+    if (!src || !words || !aligned(words, 4) || (mode != BSA_IDX_MASK_U8 && !aligned(src, 4)))
+        return BSA_ERR_INVALID_ARG;
+    cudaError_t e = bsa::launch_crm_rows(mode, src, rows, nKB, p, words, crm_words,
+                                         static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
+bsa_status bsa_upscale_threshold(const float* T_base, int64_t heads, int32_t Ub, int32_t Vb,
+                                 int32_t Ut, int32_t Vt, float* T_target, void* stream) {
+    if (heads < 0 || heads > 65535 || Ub < 1 || Vb < 1 || Ut < 1 || Vt < 1 || Ub > 65536 ||
+        Vb > 65536 || Ut > 65536 || Vt > 65536)
+        return BSA_ERR_INVALID_ARG;
+    if (heads == 0) return BSA_OK;
+    if (!T_base || !T_target || !aligned(T_base, 4) || !aligned(T_target, 4)) return BSA_ERR_INVALID_ARG;
+    cudaError_t e = bsa::launch_upscale_threshold(T_base, heads, Ub, Vb, Ut, Vt, T_target,
+                                                  static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
 bsa_status bsa_device_status(void* stream, int32_t* first_error) {

@@ -115,6 +115,8 @@ struct Params {
     const int32_t* q_map;
     const int32_t* kv_map;
     const int32_t* row_perm;
+    const uint32_t* crm;  // CRM rows [rows, crm_words] (the CRM variant only)
+    int32_t crm_words;
     __nv_bfloat16* o;
     float* lse;
     int32_t* status;
@@ -184,7 +186,23 @@ __device__ __forceinline__ int32_t ring_pos_v(int32_t i, int32_t n) {
     return lead + i + mid;
 }
 
-template <int D, int kPoly>
+// Next set bit of a CRM row (ScalingAttention section 7.3, Algorithm 2:
+// ADVANCE to the next nonzero word, INDEX by count-trailing-zeros, NEXT by
+// clearing the lowest set bit).  Warp-uniform.
+struct CrmIter {
+    const uint32_t* words;
+    int32_t n_words, w;
+    uint32_t val;
+    __device__ __forceinline__ int32_t next() {
+        while (val == 0u && w + 1 < n_words) val = words[++w];
+        if (val == 0u) return -1;  // exhausted (cannot happen for a consistent count)
+        const int32_t bit = __ffs(val) - 1;
+        val &= val - 1u;
+        return 32 * w + bit;
+    }
+};
+
+template <int D, int kPoly, bool kCrm>
 __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_constant__ Params P) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -211,16 +229,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
         }
     }
     const int64_t row = bh * nQB + qb;
-    int32_t n = P.kv_cnt[row];
-    if (n > max_kv) {
-        if (threadIdx.x == 0) raise_status(P.status, BSA_ERR_OVERFLOW);
-        n = max_kv;
+    int32_t n;
+    const int32_t* list = nullptr;
+    const uint32_t* crm_row = nullptr;
+    if constexpr (kCrm) {
+        // count = popcount of the row's words (every warp computes it)
+        crm_row = P.crm + row * P.crm_words;
+        int32_t c = 0;
+        for (int32_t w = lane; w < P.crm_words; w += 32) c += __popc(crm_row[w]);
+        n = __reduce_add_sync(0xffffffffu, c);
+    } else {
+        n = P.kv_cnt[row];
+        if (n > max_kv) {
+            if (threadIdx.x == 0) raise_status(P.status, BSA_ERR_OVERFLOW);
+            n = max_kv;
+        }
+        if (n < 0) {
+            if (threadIdx.x == 0) raise_status(P.status, BSA_ERR_BOUNDS);
+            n = 0;
+        }
+        list = P.kv_idx + row * max_kv;
     }
-    if (n < 0) {
-        if (threadIdx.x == 0) raise_status(P.status, BSA_ERR_BOUNDS);
-        n = 0;
-    }
-    const int32_t* list = P.kv_idx + row * max_kv;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -270,8 +299,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
             }
             return __shfl_sync(0xffffffffu, kb_lane, e - chunk_base);
         };
+        CrmIter it_k{crm_row, P.crm_words, -1, 0u}, it_v{crm_row, P.crm_words, -1, 0u};
         auto put = [&](int32_t e, bool is_v) -> bool {
-            const int32_t kb = block_kb(e);
+            int32_t kb;
+            if constexpr (kCrm) {
+                // K tiles are fetched in block order and V tiles trail them: one
+                // bit iterator per stream
+                kb = is_v ? it_v.next() : it_k.next();
+                if (kb < 0 || kb >= nKB) {
+                    if (lane == 0) raise_status(P.status, BSA_ERR_BOUNDS);
+                    kb = 0;
+                }
+            } else {
+                kb = block_kb(e);
+            }
             const int32_t slot = issued % C::kStages;
             const uint32_t phase = (uint32_t)(issued / C::kStages) & 1u;
             int w = 1;
@@ -555,7 +596,7 @@ size_t smem_bytes() {
     return 1024 + Cfg<D>::kData + sizeof(Barriers);
 }
 
-template <int D, int kPoly>
+template <int D, int kPoly, bool kCrm>
 cudaError_t prepare_kernel() {
     // Per device: opt in to the large dynamic shared-memory carve-out.
     static int done[64] = {0};
@@ -563,28 +604,28 @@ cudaError_t prepare_kernel() {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(k_bsa_forward<D, kPoly>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k_bsa_forward<D, kPoly, kCrm>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem_bytes<D>());
     if (e == cudaSuccess && dev < 64) done[dev] = 1;
     return e;
 }
 
 // Share of exponentials (out of every 8) computed by exp2_fma instead of
-// the MUFU unit.  BSA_EXP2_POLY=<0|2|3|4> overrides it (tuning).
+// the MUFU unit.  BSA_EXP2_POLY=<0|2> overrides it (tuning).
 int poly_setting() {
     static int v = -1;
     if (v < 0) {
         const char* s = getenv("BSA_EXP2_POLY");
         v = kDefaultPoly;
-        if (s && (s[0] == '0' || s[0] == '2' || s[0] == '3' || s[0] == '4') && s[1] == 0) v = s[0] - '0';
+        if (s && (s[0] == '0' || s[0] == '2') && s[1] == 0) v = s[0] - '0';
     }
     return v;
 }
 
-template <int D, int kPoly>
+template <int D, int kPoly, bool kCrm>
 bsa_status launch_dp(const Params& P, unsigned grid_x, unsigned grid_y, cudaStream_t stream) {
-    if (prepare_kernel<D, kPoly>() != cudaSuccess) return BSA_ERR_CUDA;
-    k_bsa_forward<D, kPoly><<<dim3(grid_x, grid_y), kThreads, smem_bytes<D>(), stream>>>(P);
+    if (prepare_kernel<D, kPoly, kCrm>() != cudaSuccess) return BSA_ERR_CUDA;
+    k_bsa_forward<D, kPoly, kCrm><<<dim3(grid_x, grid_y), kThreads, smem_bytes<D>(), stream>>>(P);
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
@@ -603,6 +644,8 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
     P.q_map = a.q_map;
     P.kv_map = a.kv_map;
     P.row_perm = a.row_perm;
+    P.crm = a.crm;
+    P.crm_words = a.crm_words;
     P.o = static_cast<__nv_bfloat16*>(a.o);
     P.lse = a.lse;
     P.status = status;
@@ -612,19 +655,16 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
     const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
     P.scale_log2 = scale * kLog2e;
     const unsigned gx = (unsigned)P.nQB, gy = (unsigned)(a.B * a.H);
-    switch (poly_setting()) {
-        case 0: return launch_dp<D, 0>(P, gx, gy, stream);
-        case 2: return launch_dp<D, 2>(P, gx, gy, stream);
-        case 3: return launch_dp<D, 3>(P, gx, gy, stream);
-        default: return launch_dp<D, 4>(P, gx, gy, stream);
-    }
+    if (a.crm != nullptr) return launch_dp<D, kDefaultPoly, true>(P, gx, gy, stream);
+    return poly_setting() == 2 ? launch_dp<D, 2, false>(P, gx, gy, stream)
+                               : launch_dp<D, 0, false>(P, gx, gy, stream);
 }
 
 template <int D>
 int32_t occupancy() {
     int per_sm = 0;
-    if (prepare_kernel<D, kDefaultPoly>() != cudaSuccess) return -1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bsa_forward<D, kDefaultPoly>, kThreads,
+    if (prepare_kernel<D, kDefaultPoly, false>() != cudaSuccess) return -1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bsa_forward<D, kDefaultPoly, false>, kThreads,
                                                       smem_bytes<D>()) != cudaSuccess)
         return -1;
     return per_sm;

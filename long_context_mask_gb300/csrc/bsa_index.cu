@@ -71,6 +71,46 @@ __global__ void __launch_bounds__(256) k_index_predicate(const void* __restrict_
     }
 }
 
+// ------------------------------------------------------------ CRM rows
+// The ballot word of each 32-block chunk is the row's CRM word (ScalingAttention
+// section 7.2): one warp per row, lane 0 stores the word.
+template <int MODE>
+__global__ void __launch_bounds__(256) k_crm_rows(const void* __restrict__ src, int64_t rows,
+                                                  int32_t nKB, float p, uint32_t* __restrict__ words,
+                                                  int32_t n_words) {
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const int64_t base_in = row * (int64_t)nKB;
+    for (int32_t w = 0; w < n_words; ++w) {
+        const int32_t kb = 32 * w + lane;
+        const bool keep = kb < nKB && keep_block<MODE>(src, base_in + kb, p);
+        const uint32_t word = __ballot_sync(kFull, keep);
+        if (lane == 0) words[row * (int64_t)n_words + w] = word;
+    }
+}
+
+// ------------------------------------------------------------ eq. (7) upscaling
+// Target (u, v) samples base (u Ub / Ut, v Vb / Vt); the lower neighbour always
+// has a nonzero bilinear weight, the upper one only when the coordinate is
+// fractional (integer test).  The ceiling rule on every mask M_p = I(T <= p)
+// is the minimum of T over the neighbours with nonzero weight.
+__global__ void k_upscale_threshold(const float* __restrict__ T, int32_t Ub, int32_t Vb, int32_t Ut,
+                                    int32_t Vt, float* __restrict__ out) {
+    const int64_t h = blockIdx.z;
+    const int32_t u = blockIdx.y;
+    const int32_t v = blockIdx.x * blockDim.x + threadIdx.x;
+    if (v >= Vt) return;
+    const int64_t xu = (int64_t)u * Ub, yv = (int64_t)v * Vb;
+    const int32_t i0 = (int32_t)(xu / Ut), j0 = (int32_t)(yv / Vt);
+    const int32_t i1 = (xu % Ut != 0 && i0 + 1 < Ub) ? i0 + 1 : i0;
+    const int32_t j1 = (yv % Vt != 0 && j0 + 1 < Vb) ? j0 + 1 : j0;
+    const float* b = T + h * (int64_t)Ub * Vb;
+    const float m = fminf(fminf(b[(int64_t)i0 * Vb + j0], b[(int64_t)i0 * Vb + j1]),
+                          fminf(b[(int64_t)i1 * Vb + j0], b[(int64_t)i1 * Vb + j1]));
+    out[(h * Ut + u) * (int64_t)Vt + v] = m;
+}
+
 // ------------------------------------------------------------ top-k
 // Order-preserving map fp32 -> uint32 (larger float -> larger key); -0 == +0.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -179,7 +219,8 @@ __global__ void __launch_bounds__(128) k_sample_blocks(
     float* __restrict__ log_w, int32_t max_kv, int32_t* status) {
     const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (row >= rows) return;
-    const float* s = scores + row * (int64_t)nKB;
+    // NULL scores: the uniform sampler, every residual block scored 1
+    const float* s = scores ? scores + row * (int64_t)nKB : nullptr;
     uint32_t ex[kWords], taken[kWords], drawn[kWords];  // exact / exact+promoted / drawn
     const int32_t nw = (nKB + 31) >> 5;
     for (int32_t w = 0; w < nw; ++w) ex[w] = taken[w] = drawn[w] = 0u;
@@ -205,11 +246,11 @@ __global__ void __launch_bounds__(128) k_sample_blocks(
         for (;;) {
             double sum = 0.0;
             for (int32_t kb = 0; kb < nKB; ++kb)
-                if (!bit_get(taken, kb)) sum = __dadd_rn(sum, (double)s[kb]);
+                if (!bit_get(taken, kb)) sum = __dadd_rn(sum, s ? (double)s[kb] : 1.0);
             lambda = __ddiv_rn((double)(m - n_cap), sum);
             bool grew = false;
             for (int32_t kb = 0; kb < nKB; ++kb) {
-                if (!bit_get(taken, kb) && __dmul_rn(lambda, (double)s[kb]) >= 1.0) {
+                if (!bit_get(taken, kb) && __dmul_rn(lambda, s ? (double)s[kb] : 1.0) >= 1.0) {
                     bit_set(taken, kb);
                     ++n_cap;
                     grew = true;
@@ -224,7 +265,7 @@ __global__ void __launch_bounds__(128) k_sample_blocks(
         int32_t nd = 0;
         for (int32_t kb = 0; kb < nKB; ++kb) {
             if (bit_get(taken, kb)) continue;
-            const double pj = __dmul_rn(lambda, (double)s[kb]);
+            const double pj = __dmul_rn(lambda, s ? (double)s[kb] : 1.0);
             const double C_prev = C;
             C = __dadd_rn(C, pj);
             if (nd < m_rest && ceil(__dsub_rn(C, ur)) > ceil(__dsub_rn(C_prev, ur))) {
@@ -241,7 +282,7 @@ __global__ void __launch_bounds__(128) k_sample_blocks(
         if (!t && !d) continue;
         if (n < max_kv) {
             out[n] = kb;
-            lw[n] = d ? (float)(-log(__dmul_rn(lambda, (double)s[kb]))) : 0.0f;
+            lw[n] = d ? (float)(-log(__dmul_rn(lambda, s ? (double)s[kb] : 1.0))) : 0.0f;
             ++n;
         }
         ++total;
@@ -269,6 +310,25 @@ cudaError_t launch_index_predicate(bsa_idx_mode mode, const void* src, int64_t r
     else
         k_index_predicate<BSA_IDX_THRESHOLD_F32><<<grid, warps * 32, 0, stream>>>(
             src, rows, nKB, p, kv_idx, kv_cnt, max_kv, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_crm_rows(bsa_idx_mode mode, const void* src, int64_t rows, int32_t nKB, float p,
+                            uint32_t* words, int32_t n_words, cudaStream_t stream) {
+    if (rows == 0) return cudaSuccess;
+    const dim3 grid((unsigned)((rows + 7) / 8));
+    if (mode == BSA_IDX_MASK_U8)
+        k_crm_rows<BSA_IDX_MASK_U8><<<grid, 256, 0, stream>>>(src, rows, nKB, p, words, n_words);
+    else
+        k_crm_rows<BSA_IDX_THRESHOLD_F32><<<grid, 256, 0, stream>>>(src, rows, nKB, p, words, n_words);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_upscale_threshold(const float* T, int64_t heads, int32_t Ub, int32_t Vb,
+                                     int32_t Ut, int32_t Vt, float* out, cudaStream_t stream) {
+    if (heads == 0) return cudaSuccess;
+    const dim3 grid((unsigned)((Vt + 127) / 128), (unsigned)Ut, (unsigned)heads);
+    k_upscale_threshold<<<grid, 128, 0, stream>>>(T, Ub, Vb, Ut, Vt, out);
     return cudaGetLastError();
 }
 

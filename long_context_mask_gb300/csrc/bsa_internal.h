@@ -22,6 +22,10 @@ cudaError_t launch_index_topk(const float* scores, int64_t rows, int32_t nKB,
                               const int32_t* k_per_row, int32_t k_const, int32_t* kv_idx,
                               int32_t* kv_cnt, int32_t max_kv, int32_t* status,
                               cudaStream_t stream);
+cudaError_t launch_crm_rows(bsa_idx_mode mode, const void* src, int64_t rows, int32_t nKB, float p,
+                            uint32_t* words, int32_t n_words, cudaStream_t stream);
+cudaError_t launch_upscale_threshold(const float* T, int64_t heads, int32_t Ub, int32_t Vb,
+                                     int32_t Ut, int32_t Vt, float* out, cudaStream_t stream);
 cudaError_t launch_reorder_rows(const int32_t* kv_cnt, const int32_t* order_in, int64_t heads,
                                 int32_t nQB, int32_t wave, int32_t* row_perm, int32_t* status,
                                 cudaStream_t stream);
@@ -30,6 +34,13 @@ cudaError_t launch_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
                                  int32_t exact_stride, int32_t m, const double* u,
                                  int32_t* kv_idx, int32_t* kv_cnt, float* log_w, int32_t max_kv,
                                  int32_t* status, cudaStream_t stream);
+
+// bsa_scores.cu
+size_t block_scores_workspace_bytes(int64_t BH, int32_t N, int32_t D);
+cudaError_t launch_block_scores(const void* q, const void* k, int32_t B, int32_t H, int32_t N,
+                                int32_t D, const int32_t* q_map, const int32_t* kv_map, float scale,
+                                int32_t mode, float* workspace, float* scores, int32_t* status,
+                                cudaStream_t stream);
 
 // bsa_order.cu
 size_t spectral_order_workspace_bytes(int64_t heads, int32_t nQB, int32_t nKB);
@@ -54,6 +65,8 @@ struct ForwardArgs {
     float scale;
     void* o;
     float* lse;
+    const uint32_t* crm;  // non-NULL: CRM rows instead of kv_idx / kv_cnt
+    int32_t crm_words;
 };
 // Returns BSA_OK, BSA_ERR_CUDA (launch / descriptor failure) or BSA_ERR_UNSUPPORTED.
 bsa_status launch_forward(const ForwardArgs& a, int32_t* status, cudaStream_t stream);

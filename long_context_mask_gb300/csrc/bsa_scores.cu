@@ -1,0 +1,126 @@
+// Block scores from block means: the scoring step in front of top-k block
+// selection and importance sampling.
+//
+// MC-Sparse, "The MC-Sparse Architecture": block-sparse attention keeps, per
+// query block, the KV blocks with the highest mean-pooled similarity.
+// InstaGen, Algorithm 1 step 2 and section 3.3: the centroid score
+// s_gc = exp(q_g . k_c / sqrt d) of a query group and a key cluster.  With
+// the tokens gathered through q_map / kv_map, a group or cluster is a
+// 128-token block of the gathered order.
+//
+//   k_block_means   one thread block per (head, block, tensor): the fp32 mean
+//                   of the block's 128 rows (gathered through the map), one
+//                   thread per column; written to the caller's workspace.
+//   k_block_scores  per head, a 64 x 64 tile of  mean(Q_u) . mean(K_v) * scale
+//                   (or its exponential) per thread block, from shared-memory
+//                   tiles of the two mean matrices.
+// The work is a read of Q and K (HBM-bound) and a small fp32 product.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "bsa_internal.h"
+
+namespace bsa {
+namespace {
+
+constexpr int kTileS = 64;   // score tile edge
+constexpr int kKChunk = 32;  // columns of the mean matrices staged per step
+
+__global__ void k_block_means(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                              int32_t N, int32_t D, const int32_t* __restrict__ q_map,
+                              const int32_t* __restrict__ kv_map, float* __restrict__ means,
+                              int64_t per_tensor, int32_t* status) {
+    const int32_t b = blockIdx.x;
+    const int64_t bh = blockIdx.y;
+    const int which = blockIdx.z;  // 0: Q, 1: K
+    const __nv_bfloat16* x = which ? k : q;
+    const int32_t* map = which ? kv_map : q_map;
+    const int32_t nb = N / kBlock;
+    for (int32_t d = threadIdx.x; d < D; d += blockDim.x) {
+        float s = 0.f;
+        for (int32_t t = 0; t < kBlock; ++t) {
+            const int32_t p = b * kBlock + t;
+            int32_t i = map ? map[bh * N + p] : p;
+            if (i < 0 || i >= N) {
+                if (d == 0) atomicCAS(status, 0, BSA_ERR_BOUNDS);
+                i = 0;
+            }
+            s += __bfloat162float(x[(bh * N + i) * D + d]);
+        }
+        means[which * per_tensor + (bh * nb + b) * D + d] = s * (1.0f / kBlock);
+    }
+}
+
+__global__ void __launch_bounds__(256) k_block_scores(const float* __restrict__ means,
+                                                      int64_t per_tensor, int32_t nb, int32_t D,
+                                                      float scale, int32_t mode,
+                                                      float* __restrict__ scores) {
+    __shared__ float qs[kTileS][kKChunk + 1];
+    __shared__ float ks[kTileS][kKChunk + 1];
+    const int64_t bh = blockIdx.z;
+    const int32_t u0 = blockIdx.y * kTileS, v0 = blockIdx.x * kTileS;
+    const float* qm = means + bh * nb * (int64_t)D;
+    const float* km = means + per_tensor + bh * nb * (int64_t)D;
+    // each thread owns a 4 x 4 patch of the 64 x 64 tile
+    const int tr = (threadIdx.x / 16) * 4, tc = (threadIdx.x % 16) * 4;
+    float acc[4][4] = {};
+    for (int32_t d0 = 0; d0 < D; d0 += kKChunk) {
+        for (int i = threadIdx.x; i < kTileS * kKChunk; i += blockDim.x) {
+            const int r = i / kKChunk, c = i % kKChunk;
+            qs[r][c] = (u0 + r < nb && d0 + c < D) ? qm[(int64_t)(u0 + r) * D + d0 + c] : 0.f;
+            ks[r][c] = (v0 + r < nb && d0 + c < D) ? km[(int64_t)(v0 + r) * D + d0 + c] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int c = 0; c < kKChunk; ++c) {
+            float a[4], bb[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                a[i] = qs[tr + i][c];
+                bb[i] = ks[tc + i][c];
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int32_t u = u0 + tr + i, v = v0 + tc + j;
+            if (u < nb && v < nb) {
+                const float s = acc[i][j] * scale;
+                scores[(bh * nb + u) * (int64_t)nb + v] = mode == 1 ? expf(s) : s;
+            }
+        }
+}
+
+}  // namespace
+
+size_t block_scores_workspace_bytes(int64_t BH, int32_t N, int32_t D) {
+    return (size_t)2 * BH * (N / kBlock) * (size_t)D * sizeof(float);
+}
+
+cudaError_t launch_block_scores(const void* q, const void* k, int32_t B, int32_t H, int32_t N,
+                                int32_t D, const int32_t* q_map, const int32_t* kv_map, float scale,
+                                int32_t mode, float* workspace, float* scores, int32_t* status,
+                                cudaStream_t stream) {
+    const int64_t BH = (int64_t)B * H;
+    const int32_t nb = N / kBlock;
+    const int64_t per_tensor = BH * nb * (int64_t)D;
+    k_block_means<<<dim3((unsigned)nb, (unsigned)BH, 2), 128, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), N, D, q_map,
+        kv_map, workspace, per_tensor, status);
+    const unsigned tiles = (unsigned)((nb + kTileS - 1) / kTileS);
+    const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
+    k_block_scores<<<dim3(tiles, tiles, (unsigned)BH), 256, 0, stream>>>(workspace, per_tensor, nb, D,
+                                                                         sc, mode, scores);
+    return cudaGetLastError();
+}
+
+}  // namespace bsa

@@ -56,6 +56,12 @@ def _load():
         lib.oracle_attention.argtypes = [P, P, P, i32, i32, i32, i32, P, P, i32, P, P, P,
                                          f64, P, i64, P, P, P]
         lib.oracle_attention.restype = None
+        lib.oracle_crm_rows.argtypes = [i32, P, i64, i32, f32, P, i32]
+        lib.oracle_crm_rows.restype = None
+        lib.oracle_upscale_threshold.argtypes = [P, i64, i32, i32, i32, i32, P]
+        lib.oracle_upscale_threshold.restype = None
+        lib.oracle_block_scores.argtypes = [P, P, i32, i32, i32, i32, P, P, f64, i32, P]
+        lib.oracle_block_scores.restype = None
         lib.oracle_spectral_order.argtypes = [P, P, i32, i64, i32, i32, i32, P, P, P, P]
         lib.oracle_spectral_order.restype = None
         lib.oracle_num_threads.argtypes = []
@@ -130,20 +136,60 @@ def reorder_rows(kv_cnt, wave, order_in=None):
     return perm
 
 
-def sample_blocks(scores, exact_idx, exact_cnt, m, u, max_kv):
-    """Exact list + PPSWOR/systematic-PPS sample -> (kv_idx, kv_cnt, log_w, n_overflow)."""
-    scores = _c(scores, np.float32)
-    rows, nkb = scores.shape
+def sample_blocks(scores, exact_idx, exact_cnt, m, u, max_kv, nkb=None):
+    """Exact list + PPSWOR/systematic-PPS sample -> (kv_idx, kv_cnt, log_w, n_overflow).
+
+    scores None selects the uniform sampler (pass nkb and rows via exact_cnt)."""
+    if scores is None:
+        rows = len(exact_cnt)
+    else:
+        scores = _c(scores, np.float32)
+        rows, nkb = scores.shape
     exact_idx = _c(exact_idx, np.int32)
     exact_cnt = _c(exact_cnt, np.int32)
     u = _c(u, np.float64)
     idx = np.empty((rows, max_kv), np.int32)
     cnt = np.empty(rows, np.int32)
     lw = np.empty((rows, max_kv), np.float32)
-    ov = _load().oracle_sample_blocks(_ptr(scores), rows, nkb, _ptr(exact_idx), _ptr(exact_cnt),
+    ov = _load().oracle_sample_blocks(_ptr(scores), rows, int(nkb), _ptr(exact_idx), _ptr(exact_cnt),
                                       exact_idx.shape[1], int(m), _ptr(u), _ptr(idx), _ptr(cnt),
                                       _ptr(lw), int(max_kv))
     return idx, cnt, lw, int(ov)
+
+
+def crm_rows(src, p=None):
+    """CRM rows: uint32 [rows, ceil(nKB/32)], bit i of word w = block 32w+i kept.
+    src uint8 mask (nonzero keeps) or fp32 threshold map with p (T <= p keeps)."""
+    src = np.ascontiguousarray(src)
+    rows, nkb = src.shape
+    nw = (nkb + 31) // 32
+    out = np.empty((rows, nw), np.uint32)
+    mode = 0 if src.dtype == np.uint8 else 1
+    if mode == 1:
+        src = src.astype(np.float32)
+    _load().oracle_crm_rows(mode, _ptr(src), rows, nkb, float(np.float32(p or 0.0)), _ptr(out), nw)
+    return out
+
+
+def upscale_threshold(T, Ut, Vt):
+    """Threshold maps fp32 [heads, Ub, Vb] -> [heads, Ut, Vt] (eq. 7 reading)."""
+    T = _c(T, np.float32)
+    heads, ub, vb = T.shape
+    out = np.empty((heads, Ut, Vt), np.float32)
+    _load().oracle_upscale_threshold(_ptr(T), heads, ub, vb, int(Ut), int(Vt), _ptr(out))
+    return out
+
+
+def block_scores(q, k, q_map=None, kv_map=None, scale=0.0, mode=0):
+    """Scores [B*H*nQB, nKB] (fp64) from the block means of Q and K (mode 0:
+    scaled dot product, mode 1: its exponential, the centroid score)."""
+    q, k = _as_u16(q), _as_u16(k)
+    B, H, N, D = q.shape
+    nb = N // 128
+    out = np.empty((B * H * nb, nb), np.float64)
+    _load().oracle_block_scores(_ptr(q), _ptr(k), B, H, N, D, _ptr(_c(q_map, np.int32)),
+                                _ptr(_c(kv_map, np.int32)), float(scale), int(mode), _ptr(out))
+    return out
 
 
 def spectral_order(kv_idx, kv_cnt, n_kb, x0, iters):

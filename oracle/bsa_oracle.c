@@ -25,6 +25,11 @@
  *                          probabilities, cap at 1 and renormalise), the
  *                          promotion of pi = 1 keys, systematic PPS sampling,
  *                          and Algorithm 1 step 13 (w = 1/pi).
+ *   oracle_crm_rows        ScalingAttention, section 7.2 (CRM bitmask rows).
+ *   oracle_upscale_threshold ScalingAttention, section 7.1 eq. (7).
+ *   oracle_block_scores    MC-Sparse, "The MC-Sparse Architecture" (mean-pooled
+ *                          block similarity) and InstaGen Algorithm 1 step 2
+ *                          (centroid scores exp(q_g . k_c / sqrt d)).
  *   oracle_spectral_order  WaveAlign, section IV-C (rank-2 embedding of the
  *                          centered mask by matrix-free subspace iteration,
  *                          rows ordered by polar angle).
@@ -193,8 +198,15 @@ int64_t oracle_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
     int64_t overflow = 0;
     uint8_t* state = (uint8_t*)malloc((size_t)nKB); /* 0 residual, 1 exact, 2 promoted, 3 sampled */
     double* pi = (double*)malloc(sizeof(double) * (size_t)nKB);
+    /* NULL scores: the uniform sampler (InstaGen Algorithm 1 steps 6-8), i.e.
+       every residual block with the same score and pi_j = m / |R|. */
+    float* ones = NULL;
+    if (!scores) {
+        ones = (float*)malloc(sizeof(float) * (size_t)nKB);
+        for (int32_t kb = 0; kb < nKB; ++kb) ones[kb] = 1.0f;
+    }
     for (int64_t r = 0; r < rows; ++r) {
-        const float* s = scores + r * nKB;
+        const float* s = scores ? scores + r * nKB : ones;
         memset(state, 0, (size_t)nKB);
         for (int32_t e = 0; e < exact_cnt[r]; ++e) state[exact_idx[r * exact_stride + e]] = 1;
         int32_t n_res = 0;
@@ -258,6 +270,7 @@ int64_t oracle_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
         kv_cnt[r] = n;
         overflow += total > max_kv;
     }
+    free(ones);
     free(pi);
     free(state);
     return overflow;
@@ -460,4 +473,101 @@ void oracle_spectral_order(const int32_t* kv_idx, const int32_t* kv_cnt, int32_t
     free(X);
     free(Z);
     free(mu);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Block scores from block means.                                            */
+/* MC-Sparse, "The MC-Sparse Architecture" (block-sparse attention keeps the */
+/* KV blocks with the highest mean-pooled similarity) and InstaGen section   */
+/* 3.3 / Algorithm 1 step 2 (centroid score s_gc = exp(q_g . k_c / sqrt d)   */
+/* with q_g, k_c the means of a query group and a key cluster).  A group /   */
+/* cluster is a 128-token block of the gathered order (q_map / kv_map, or    */
+/* the identity).  mode 0: mean(Q_u) . mean(K_v) * scale;  mode 1:           */
+/* exp(mean(Q_u) . mean(K_v) * scale).  scale <= 0 selects 1/sqrt(D).        */
+/* Output scores [B*H*nQB, nKB] in fp64.                                      */
+/* ------------------------------------------------------------------------- */
+void oracle_block_scores(const uint16_t* q, const uint16_t* k, int32_t B, int32_t H, int32_t N,
+                         int32_t D, const int32_t* q_map, const int32_t* kv_map, double scale,
+                         int32_t mode, double* scores) {
+    const int32_t nb = N / ORACLE_BLOCK;
+    if (scale <= 0.0) scale = 1.0 / sqrt((double)D);
+    const int64_t BH = (int64_t)B * H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        double* qm = (double*)malloc(sizeof(double) * (size_t)nb * D);
+        double* km = (double*)malloc(sizeof(double) * (size_t)nb * D);
+        for (int32_t b = 0; b < nb; ++b) {
+            for (int32_t d = 0; d < D; ++d) {
+                double sq = 0.0, sk = 0.0;
+                for (int32_t t = 0; t < ORACLE_BLOCK; ++t) {
+                    const int32_t p = b * ORACLE_BLOCK + t;
+                    const int32_t i = q_map ? q_map[bh * N + p] : p;
+                    const int32_t j = kv_map ? kv_map[bh * N + p] : p;
+                    sq += bf16_to_double(q[(bh * N + i) * D + d]);
+                    sk += bf16_to_double(k[(bh * N + j) * D + d]);
+                }
+                qm[(int64_t)b * D + d] = sq / ORACLE_BLOCK;
+                km[(int64_t)b * D + d] = sk / ORACLE_BLOCK;
+            }
+        }
+        for (int32_t u = 0; u < nb; ++u)
+            for (int32_t v = 0; v < nb; ++v) {
+                double dot = 0.0;
+                for (int32_t d = 0; d < D; ++d) dot += qm[(int64_t)u * D + d] * km[(int64_t)v * D + d];
+                const double s = dot * scale;
+                scores[(bh * nb + u) * (int64_t)nb + v] = mode == 1 ? exp(s) : s;
+            }
+        free(km);
+        free(qm);
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* CRM rows, ScalingAttention section 7.2: each row is an array of uint32     */
+/* words, bit i of word w set when KV block 32w + i is kept.  mode 0: mask    */
+/* (nonzero keeps), mode 1: threshold map (T <= p in fp32 keeps).             */
+/* ------------------------------------------------------------------------- */
+void oracle_crm_rows(int32_t mode, const void* src, int64_t rows, int32_t nKB, float p,
+                     uint32_t* words, int32_t n_words) {
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int32_t w = 0; w < n_words; ++w) words[r * n_words + w] = 0u;
+        for (int32_t kb = 0; kb < nKB; ++kb) {
+            int keep;
+            if (mode == 0) keep = ((const uint8_t*)src)[r * nKB + kb] != 0;
+            else keep = ((const float*)src)[r * nKB + kb] <= p;
+            if (keep) words[r * n_words + kb / 32] |= 1u << (kb % 32);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Resolution upscaling of a threshold map, ScalingAttention section 7.1     */
+/* eq. (7): R_target(u, v) = ceil(Phi(R_base, u / s_h, v / s_w)) with Phi    */
+/* bilinear interpolation and s = target / base size.  On a 0/1 mask the     */
+/* ceiling keeps a target block when any base block with a nonzero bilinear  */
+/* weight is active; applied to every mask M_p = I(T <= p) at once, that is  */
+/* the minimum of T over those base blocks.  Base coordinate of target index */
+/* u is x = u * Ub / Ut; its neighbours are floor(x) and floor(x) + 1        */
+/* (clamped to the last index), the second with weight x - floor(x), which   */
+/* is nonzero exactly when u * Ub is not a multiple of Ut (integer test).    */
+/* ------------------------------------------------------------------------- */
+void oracle_upscale_threshold(const float* T, int64_t heads, int32_t Ub, int32_t Vb,
+                              int32_t Ut, int32_t Vt, float* out) {
+    for (int64_t h = 0; h < heads; ++h)
+        for (int32_t u = 0; u < Ut; ++u) {
+            const int64_t xu = (int64_t)u * Ub;
+            const int32_t i0 = (int32_t)(xu / Ut);
+            const int32_t i1 = (xu % Ut != 0 && i0 + 1 < Ub) ? i0 + 1 : i0;
+            for (int32_t v = 0; v < Vt; ++v) {
+                const int64_t yv = (int64_t)v * Vb;
+                const int32_t j0 = (int32_t)(yv / Vt);
+                const int32_t j1 = (yv % Vt != 0 && j0 + 1 < Vb) ? j0 + 1 : j0;
+                const float* b = T + h * (int64_t)Ub * Vb;
+                float m = b[(int64_t)i0 * Vb + j0];
+                if (b[(int64_t)i0 * Vb + j1] < m) m = b[(int64_t)i0 * Vb + j1];
+                if (b[(int64_t)i1 * Vb + j0] < m) m = b[(int64_t)i1 * Vb + j0];
+                if (b[(int64_t)i1 * Vb + j1] < m) m = b[(int64_t)i1 * Vb + j1];
+                out[(h * Ut + u) * (int64_t)Vt + v] = m;
+            }
+        }
 }

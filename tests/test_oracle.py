@@ -495,3 +495,112 @@ def test_spectral_order_is_equivariant_under_row_relabelling():
     Xp, angp, orderp = oracle.spectral_order(idx_p, cnt_p, nkb, x0[:, perm], iters=10)
     np.testing.assert_allclose(Xp[0], X[0][perm], atol=1e-10)
     np.testing.assert_allclose(angp[0], ang[0][perm], atol=1e-10)
+
+
+# --------------------------------------------------------------------------
+# Block scores from block means (MC-Sparse mean-pooled score; InstaGen
+# centroid score exp(q_g . k_c / sqrt d)).
+# --------------------------------------------------------------------------
+def test_block_scores_closed_form_for_constant_blocks_and_attention_logit():
+    """Blocks whose 128 rows are all equal have means equal to that row, so the
+    score is the scaled dot product; with one listed block of identical keys
+    the attention oracle's LSE is that logit + ln 128 (an independent path)."""
+    N, D = 384, 32
+    rng = np.random.default_rng(3)
+    a = torch.from_numpy(rng.standard_normal((3, D))).to(torch.bfloat16)
+    b = torch.from_numpy(rng.standard_normal((3, D))).to(torch.bfloat16)
+    q = a.repeat_interleave(128, 0)[None, None]
+    k = b.repeat_interleave(128, 0)[None, None]
+    S = oracle.block_scores(q, k)
+    ref = _f64(a) @ _f64(b).T / math.sqrt(D)
+    np.testing.assert_allclose(S, ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(oracle.block_scores(q, k, mode=1), np.exp(ref), rtol=1e-12)
+    v = torch.zeros_like(k)
+    idx = np.array([[2], [0], [1]], np.int32)
+    O, L, tok = oracle.attention(q, k, v, idx, np.ones(3, np.int32))
+    for qb, kb in enumerate([2, 0, 1]):
+        np.testing.assert_allclose(L[qb * 128:(qb + 1) * 128], S[qb, kb] + math.log(128), atol=1e-12)
+
+
+def test_block_scores_ignore_order_inside_a_block_and_follow_maps():
+    B, H, N, D = 1, 2, 512, 16
+    q, k = _bf16((B, H, N, D), 41), _bf16((B, H, N, D), 42)
+    rng = np.random.default_rng(4)
+    # permuting tokens inside each block leaves the means, hence the scores, unchanged
+    within = np.stack([np.concatenate([blk * 128 + rng.permutation(128) for blk in range(N // 128)])
+                       for _ in range(H)]).astype(np.int32)
+    np.testing.assert_allclose(oracle.block_scores(q, k, q_map=within, kv_map=within),
+                               oracle.block_scores(q, k), rtol=0, atol=1e-12)
+    # a map equals scoring the physically gathered tensors
+    perm = np.stack([rng.permutation(N) for _ in range(H)]).astype(np.int32)
+    qg = torch.stack([q[0, h][torch.from_numpy(perm[h]).long()] for h in range(H)])[None]
+    kg = torch.stack([k[0, h][torch.from_numpy(perm[h]).long()] for h in range(H)])[None]
+    np.testing.assert_allclose(oracle.block_scores(q, k, q_map=perm, kv_map=perm),
+                               oracle.block_scores(qg, kg), rtol=0, atol=1e-12)
+
+
+def test_uniform_sampler_inclusion_and_weights():
+    """No scores: every residual block has pi = m / |R| (InstaGen Alg. 1 steps 6-8)."""
+    nkb, m, n = 30, 4, 20000
+    exact = [3, 17]
+    ex = np.tile(np.array(exact, np.int32), (n, 1))
+    ec = np.full(n, len(exact), np.int32)
+    u = np.random.default_rng(6).random(n)
+    idx, cnt, lw, ov = oracle.sample_blocks(None, ex, ec, m, u, max_kv=nkb, nkb=nkb)
+    assert ov == 0 and np.all(cnt == len(exact) + m)
+    pi = m / (nkb - len(exact))
+    freq = np.zeros(nkb)
+    for r in range(n):
+        freq[idx[r, :cnt[r]]] += 1
+    freq /= n
+    resid = [j for j in range(nkb) if j not in exact]
+    assert np.all(np.abs(freq[resid] - pi) <= 4 * math.sqrt(pi * (1 - pi) / n))
+    drawn = ~np.isin(idx[:, :cnt[0]], exact)
+    assert np.allclose(lw[:, :cnt[0]][drawn], -math.log(pi), rtol=1e-6)
+
+
+# --------------------------------------------------------------------------
+# CRM rows and eq. (7) upscaling (ScalingAttention sections 7.1-7.2).
+# --------------------------------------------------------------------------
+def test_crm_rows_encode_the_same_blocks_as_the_lists():
+    g = np.random.default_rng(12)
+    mask = (g.random((50, 75)) < 0.3).astype(np.uint8)
+    words = oracle.crm_rows(mask)
+    assert words.shape == (50, 3)
+    idx, cnt, _ = oracle.index_mask(mask)
+    for r in range(50):
+        bits = [32 * w + i for w in range(3) for i in range(32) if (int(words[r, w]) >> i) & 1]
+        assert bits == list(idx[r, :cnt[r]])
+    T = g.random((50, 75)).astype(np.float32)
+    np.testing.assert_array_equal(oracle.crm_rows(T, 0.4), oracle.crm_rows((T <= np.float32(0.4)).astype(np.uint8)))
+
+
+def test_upscale_hand_worked_example():
+    lines = [l.split() for l in open(os.path.join(GOLD, "upscale_eq7_example.txt"))
+             if l.strip() and not l.startswith("#")]
+    ub, vb = int(lines[0][1]), int(lines[0][2])
+    base = np.array([[int(x) for x in l] for l in lines[1:1 + ub]], np.float32)
+    ut, vt = int(lines[1 + ub][1]), int(lines[1 + ub][2])
+    exp = np.array([[int(x) for x in l] for l in lines[3 + ub:3 + ub + ut]])
+    # a 0/1 mask as a threshold map: active blocks get T = 0, others T = 1; keep T <= 0.5
+    T = np.where(base > 0, 0.0, 1.0).astype(np.float32)[None]
+    out = oracle.upscale_threshold(T, ut, vt)[0]
+    np.testing.assert_array_equal((out <= 0.5).astype(int), exp)
+
+
+def test_upscale_is_identity_at_scale_one_and_conservative_for_every_threshold():
+    g = np.random.default_rng(13)
+    T = g.random((2, 9, 11)).astype(np.float32)
+    np.testing.assert_array_equal(oracle.upscale_threshold(T, 9, 11), T)
+    out = oracle.upscale_threshold(T, 23, 30)
+    for p in (0.1, 0.3, 0.7):
+        # conservative: every target block whose nearest-lower base block is
+        # active stays active; and never more active than the 2x2 neighbourhood
+        for h in range(2):
+            for u in range(23):
+                for v in range(30):
+                    i0, j0 = u * 9 // 23, v * 11 // 30
+                    if T[h, i0, j0] <= p:
+                        assert out[h, u, v] <= p
+                    nb = T[h, i0:min(i0 + 2, 9), j0:min(j0 + 2, 11)]
+                    assert out[h, u, v] >= nb.min()
