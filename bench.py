@@ -133,7 +133,8 @@ class ClockSampler:
 class Path:
     """Device buffers and the per-step launch sequence for one workload."""
 
-    def __init__(self, prob, dev, order: str, scores_on_gpu: bool = False, crm: bool = False):
+    def __init__(self, prob, dev, order: str, scores_on_gpu: bool = False, crm: bool = False,
+                 kv_gather: str = "auto"):
         import long_context_mask_gb300 as bsa
         self.bsa = bsa
         self.prob = prob
@@ -184,7 +185,16 @@ class Path:
             self.spec = torch.empty((self.heads, nqb), dtype=torch.int32, device=dev)
             self.spec_ws = torch.empty(bsa.spectral_order_workspace_size(self.heads, nqb, nqb),
                                        dtype=torch.uint8, device=dev)
-        self.launches_per_step = (1 + (self.mode is not None) + bool(prob.m_sample)
+        # Gathered keys/values: copy them into gathered order once per step
+        # (one HBM pass) when blocks are listed by many query blocks each, or
+        # gather rows inside the forward kernel when each block is used once
+        # (the Scatter layer's one block per query block).
+        if kv_gather == "auto":
+            kv_gather = "kernel" if prob.diag_list else "hbm"
+        self.pregather = self.kv_map is not None and kv_gather == "hbm" and not self.crm
+        if self.pregather:
+            self.kg, self.vg = torch.empty_like(self.k), torch.empty_like(self.v)
+        self.launches_per_step = (1 + 2 * self.pregather + (self.mode is not None) + bool(prob.m_sample)
                                   + (order != "identity") + (order == "spectral")
                                   + 2 * self.scores_on_gpu)
 
@@ -220,12 +230,22 @@ class Path:
                                  q_map=self.q_map, kv_map=self.kv_map)
             return
         idx, cnt = self.lists()
-        self.bsa.forward(self.q, self.k, self.v, idx, cnt, self.o, self.lse, log_w=self.lw,
-                         q_map=self.q_map, kv_map=self.kv_map,
+        k, v, kv_map = self.k, self.v, self.kv_map
+        if self.pregather:
+            k, v, kv_map = self.kg, self.vg, None
+        self.bsa.forward(self.q, k, v, idx, cnt, self.o, self.lse, log_w=self.lw,
+                         q_map=self.q_map, kv_map=kv_map,
                          row_perm=None if self.order == "identity" else self.row_perm)
+
+    def prepare_kv(self):
+        """Keys/values into gathered order in HBM (only when pre-gathering)."""
+        if self.pregather:
+            self.bsa.gather_rows(self.k, self.kv_map, self.kg)
+            self.bsa.gather_rows(self.v, self.kv_map, self.vg)
 
     def step(self):
         self.build_lists()
+        self.prepare_kv()
         self.attend()
 
     def effective_flops(self):
@@ -306,6 +326,10 @@ def parse():
                     help="score blocks from Q/K inside the step (mean-pooled; centroid for --config 4)")
     ap.add_argument("--dense", action="store_true",
                     help="every query block attends to every KV block (the in-build dense ceiling)")
+    ap.add_argument("--kv-gather", default="auto", choices=["auto", "kernel", "hbm"],
+                    help="index-mapped K/V: gather rows inside the forward kernel, or copy them "
+                         "into gathered order in HBM first (auto: HBM unless each block is "
+                         "listed once)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle CPU time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -347,7 +371,8 @@ def config_dict(prob, config, order, density, world):
             "l2": "flushed between timed steps (256 MiB write)",
             "parallelism": "one independent workload per GPU" if world > 1 else "single GPU",
             "scores": "from Q/K inside the step" if getattr(prob, "_scores_on_gpu", False) else "given",
-            "kv_sets": "CRM bitmask rows" if getattr(prob, "_crm", False) else "index lists"}
+            "kv_sets": "CRM bitmask rows" if getattr(prob, "_crm", False) else "index lists",
+            "kv_rows": getattr(prob, "_kv_rows", "contiguous")}
 
 
 def run_reference(args, world, rank):
@@ -398,7 +423,10 @@ def main():
     prob = make_problem(args.config, args.heads, args.dense)
     prob._scores_on_gpu = args.scores_on_gpu and prob.scores is not None
     prob._crm = args.crm and (prob.mask is not None or prob.T is not None)
-    path = Path(prob, dev, args.order, args.scores_on_gpu, args.crm)
+    path = Path(prob, dev, args.order, args.scores_on_gpu, args.crm, args.kv_gather)
+    if path.kv_map is not None:
+        prob._kv_rows = ("copied into gathered order in HBM each step (bsa_gather_rows)"
+                         if path.pregather else "gathered through kv_map inside the forward kernel")
     path.step()
     torch.cuda.synchronize()
     if args.profile_once:
@@ -435,6 +463,7 @@ def main():
         step_ms = [a.elapsed_time(b) for a, b in ev]
         # ---- the dominant kernel alone (same inputs, L2 flushed before each launch)
         path.build_lists()
+        path.prepare_kv()
         for i in range(K):
             flush.zero_()
             fwd_ev[i][0].record(stream)

@@ -289,6 +289,32 @@ bsa_status bsa_forward(const void* q, const void* k, const void* v, int32_t B, i
                        float* lse, void* stream);
 
 /*
+ * bsa_gather_rows - token rows permuted into gathered order in HBM:
+ *     dst[bh][p][:] = src[bh][map[bh][p]][:]    for p in 0..N-1.
+ *
+ * Defined by: InstaGen, section 3.3 and Introduction (permuted block-sparse
+ * attention: tokens permuted so that every cluster is a contiguous block)
+ * and INTRA, "CQS-Aware Token-Sparse FlashAttention Kernel" (the index
+ * maps).  bsa_forward with kv_map reads the same rows through the map
+ * inside the kernel; calling bsa_forward on the outputs of this call with
+ * kv_map = NULL gives the same O and LSE (bit for bit) and loads every
+ * listed block as one contiguous tile.  That pays when a head's key/value
+ * blocks are listed by several query blocks each; a row-granular gather
+ * inside the kernel costs the same for every listing.
+ *
+ *  src     device bf16 [heads, N, D] contiguous, 16-byte aligned.
+ *  map     device int32 [heads, N], 4-byte aligned; entries in [0, N).  An
+ *          entry outside [0, N) writes a zero row and raises
+ *          BSA_ERR_BOUNDS.  Duplicate entries are allowed (rows repeat).
+ *  heads   0 .. 65535 (0: nothing to do); N 1 .. 2^24; heads * N < 2^31.
+ *  D       64 or 128.
+ *  dst     device bf16 [heads, N, D] out, 16-byte aligned; must not overlap
+ *          src.
+ */
+bsa_status bsa_gather_rows(const void* src, const int32_t* map, int64_t heads, int32_t N,
+                           int32_t D, void* dst, void* stream);
+
+/*
  * bsa_build_crm - the CRM (compressed row mask) form of a mask or threshold
  * map: per row, uint32 words in which bit i of word w is set when KV block
  * 32w + i is kept (ScalingAttention, section 7.2: one 32-bit load decodes 32

@@ -24,7 +24,7 @@ EXPORTS = ("bsa_build_index", "bsa_build_crm", "bsa_forward_crm", "bsa_upscale_t
            "bsa_block_scores", "bsa_block_scores_workspace_size",
            "bsa_reorder_rows", "bsa_spectral_order",
            "bsa_spectral_order_workspace_size", "bsa_spectral_order_noalloc", "bsa_sample_blocks",
-           "bsa_forward",
+           "bsa_forward", "bsa_gather_rows",
            "bsa_device_status", "bsa_resident_ctas", "bsa_status_string", "bsa_selftest_exp2",
            "bsa_selftest_wait_timeout")
 
@@ -59,6 +59,8 @@ def load_library():
     lib.bsa_forward_crm.restype = i32
     lib.bsa_upscale_threshold.argtypes = [P, i64, i32, i32, i32, i32, P, P]
     lib.bsa_upscale_threshold.restype = i32
+    lib.bsa_gather_rows.argtypes = [P, P, i64, i32, i32, P, P]
+    lib.bsa_gather_rows.restype = i32
     lib.bsa_block_scores.argtypes = [P, P, i32, i32, i32, i32, P, P, f32, i32, P, ctypes.c_size_t,
                                      P, P]
     lib.bsa_block_scores.restype = i32
@@ -185,6 +187,23 @@ def upscale_threshold(T_base, T_target, *, stream=None):
     _, ut, vt = T_target.shape
     _check("bsa_upscale_threshold", load_library().bsa_upscale_threshold(
         _ptr(T_base), heads, ub, vb, ut, vt, _ptr(T_target), _stream(stream)))
+
+
+def gather_rows(src, map, dst=None, *, stream=None):
+    """dst[h, p] = src[h, map[h, p]] for bf16 [..., N, D] rows (tokens permuted in HBM)."""
+    import torch
+    _dtype(src, "src", torch.bfloat16)
+    _dtype(map, "map", torch.int32)
+    N, D = src.shape[-2], src.shape[-1]
+    heads = src.numel() // (N * D)
+    if dst is None:
+        dst = torch.empty_like(src)
+    _dtype(dst, "dst", torch.bfloat16)
+    if map.numel() != heads * N or dst.shape != src.shape:
+        raise ValueError("gather_rows: map must hold heads * N entries and dst match src")
+    _check("bsa_gather_rows", load_library().bsa_gather_rows(_ptr(src), _ptr(map), heads, N, D,
+                                                             _ptr(dst), _stream(stream)))
+    return dst
 
 
 def reorder_rows(kv_cnt, wave: int, row_perm, *, order_in=None, stream=None):
@@ -333,7 +352,7 @@ __all__ = ["BLOCK", "BsaError", "IDX_MASK_U8", "IDX_THRESHOLD_F32", "IDX_TOPK_F3
            "reorder_rows", "sample_blocks", "forward", "device_status", "resident_ctas",
            "effective_flops", "dense_attention_flops", "load_library", "lib_path", "EXPORTS",
            "block_scores", "SCORE_MEAN_DOT", "SCORE_CENTROID_EXP", "build_crm", "forward_crm",
-           "upscale_threshold",
+           "upscale_threshold", "gather_rows",
            "spectral_order", "spectral_order_workspace_size", "spectral_order_noalloc",
            "NOALLOC_SCRATCH_BYTES", "reorder_guard",
            "selftest_exp2", "selftest_wait_timeout", "math"]

@@ -20,7 +20,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbsa.so")
 SOURCES = ["bsa_api.cu", "bsa_index.cu", "bsa_scores.cu", "bsa_order.cu", "bsa_attn.cu",
            "bsa_selftest.cu",
-           "bsa_noalloc.cu"]
+           "bsa_noalloc.cu", "bsa_gather.cu"]
 HEADERS = ["bsa_internal.h", "bsa_ptx.cuh", "bsa_math.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

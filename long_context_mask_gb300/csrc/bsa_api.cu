@@ -251,6 +251,24 @@ bsa_status bsa_upscale_threshold(const float* T_base, int64_t heads, int32_t Ub,
     return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
+bsa_status bsa_gather_rows(const void* src, const int32_t* map, int64_t heads, int32_t N,
+                           int32_t D, void* dst, void* stream) {
+    if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+    if (heads < 0 || heads > 65535 || N < 1 || N > (1 << 24)) return BSA_ERR_INVALID_ARG;
+    if (heads * (int64_t)N >= ((int64_t)1 << 31)) return BSA_ERR_INVALID_ARG;
+    if (heads == 0) return BSA_OK;
+    if (!src || !map || !dst || !aligned(src, 16) || !aligned(dst, 16) || !aligned(map, 4))
+        return BSA_ERR_INVALID_ARG;
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
+    const uintptr_t bytes = (uintptr_t)(heads * (int64_t)N) * (uintptr_t)D * 2u;
+    if (s0 < d0 + bytes && d0 < s0 + bytes) return BSA_ERR_INVALID_ARG;  // overlapping buffers
+    int32_t* status = bsa::status_word_ptr();
+    if (!status) return BSA_ERR_CUDA;
+    cudaError_t e = bsa::launch_gather_rows(src, map, heads, N, D, dst, status,
+                                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
 bsa_status bsa_device_status(void* stream, int32_t* first_error) {
     if (!first_error) return BSA_ERR_INVALID_ARG;
     int32_t* status = bsa::status_word_ptr();

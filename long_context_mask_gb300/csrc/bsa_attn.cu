@@ -12,11 +12,18 @@
 // head-major in slot order: the sequential-head, wave-ordered schedule of
 // WaveAlign section V.
 //
-// Warp roles (6 warps):
-//   warp 0      TMA producer: Q once, then K_j and V_j of every listed block
-//               into a ring of kStages shared-memory slots (tile loads, or
-//               tile::gather4 row gathers when index maps are given).  The
-//               list is read 32 entries at a time by the whole warp.
+// Warp roles (8 warps):
+//   warp 0      producer: Q once (one TMA tile copy, or tile::gather4 row
+//               gathers through q_map), then K_j and V_j of every listed
+//               block into a ring of kStages shared-memory slots, one TMA
+//               tile copy each.  The list is read 32 entries at a time by the
+//               whole warp.
+//   warps 6, 7  with kv_map given, warp 0 and these two gather the K/V
+//               tiles in turn: each copies the 128 token rows of its tiles
+//               with 16-byte cp.async into the swizzled layout, one warp
+//               alone being too slow for row-granular copies (INTRA's
+//               gather, on the load/store path instead of the tensor-copy
+//               unit).
 //   warp 1      allocates tensor memory; one lane issues tcgen05.mma in the
 //               order QK(0), QK(1), QK(2), then for i = 0..n-1: PV(i),
 //               QK(i+3): S_j = Q K_j^T into TMEM score buffer j % 3 (QK runs
@@ -77,7 +84,10 @@ constexpr int kDefaultPoly = 0;            // exponentials per 8 on the FMA pipe
 constexpr float kRescaleThreshold = 8.0f;  // rescale O only when the max grows by > 2^8
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
-constexpr int kThreads = 192;
+constexpr int kExtraProducerWarp = 6;  // warps 6, 7 also copy gathered K/V rows
+constexpr int kGatherWarps = 3;        // warp 0 and warps 6, 7
+// 6 warps; 8 (two per SM sub-partition) when K/V rows are gathered
+constexpr int threads_for(bool gather) { return gather ? 256 : 192; }
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 384;
 constexpr int kSBuf = 3;  // TMEM score buffers
@@ -108,7 +118,9 @@ struct Params {
     // column halves) so that one copy brings a whole 128-row tile, reading
     // each 2D-byte row in full, and lands it as D/64 swizzled 16 KB boxes.
     CUtensorMap map_q, map_k, map_v;     // 3D box 64 x 128 rows x D/64
-    CUtensorMap gmap_q, gmap_k, gmap_v;  // 2D box 64 x 1 row (gather4)
+    CUtensorMap gmap_q;                  // 2D box 64 x 1 row (gather4 of the Q tile)
+    const __nv_bfloat16* k;              // gathered K/V rows are copied with cp.async
+    const __nv_bfloat16* v;
     const int32_t* kv_idx;
     const int32_t* kv_cnt;
     const float* log_w;
@@ -154,6 +166,36 @@ __device__ __forceinline__ int4 map_rows(const int32_t* map, int64_t base, int32
         }
     }
     return t;
+}
+
+// One K/V tile gathered through a map, copied 16 bytes per lane into the
+// 128-byte-swizzled box layout that a TMA tile copy would write (chunk c of
+// row r lands at chunk c ^ (r mod 8) of its 128-byte line).  Lane l holds
+// the tokens of rows l, l + 32, l + 64, l + 96 in tok[0..3].  Lanes covering
+// one row copy consecutive 16-byte chunks of it, so every warp-wide copy
+// reads whole 128-byte lines.
+template <int D>
+__device__ __forceinline__ void copy_tile(uint32_t dst, const __nv_bfloat16* base, int64_t bh,
+                                          int32_t N, int lane, const int32_t (&tok)[4]) {
+    using C = Cfg<D>;
+    constexpr int kLanesPerRow = D / 8;              // 16-byte chunks per token row
+    constexpr int kRowsPerCopy = 32 / kLanesPerRow;  // rows covered by one warp-wide copy
+    const int sub = lane / kLanesPerRow, chunk = lane % kLanesPerRow;
+    const int box = chunk >> 3, c = chunk & 7;
+    const uint32_t d0 = dst + box * C::kBoxBytes + ((uint32_t)c << 4);
+    const __nv_bfloat16* s0 = base + bh * N * D + box * 64 + c * 8;
+    // rows 32 j .. 32 j + 31 take their tokens from tok[j]; the inner loop is
+    // kept rolled so that the producer's code stays small next to the softmax
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll 2
+        for (int k = 0; k < 32 / kRowsPerCopy; ++k) {
+            const int rl = k * kRowsPerCopy + sub;  // row within this group of 32
+            const int r = 32 * j + rl;
+            const int32_t t = __shfl_sync(0xffffffffu, tok[j], rl);
+            cp_async16((d0 + r * 128) ^ ((uint32_t)(r & 7) << 4), s0 + (int64_t)t * D);
+        }
+    }
 }
 
 template <int D>
@@ -202,8 +244,8 @@ struct CrmIter {
     }
 };
 
-template <int D, int kPoly, bool kCrm>
-__global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_constant__ Params P) {
+template <int D, int kPoly, bool kCrm, bool kGather>
+__global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const __grid_constant__ Params P) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -253,7 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(smem_u32(&bars->full[s]), 1);
+            // tile loads: one arrive.expect_tx; gathered rows: one cp.async
+            // arrival per lane of the warp that copied the tile
+            mbar_init(smem_u32(&bars->full[s]), kGather ? 32 : 1);
             mbar_init(smem_u32(&bars->empty[s]), 1);
         }
         mbar_init(smem_u32(&bars->q_full), 1);
@@ -267,84 +311,155 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
         tmem_relinquish();
     }
     if (warp == kProducerWarp && lane == 0) {
-        prefetch_tensormap(P.kv_map ? &P.gmap_k : &P.map_k);
-        prefetch_tensormap(P.kv_map ? &P.gmap_v : &P.map_v);
+        if constexpr (!kGather) {
+            prefetch_tensormap(&P.map_k);
+            prefetch_tensormap(&P.map_v);
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == kProducerWarp) {
-        // ------------------------------------------------------------ producer
-        int32_t issued = 0;
-        if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bars->q_full), C::kTile);
-        __syncwarp();
-        load_tile<D>(s_q, &P.map_q, &P.gmap_q, P.q_map, bh, N, qb, smem_u32(&bars->q_full), lane,
-                     P.status);
-        // Load order = MMA consumption order: K_0, K_1, K_2, then V_i, K_{i+3}.
-        // Tile t of that sequence is V_i for t = 3 + 2i (i < n - 3) etc.; it is
-        // generated below as (block, is_v) pairs.  The list is read 32 entries
-        // at a time with one coalesced load and broadcast by shuffles.
-        bool ok = true;
-        int32_t chunk_base = -64, kb_lane = 0;
-        auto block_kb = [&](int32_t e) -> int32_t {
-            if (e - chunk_base >= 32 || e < chunk_base) {
-                chunk_base = e & ~31;
-                kb_lane = chunk_base + lane < n ? list[chunk_base + lane] : 0;
-                if (kb_lane < 0 || kb_lane >= nKB) {
-                    raise_status(P.status, BSA_ERR_BOUNDS);
-                    kb_lane = 0;  // keeps the pipeline in step; this row's result is unspecified
+    if (warp == kProducerWarp || warp >= kExtraProducerWarp) {
+        // ------------------------------------------------------------ producers
+        // Tile loads: warp 0 alone (one TMA copy per tile).  Gathered K/V
+        // (kv_map given): warps 0, 6, 7 take the tiles in turn and copy each
+        // with cp.async, because a single issuing warp cannot keep up with
+        // row-granular copies.  Every producer warp walks the whole list, so
+        // each knows every tile's ring slot and phase.
+        const int g = warp == kProducerWarp ? 0 : warp - kExtraProducerWarp + 1;
+        constexpr int n_prod = kGather ? kGatherWarps : 1;
+        if (g < n_prod) {
+            int32_t issued = 0;
+            if (g == 0) {
+                if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bars->q_full), C::kTile);
+                __syncwarp();
+                load_tile<D>(s_q, &P.map_q, &P.gmap_q, P.q_map, bh, N, qb, smem_u32(&bars->q_full), lane,
+                             P.status);
+            }
+            // Load order = MMA consumption order: K_0, K_1, K_2, then V_i, K_{i+3}.
+            // The list is read 32 entries at a time with one coalesced load and
+            // broadcast by shuffles.
+            int32_t chunk_base = -64, kb_lane = 0;
+            auto block_kb = [&](int32_t e) -> int32_t {
+                if (e - chunk_base >= 32 || e < chunk_base) {
+                    chunk_base = e & ~31;
+                    kb_lane = chunk_base + lane < n ? list[chunk_base + lane] : 0;
+                    if (kb_lane < 0 || kb_lane >= nKB) {
+                        raise_status(P.status, BSA_ERR_BOUNDS);
+                        kb_lane = 0;  // keeps the pipeline in step; this row's result is unspecified
+                    }
+                }
+                return __shfl_sync(0xffffffffu, kb_lane, e - chunk_base);
+            };
+            CrmIter it_k{crm_row, P.crm_words, -1, 0u}, it_v{crm_row, P.crm_words, -1, 0u};
+            // Tile t of the load sequence is K_t for t < min(n, 3); then V_i at
+            // 3 + 2i and K_{i+3} at 3 + 2i + 1 while i + 3 < n; then the
+            // remaining V tiles.  K blocks are fetched in increasing order
+            // (lookahead 3) and V blocks trail; both read the list through the
+            // same 32-entry window, refetched when a block falls outside it.
+            const int32_t lead = n < kSBuf ? n : kSBuf;
+            const int32_t inter = 2 * (n - lead);  // interleaved V/K positions
+            auto tile_is_v = [&](int32_t t) -> bool {
+                return t >= lead && (t - lead >= inter || ((t - lead) & 1) == 0);
+            };
+            // Block of tile t.  Called once per tile in increasing t: the CRM
+            // iterators (one per stream) advance one set bit per call.
+            auto tile_kb = [&](int32_t t) -> int32_t {
+                int32_t e;
+                const bool is_v = tile_is_v(t);
+                if (t < lead) e = t;
+                else if (t - lead < inter) e = ((t - lead) >> 1) + (is_v ? 0 : kSBuf);
+                else e = (n - lead) + (t - lead - inter);
+                int32_t kb;
+                if constexpr (kCrm) {
+                    kb = is_v ? it_v.next() : it_k.next();
+                    if (kb < 0 || kb >= nKB) {
+                        if (lane == 0) raise_status(P.status, BSA_ERR_BOUNDS);
+                        kb = 0;
+                    }
+                } else {
+                    kb = block_kb(e);
+                }
+                return kb;
+            };
+            // Blocks of tiles t .. t + n_prod - 1.  With gathered rows a warp
+            // copies every n_prod-th tile and reads the tokens of its next
+            // tile while copying the current one, so that the map read (which
+            // queues behind the row copies on the load/store path) is off the
+            // critical path.
+            const int32_t n_tiles = 2 * n;
+            int32_t kb_q[n_prod];
+#pragma unroll
+            for (int i = 0; i < n_prod; ++i) kb_q[i] = i < n_tiles ? tile_kb(i) : 0;
+            int32_t tok[4] = {0, 0, 0, 0}, tok_next[4] = {0, 0, 0, 0};
+            // lane l reads the tokens of rows l, l + 32, l + 64, l + 96
+            const int32_t* map_head = P.kv_map + bh * N + lane;
+            if constexpr (kGather) {
+                if (g < n_tiles) {
+                    int32_t kb_g = kb_q[0];  // kb_q[g] without a dynamic register index
+#pragma unroll
+                    for (int i = 1; i < n_prod; ++i) kb_g = i == g ? kb_q[i] : kb_g;
+                    const int32_t* mrow = map_head + (int64_t)kb_g * 128;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) tok[j] = mrow[32 * j];
                 }
             }
-            return __shfl_sync(0xffffffffu, kb_lane, e - chunk_base);
-        };
-        CrmIter it_k{crm_row, P.crm_words, -1, 0u}, it_v{crm_row, P.crm_words, -1, 0u};
-        auto put = [&](int32_t e, bool is_v) -> bool {
-            int32_t kb;
-            if constexpr (kCrm) {
-                // K tiles are fetched in block order and V tiles trail them: one
-                // bit iterator per stream
-                kb = is_v ? it_v.next() : it_k.next();
-                if (kb < 0 || kb >= nKB) {
-                    if (lane == 0) raise_status(P.status, BSA_ERR_BOUNDS);
-                    kb = 0;
+            for (int32_t t = 0; t < n_tiles; ++t) {
+                const int32_t kb = kb_q[0];
+                const bool is_v = tile_is_v(t);
+#pragma unroll
+                for (int i = 0; i + 1 < n_prod; ++i) kb_q[i] = kb_q[i + 1];
+                kb_q[n_prod - 1] = t + n_prod < n_tiles ? tile_kb(t + n_prod) : 0;
+                if (t % n_prod != g) {  // another warp's tile
+                    issued = t + 1;
+                    continue;
                 }
-            } else {
-                kb = block_kb(e);
+                if constexpr (kGather) {
+                    if (t + n_prod < n_tiles) {
+                        const int32_t* mrow = map_head + (int64_t)kb_q[n_prod - 1] * 128;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) tok_next[j] = mrow[32 * j];
+                    }
+                }
+                const int32_t slot = t % C::kStages;
+                const uint32_t phase = (uint32_t)(t / C::kStages) & 1u;
+                int w = 1;
+                if (lane == 0) w = mbar_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                w = __shfl_sync(0xffffffffu, w, 0);
+                if (!w || aborted(bars)) {
+                    if (lane == 0) set_abort(bars, P.status);
+                    break;
+                }
+                const uint32_t fb = smem_u32(&bars->full[slot]);
+                const uint32_t dst = s_ring + slot * C::kTile;
+                if constexpr (kGather) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (tok[j] < 0 || tok[j] >= N) {
+                            raise_status(P.status, BSA_ERR_BOUNDS);
+                            tok[j] = 0;
+                        }
+                    copy_tile<D>(dst, is_v ? P.v : P.k, bh, N, lane, tok);
+                    cp_async_arrive_noinc(fb);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) tok[j] = tok_next[j];
+                } else if (lane == 0) {  // tile load
+                    mbar_arrive_expect_tx(fb, C::kTile);
+                    tma_load_3d(dst, is_v ? &P.map_v : &P.map_k, 0, (int32_t)(bh * N) + kb * 128, 0, fb);
+                }
+                issued = t + 1;
             }
-            const int32_t slot = issued % C::kStages;
-            const uint32_t phase = (uint32_t)(issued / C::kStages) & 1u;
-            int w = 1;
-            if (lane == 0) w = mbar_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
-            w = __shfl_sync(0xffffffffu, w, 0);
-            if (!w || aborted(bars)) {
-                if (lane == 0) set_abort(bars, P.status);
-                return false;
+            // Drain: every issued copy must land before the block exits.
+            if constexpr (kGather) cp_async_wait_all();
+            if (g == 0 && lane == 0) {
+                if (!mbar_wait(smem_u32(&bars->q_full), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT)) raise_status(P.status, BSA_ERR_TIMEOUT);
+                const int32_t first = issued > C::kStages ? issued - C::kStages : 0;
+                for (int32_t i = first; i < issued; ++i)
+                    if (!mbar_wait(smem_u32(&bars->full[i % C::kStages]), (uint32_t)(i / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT))
+                        raise_status(P.status, BSA_ERR_TIMEOUT);
             }
-            const uint32_t fb = smem_u32(&bars->full[slot]);
-            if (lane == 0) mbar_arrive_expect_tx(fb, C::kTile);
-            __syncwarp();
-            load_tile<D>(s_ring + slot * C::kTile, is_v ? &P.map_v : &P.map_k,
-                         is_v ? &P.gmap_v : &P.gmap_k, P.kv_map, bh, N, kb, fb, lane, P.status);
-            ++issued;
-            return true;
-        };
-        // K blocks are fetched in increasing order (lookahead 3), V blocks trail;
-        // both read the list through the same 32-entry window when close enough,
-        // so block_kb may refetch a chunk when the two cross a chunk boundary.
-        for (int32_t e = 0; ok && e < n && e < kSBuf; ++e) ok = put(e, false);
-        for (int32_t i = 0; ok && i < n; ++i) {
-            ok = put(i, true);
-            if (ok && i + kSBuf < n) ok = put(i + kSBuf, false);
-        }
-        // Drain: every issued copy must land before the block exits.
-        if (lane == 0) {
-            if (!mbar_wait(smem_u32(&bars->q_full), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT)) raise_status(P.status, BSA_ERR_TIMEOUT);
-            const int32_t first = issued > C::kStages ? issued - C::kStages : 0;
-            for (int32_t i = first; i < issued; ++i)
-                if (!mbar_wait(smem_u32(&bars->full[i % C::kStages]), (uint32_t)(i / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT))
-                    raise_status(P.status, BSA_ERR_TIMEOUT);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
@@ -360,6 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
             auto issue_qk = [&](int32_t j) -> bool {
                 const int32_t slot = item % C::kStages;
                 if (!mbar_wait(smem_u32(&bars->full[slot]), (uint32_t)(item / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT)) return false;
+                if constexpr (kGather) fence_proxy_async_smem();  // rows written by cp.async
                 tc_fence_after();
                 const uint64_t ks = dk + (uint64_t)((slot * C::kTile) >> 4);
                 const uint32_t d_col = (uint32_t)(j % kSBuf) * 128u;
@@ -380,6 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bsa_forward(const __grid_consta
                 const int32_t slot = item % C::kStages;
                 ok = mbar_wait(smem_u32(&bars->full[slot]), (uint32_t)(item / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
                 if (!ok) break;
+                if constexpr (kGather) fence_proxy_async_smem();
                 tc_fence_after();
                 const uint64_t vs = dv + (uint64_t)((slot * C::kTile) >> 4);
                 const uint32_t p_col = (uint32_t)(i % kSBuf) * 128u;
@@ -596,7 +713,7 @@ size_t smem_bytes() {
     return 1024 + Cfg<D>::kData + sizeof(Barriers);
 }
 
-template <int D, int kPoly, bool kCrm>
+template <int D, int kPoly, bool kCrm, bool kGather>
 cudaError_t prepare_kernel() {
     // Per device: opt in to the large dynamic shared-memory carve-out.
     static int done[64] = {0};
@@ -604,7 +721,7 @@ cudaError_t prepare_kernel() {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(k_bsa_forward<D, kPoly, kCrm>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k_bsa_forward<D, kPoly, kCrm, kGather>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem_bytes<D>());
     if (e == cudaSuccess && dev < 64) done[dev] = 1;
     return e;
@@ -622,10 +739,11 @@ int poly_setting() {
     return v;
 }
 
-template <int D, int kPoly, bool kCrm>
+template <int D, int kPoly, bool kCrm, bool kGather>
 bsa_status launch_dp(const Params& P, unsigned grid_x, unsigned grid_y, cudaStream_t stream) {
-    if (prepare_kernel<D, kPoly, kCrm>() != cudaSuccess) return BSA_ERR_CUDA;
-    k_bsa_forward<D, kPoly, kCrm><<<dim3(grid_x, grid_y), kThreads, smem_bytes<D>(), stream>>>(P);
+    if (prepare_kernel<D, kPoly, kCrm, kGather>() != cudaSuccess) return BSA_ERR_CUDA;
+    k_bsa_forward<D, kPoly, kCrm, kGather>
+        <<<dim3(grid_x, grid_y), threads_for(kGather), smem_bytes<D>(), stream>>>(P);
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
@@ -635,9 +753,10 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
     memset(&P, 0, sizeof(P));
     const uint64_t rows = (uint64_t)a.B * a.H * a.N;
     bool ok = encode_tile_map(&P.map_q, a.q, rows, D) && encode_tile_map(&P.map_k, a.k, rows, D) &&
-              encode_tile_map(&P.map_v, a.v, rows, D) && encode_map(&P.gmap_q, a.q, rows, D, 1) &&
-              encode_map(&P.gmap_k, a.k, rows, D, 1) && encode_map(&P.gmap_v, a.v, rows, D, 1);
+              encode_tile_map(&P.map_v, a.v, rows, D) && encode_map(&P.gmap_q, a.q, rows, D, 1);
     if (!ok) return BSA_ERR_CUDA;
+    P.k = static_cast<const __nv_bfloat16*>(a.k);
+    P.v = static_cast<const __nv_bfloat16*>(a.v);
     P.kv_idx = a.kv_idx;
     P.kv_cnt = a.kv_cnt;
     P.log_w = a.log_w;
@@ -655,16 +774,22 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
     const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
     P.scale_log2 = scale * kLog2e;
     const unsigned gx = (unsigned)P.nQB, gy = (unsigned)(a.B * a.H);
-    if (a.crm != nullptr) return launch_dp<D, kDefaultPoly, true>(P, gx, gy, stream);
-    return poly_setting() == 2 ? launch_dp<D, 2, false>(P, gx, gy, stream)
-                               : launch_dp<D, 0, false>(P, gx, gy, stream);
+    const bool crm = a.crm != nullptr, gather = a.kv_map != nullptr;
+    if (gather)
+        return crm ? launch_dp<D, kDefaultPoly, true, true>(P, gx, gy, stream)
+                   : launch_dp<D, kDefaultPoly, false, true>(P, gx, gy, stream);
+    if (crm) return launch_dp<D, kDefaultPoly, true, false>(P, gx, gy, stream);
+    return poly_setting() == 2 ? launch_dp<D, 2, false, false>(P, gx, gy, stream)
+                               : launch_dp<D, 0, false, false>(P, gx, gy, stream);
 }
 
 template <int D>
 int32_t occupancy() {
     int per_sm = 0;
-    if (prepare_kernel<D, kDefaultPoly, false>() != cudaSuccess) return -1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bsa_forward<D, kDefaultPoly, false>, kThreads,
+    // every instantiation holds one block per SM (shared memory bound)
+    if (prepare_kernel<D, kDefaultPoly, false, false>() != cudaSuccess) return -1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bsa_forward<D, kDefaultPoly, false, false>,
+                                                      threads_for(false),
                                                       smem_bytes<D>()) != cudaSuccess)
         return -1;
     return per_sm;

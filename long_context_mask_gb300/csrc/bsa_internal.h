@@ -24,6 +24,9 @@ cudaError_t launch_index_topk(const float* scores, int64_t rows, int32_t nKB,
                               cudaStream_t stream);
 cudaError_t launch_crm_rows(bsa_idx_mode mode, const void* src, int64_t rows, int32_t nKB, float p,
                             uint32_t* words, int32_t n_words, cudaStream_t stream);
+// dst[bh][p] = src[bh][map[bh][p]] for bf16 rows of D elements (bsa_gather.cu).
+cudaError_t launch_gather_rows(const void* src, const int32_t* map, int64_t heads, int32_t N,
+                               int32_t D, void* dst, int32_t* status, cudaStream_t stream);
 cudaError_t launch_upscale_threshold(const float* T, int64_t heads, int32_t Ub, int32_t Vb,
                                      int32_t Ut, int32_t Vt, float* out, cudaStream_t stream);
 cudaError_t launch_reorder_rows(const int32_t* kv_cnt, const int32_t* order_in, int64_t heads,

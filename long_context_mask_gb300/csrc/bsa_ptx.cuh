@@ -90,6 +90,25 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
         "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
         : "memory");
 }
+// ---------------------------------------------------------------- cp.async
+// 16-byte global -> shared copy through L2 (bypassing L1).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// The barrier receives one arrival from this thread once all of the thread's
+// earlier cp.async copies have landed; the arrival is not pre-counted
+// (.noinc), so the barrier's expected count must include it.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+// Orders shared-memory writes made through the generic proxy (st.shared,
+// cp.async) before later async-proxy reads (tcgen05.mma, TMA) of this thread.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }

@@ -97,6 +97,19 @@ def test_spectral_order_workspace_and_validation(lib):
     assert f(FAKE, FAKE, 8, 2, 100, 80, 10, FAKE, None, 1 << 20, None, None, FAKE, None) == 1
 
 
+def test_gather_rows_host_validation(lib):
+    g = lib.bsa_gather_rows
+    far = ctypes.c_void_p(0x40000000)
+    assert g(FAKE, FAKE, 2, 256, 96, far, None) == 2            # unsupported head dim
+    assert g(FAKE, FAKE, 2, 0, 128, far, None) == 1             # N < 1
+    assert g(FAKE, FAKE, 70000, 256, 128, far, None) == 1       # heads > 65535
+    assert g(FAKE, FAKE, 200, 1 << 24, 128, far, None) == 1     # heads * N >= 2^31
+    assert g(None, FAKE, 2, 256, 128, far, None) == 1           # null src
+    assert g(FAKE_ODD, FAKE, 2, 256, 128, far, None) == 1       # src not 16-byte aligned
+    assert g(FAKE, FAKE, 2, 256, 128, FAKE, None) == 1          # dst overlaps src
+    assert g(None, None, 0, 256, 128, None, None) == 0          # empty: nothing to do
+
+
 def test_device_status_rejects_null_output(lib):
     assert lib.bsa_device_status(None, None) == 1
 
