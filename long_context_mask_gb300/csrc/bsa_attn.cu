@@ -13,10 +13,10 @@
 // WaveAlign section V.
 //
 // Warp roles (8 warps):
-//   warp 0      producer: Q once (one TMA tile copy, or tile::gather4 row
-//               gathers through q_map), then K_j and V_j of every listed
-//               block into a ring of kStages shared-memory slots, one TMA
-//               tile copy each.  The list is read 32 entries at a time by the
+//   warp 0      producer: Q once (one TMA tile copy; with q_map the softmax
+//               warps gather it), then K_j and V_j of every listed block
+//               into a ring of kStages shared-memory slots, one TMA tile
+//               copy each.  The list is read 32 entries at a time by the
 //               whole warp.
 //   warps 6, 7  with kv_map given, warp 0 and these two gather the K/V
 //               tiles in turn: each copies the 128 token rows of its tiles
@@ -31,7 +31,9 @@
 //               read from TMEM.  This lane touches no global memory; it waits
 //               only for P_i and for data, and keeps the tensor core's
 //               instruction queue fed.
-//   warps 2..5  softmax: one thread per query row (TMEM lane); reads S_j,
+//   warps 2..5  softmax: one thread per query row (TMEM lane); with q_map
+//               each warp first copies its 32 query rows into the Q tile
+//               (cp.async, 16 bytes per lane); reads S_j,
 //               updates the running max (log2 domain) and sum, rescales O in
 //               TMEM when the max grows by more than 2^8, writes P_j (bf16)
 //               over S_j, and runs the epilogue (O / l -> bf16 through the
@@ -118,8 +120,8 @@ struct Params {
     // column halves) so that one copy brings a whole 128-row tile, reading
     // each 2D-byte row in full, and lands it as D/64 swizzled 16 KB boxes.
     CUtensorMap map_q, map_k, map_v;     // 3D box 64 x 128 rows x D/64
-    CUtensorMap gmap_q;                  // 2D box 64 x 1 row (gather4 of the Q tile)
-    const __nv_bfloat16* k;              // gathered K/V rows are copied with cp.async
+    const __nv_bfloat16* q;              // gathered rows are copied with cp.async
+    const __nv_bfloat16* k;
     const __nv_bfloat16* v;
     const int32_t* kv_idx;
     const int32_t* kv_cnt;
@@ -153,21 +155,6 @@ __device__ __forceinline__ void set_abort(Barriers* b, int32_t* status) {
     raise_status(status, BSA_ERR_TIMEOUT);
 }
 
-// Token rows of a 128-row tile gathered through a map: lane l covers rows 4l..4l+3.
-__device__ __forceinline__ int4 map_rows(const int32_t* map, int64_t base, int32_t N, int lane,
-                                         int32_t* status) {
-    int4 t = *reinterpret_cast<const int4*>(map + base + 4 * lane);
-    int32_t* v = reinterpret_cast<int32_t*>(&t);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        if (v[i] < 0 || v[i] >= N) {
-            raise_status(status, BSA_ERR_BOUNDS);
-            v[i] = 0;
-        }
-    }
-    return t;
-}
-
 // One K/V tile gathered through a map, copied 16 bytes per lane into the
 // 128-byte-swizzled box layout that a TMA tile copy would write (chunk c of
 // row r lands at chunk c ^ (r mod 8) of its 128-byte line).  Lane l holds
@@ -198,22 +185,25 @@ __device__ __forceinline__ void copy_tile(uint32_t dst, const __nv_bfloat16* bas
     }
 }
 
+// Rows 32 g .. 32 g + 31 of a tile gathered through a map (lane l holds the
+// token of row 32 g + l), copied like copy_tile.  The softmax warps load the
+// query tile this way, each warp the 32 rows it owns.
 template <int D>
-__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* tile_map,
-                                          const CUtensorMap* gather_map, const int32_t* map,
-                                          int64_t bh, int32_t N, int32_t blk, uint32_t bar,
-                                          int lane, int32_t* status) {
+__device__ __forceinline__ void copy_rows32(uint32_t dst, const __nv_bfloat16* base, int64_t bh,
+                                            int32_t N, int g, int lane, int32_t tok) {
     using C = Cfg<D>;
-    const int32_t row0 = (int32_t)(bh * N) + blk * 128;
-    if (map == nullptr) {
-        if (lane == 0) tma_load_3d(dst, tile_map, 0, row0, 0, bar);
-    } else {
-        const int4 t = map_rows(map, bh * N + (int64_t)blk * 128, N, lane, status);
-        const int32_t base = (int32_t)(bh * N);
+    constexpr int kLanesPerRow = D / 8;
+    constexpr int kRowsPerCopy = 32 / kLanesPerRow;
+    const int sub = lane / kLanesPerRow, chunk = lane % kLanesPerRow;
+    const int box = chunk >> 3, c = chunk & 7;
+    const uint32_t d0 = dst + box * C::kBoxBytes + ((uint32_t)c << 4);
+    const __nv_bfloat16* s0 = base + bh * N * D + box * 64 + c * 8;
 #pragma unroll
-        for (int b = 0; b < C::kBoxes; ++b)
-            tma_gather4(dst + b * C::kBoxBytes + lane * 512, gather_map, 64 * b, base + t.x,
-                        base + t.y, base + t.z, base + t.w, bar);
+    for (int k = 0; k < 32 / kRowsPerCopy; ++k) {
+        const int rl = k * kRowsPerCopy + sub;
+        const int r = 32 * g + rl;
+        const int32_t t = __shfl_sync(0xffffffffu, tok, rl);
+        cp_async16((d0 + r * 128) ^ ((uint32_t)(r & 7) << 4), s0 + (int64_t)t * D);
     }
 }
 
@@ -300,7 +290,8 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
             mbar_init(smem_u32(&bars->full[s]), kGather ? 32 : 1);
             mbar_init(smem_u32(&bars->empty[s]), 1);
         }
-        mbar_init(smem_u32(&bars->q_full), 1);
+        // Q by one TMA tile copy, or gathered by the 128 softmax threads
+        mbar_init(smem_u32(&bars->q_full), P.q_map ? 128 : 1);
         for (int s = 0; s < kSBuf; ++s) mbar_init(smem_u32(&bars->p_full[s]), 128);
         mbar_init(smem_u32(&bars->mma_done), 1);
         bars->abort = 0;
@@ -332,11 +323,9 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
         constexpr int n_prod = kGather ? kGatherWarps : 1;
         if (g < n_prod) {
             int32_t issued = 0;
-            if (g == 0) {
-                if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bars->q_full), C::kTile);
-                __syncwarp();
-                load_tile<D>(s_q, &P.map_q, &P.gmap_q, P.q_map, bh, N, qb, smem_u32(&bars->q_full), lane,
-                             P.status);
+            if (g == 0 && P.q_map == nullptr && lane == 0) {  // gathered Q: the softmax warps
+                mbar_arrive_expect_tx(smem_u32(&bars->q_full), C::kTile);
+                tma_load_3d(s_q, &P.map_q, 0, (int32_t)(bh * N) + qb * 128, 0, smem_u32(&bars->q_full));
             }
             // Load order = MMA consumption order: K_0, K_1, K_2, then V_i, K_{i+3}.
             // The list is read 32 entries at a time with one coalesced load and
@@ -470,6 +459,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
             const uint64_t dk = smem_desc_sw128(s_ring, 16, 1024);
             const uint64_t dv = smem_desc_sw128(s_ring, C::kBoxBytes, 1024);
             bool ok = mbar_wait(smem_u32(&bars->q_full), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+            if (P.q_map != nullptr) fence_proxy_async_smem();  // Q rows written by cp.async
             tc_fence_after();
             int32_t item = 0;  // ring position of the next tile (same order as the producer)
             auto issue_qk = [&](int32_t j) -> bool {
@@ -529,6 +519,10 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
                 raise_status(P.status, BSA_ERR_BOUNDS);
                 tok_ok = false;
             }
+            // this warp's 32 query rows into the Q tile (row 0 stands in for
+            // an invalid token; that row's output is not written)
+            copy_rows32<D>(s_q, P.q, bh, N, qd, lane, tok_ok ? tok : 0);
+            cp_async_arrive_noinc(smem_u32(&bars->q_full));
         }
         const float sl2 = P.scale_log2;
         const float* lw_row = P.log_w ? P.log_w + row * max_kv : nullptr;
@@ -660,6 +654,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
         }
     }
 
+    cp_async_wait_all();  // no copies of this thread may outlive the block
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -690,19 +685,6 @@ bool encode_tile_map(CUtensorMap* map, const void* base, uint64_t rows, int D) {
     cuuint32_t box[3] = {64, 128, (cuuint32_t)(D / 64)};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-bool encode_map(CUtensorMap* map, const void* base, uint64_t rows, int D, uint32_t box_rows) {
-    auto enc = get_encode();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -753,8 +735,9 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
     memset(&P, 0, sizeof(P));
     const uint64_t rows = (uint64_t)a.B * a.H * a.N;
     bool ok = encode_tile_map(&P.map_q, a.q, rows, D) && encode_tile_map(&P.map_k, a.k, rows, D) &&
-              encode_tile_map(&P.map_v, a.v, rows, D) && encode_map(&P.gmap_q, a.q, rows, D, 1);
+              encode_tile_map(&P.map_v, a.v, rows, D);
     if (!ok) return BSA_ERR_CUDA;
+    P.q = static_cast<const __nv_bfloat16*>(a.q);
     P.k = static_cast<const __nv_bfloat16*>(a.k);
     P.v = static_cast<const __nv_bfloat16*>(a.v);
     P.kv_idx = a.kv_idx;

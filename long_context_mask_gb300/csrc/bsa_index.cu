@@ -13,7 +13,7 @@
 //    (head, bucket of W slots); each row's slot in its bucket is its rank
 //    under (count descending, input position ascending).
 //  * Block sampling (InstaGen section 3.2.1 eq. (4), systematic PPS,
-//    Algorithm 1 step 13): one thread per row, fp64, fixed summation order,
+//    Algorithm 1 step 13): one thread per row, fp32, fixed summation order,
 //    explicit round-to-nearest arithmetic (never fused).
 #include <cuda_runtime.h>
 #include <math.h>
@@ -221,9 +221,9 @@ __global__ void __launch_bounds__(128) k_sample_blocks(
     if (row >= rows) return;
     // NULL scores: the uniform sampler, every residual block scored 1
     const float* s = scores ? scores + row * (int64_t)nKB : nullptr;
-    uint32_t ex[kWords], taken[kWords], drawn[kWords];  // exact / exact+promoted / drawn
+    uint32_t taken[kWords], drawn[kWords];  // exact + promoted / drawn
     const int32_t nw = (nKB + 31) >> 5;
-    for (int32_t w = 0; w < nw; ++w) ex[w] = taken[w] = drawn[w] = 0u;
+    for (int32_t w = 0; w < nw; ++w) taken[w] = drawn[w] = 0u;
     const int32_t ec = exact_cnt[row];
     for (int32_t e = 0; e < ec; ++e) {
         const int32_t kb = exact_idx[row * (int64_t)exact_stride + e];
@@ -231,26 +231,34 @@ __global__ void __launch_bounds__(128) k_sample_blocks(
             raise_status(status, BSA_ERR_BOUNDS);
             continue;
         }
-        bit_set(ex, kb);
         bit_set(taken, kb);
     }
     int32_t n_res = 0;
-    for (int32_t kb = 0; kb < nKB; ++kb) n_res += !bit_get(taken, kb);
+    for (int32_t w = 0; w < nw; ++w) n_res += __popc(taken[w]);
+    n_res = nKB - n_res;
 
-    double lambda = 0.0;
+    // fp32 throughout, IEEE round-to-nearest without contraction, sums in
+    // ascending block order: these values decide which blocks are drawn
+    float lambda = 0.0f;
     if (n_res <= m) {
         for (int32_t w = 0; w < nw; ++w) taken[w] = 0xffffffffu;  // all residual blocks promoted
     } else {
         // eq. (4): cap at 1 and renormalise until the capped set is stable
         int32_t n_cap = 0;
         for (;;) {
-            double sum = 0.0;
-            for (int32_t kb = 0; kb < nKB; ++kb)
-                if (!bit_get(taken, kb)) sum = __dadd_rn(sum, s ? (double)s[kb] : 1.0);
-            lambda = __ddiv_rn((double)(m - n_cap), sum);
+            float sum = 0.0f, smax = 0.0f;
+            for (int32_t kb = 0; kb < nKB; ++kb) {
+                if (bit_get(taken, kb)) continue;
+                const float x = s ? s[kb] : 1.0f;
+                sum = __fadd_rn(sum, x);
+                smax = fmaxf(smax, x);
+            }
+            lambda = __fdiv_rn((float)(m - n_cap), sum);
+            // rounding is monotone: if the largest score stays below 1, all do
+            if (__fmul_rn(lambda, smax) < 1.0f) break;
             bool grew = false;
             for (int32_t kb = 0; kb < nKB; ++kb) {
-                if (!bit_get(taken, kb) && __dmul_rn(lambda, s ? (double)s[kb] : 1.0) >= 1.0) {
+                if (!bit_get(taken, kb) && __fmul_rn(lambda, s ? s[kb] : 1.0f) >= 1.0f) {
                     bit_set(taken, kb);
                     ++n_cap;
                     grew = true;
@@ -260,15 +268,14 @@ __global__ void __launch_bounds__(128) k_sample_blocks(
         }
         // systematic PPS over the uncapped residual, ascending block order
         const int32_t m_rest = m - n_cap;
-        const double ur = u[row];
-        double C = 0.0;
+        const float ur = __double2float_rn(u[row]);
+        float C = 0.0f;
         int32_t nd = 0;
-        for (int32_t kb = 0; kb < nKB; ++kb) {
+        for (int32_t kb = 0; kb < nKB && nd < m_rest; ++kb) {
             if (bit_get(taken, kb)) continue;
-            const double pj = __dmul_rn(lambda, s ? (double)s[kb] : 1.0);
-            const double C_prev = C;
-            C = __dadd_rn(C, pj);
-            if (nd < m_rest && ceil(__dsub_rn(C, ur)) > ceil(__dsub_rn(C_prev, ur))) {
+            const float C_prev = C;
+            C = __fadd_rn(C, __fmul_rn(lambda, s ? s[kb] : 1.0f));
+            if (ceilf(__fsub_rn(C, ur)) > ceilf(__fsub_rn(C_prev, ur))) {
                 bit_set(drawn, kb);
                 ++nd;
             }
@@ -277,15 +284,21 @@ __global__ void __launch_bounds__(128) k_sample_blocks(
     int32_t n = 0, total = 0;
     int32_t* out = kv_idx + row * (int64_t)max_kv;
     float* lw = log_w + row * (int64_t)max_kv;
-    for (int32_t kb = 0; kb < nKB; ++kb) {
-        const bool t = bit_get(taken, kb), d = bit_get(drawn, kb);
-        if (!t && !d) continue;
-        if (n < max_kv) {
-            out[n] = kb;
-            lw[n] = d ? (float)(-log(__dmul_rn(lambda, s ? (double)s[kb] : 1.0))) : 0.0f;
-            ++n;
+    for (int32_t w = 0; w < nw; ++w) {
+        uint32_t bits = taken[w] | drawn[w];
+        if (32 * w + 32 > nKB) bits &= (nKB - 32 * w >= 32) ? 0xffffffffu : ((1u << (nKB - 32 * w)) - 1u);
+        while (bits) {
+            const int32_t kb = 32 * w + __ffs(bits) - 1;
+            bits &= bits - 1u;
+            if (n < max_kv) {
+                out[n] = kb;
+                // drawn: -log(pi) evaluated in double from the fp32 pi
+                lw[n] = bit_get(drawn, kb) ? (float)(-log((double)__fmul_rn(lambda, s ? s[kb] : 1.0f)))
+                                           : 0.0f;
+                ++n;
+            }
+            ++total;
         }
-        ++total;
     }
     for (int32_t e = n; e < max_kv; ++e) {
         out[e] = -1;
@@ -293,7 +306,6 @@ __global__ void __launch_bounds__(128) k_sample_blocks(
     }
     kv_cnt[row] = n;
     if (total > max_kv) raise_status(status, BSA_ERR_OVERFLOW);
-    (void)ex;
 }
 
 }  // namespace

@@ -187,8 +187,12 @@ void oracle_reorder_rows(const int32_t* kv_cnt, const int32_t* order_in, int64_t
 /* Output list: exact, promoted and sampled blocks merged in ascending block */
 /* order, with log_w 0 for exact and promoted entries.  Returns the number   */
 /* of rows whose merged list did not fit in max_kv (truncated).              */
-/* Summation order is ascending block order; the file is built without      */
-/* fused multiply-adds.                                                      */
+/* Arithmetic: these floating-point values decide integers (which blocks    */
+/* are capped and drawn), so they are computed in the GPU sampler's          */
+/* precision, fp32 (the pages fix none): sums in ascending block order,      */
+/* IEEE round-to-nearest, no fused multiply-adds (the file is built with     */
+/* -ffp-contract=off).  u is rounded to fp32 first.  The log-weights are     */
+/* -log(pi) evaluated in double from the fp32 pi and rounded to fp32.        */
 /* ------------------------------------------------------------------------- */
 int64_t oracle_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
                              const int32_t* exact_idx, const int32_t* exact_cnt,
@@ -197,7 +201,7 @@ int64_t oracle_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
                              int32_t max_kv) {
     int64_t overflow = 0;
     uint8_t* state = (uint8_t*)malloc((size_t)nKB); /* 0 residual, 1 exact, 2 promoted, 3 sampled */
-    double* pi = (double*)malloc(sizeof(double) * (size_t)nKB);
+    float* pi = (float*)malloc(sizeof(float) * (size_t)nKB);
     /* NULL scores: the uniform sampler (InstaGen Algorithm 1 steps 6-8), i.e.
        every residual block with the same score and pi_j = m / |R|. */
     float* ones = NULL;
@@ -219,15 +223,15 @@ int64_t oracle_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
         } else {
             /* eq. (4): cap at 1 and renormalise until the capped set is stable */
             int32_t n_cap = 0;
-            double lambda = 0.0;
+            float lambda = 0.0f;
             for (;;) {
-                double sum = 0.0;
+                float sum = 0.0f;
                 for (int32_t kb = 0; kb < nKB; ++kb)
-                    if (state[kb] == 0) sum += (double)s[kb];
-                lambda = (double)(m - n_cap) / sum;
+                    if (state[kb] == 0) sum += s[kb];
+                lambda = (float)(m - n_cap) / sum;
                 int32_t grew = 0;
                 for (int32_t kb = 0; kb < nKB; ++kb) {
-                    if (state[kb] == 0 && lambda * (double)s[kb] >= 1.0) {
+                    if (state[kb] == 0 && lambda * s[kb] >= 1.0f) {
                         state[kb] = 2;
                         ++n_cap;
                         grew = 1;
@@ -237,15 +241,15 @@ int64_t oracle_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
             }
             /* systematic PPS over the uncapped residual */
             const int32_t m_rest = m - n_cap;
-            const double ur = u[r];
-            double C = 0.0;
+            const float ur = (float)u[r];
+            float C = 0.0f;
             int32_t drawn = 0;
             for (int32_t kb = 0; kb < nKB; ++kb) {
                 if (state[kb] != 0) continue;
-                const double p = lambda * (double)s[kb];
-                const double C_prev = C;
+                const float p = lambda * s[kb];
+                const float C_prev = C;
                 C = C + p;
-                if (drawn < m_rest && ceil(C - ur) > ceil(C_prev - ur)) {
+                if (drawn < m_rest && ceilf(C - ur) > ceilf(C_prev - ur)) {
                     state[kb] = 3;
                     pi[kb] = p;
                     ++drawn;
@@ -258,7 +262,7 @@ int64_t oracle_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
             if (state[kb] == 0) continue;
             if (n < max_kv) {
                 kv_idx[r * max_kv + n] = kb;
-                log_w[r * max_kv + n] = state[kb] == 3 ? (float)(-log(pi[kb])) : 0.0f;
+                log_w[r * max_kv + n] = state[kb] == 3 ? (float)(-log((double)pi[kb])) : 0.0f;
                 ++n;
             }
             ++total;
