@@ -53,8 +53,8 @@ def _load():
         lib.oracle_reorder_rows.restype = None
         lib.oracle_sample_blocks.argtypes = [P, i64, i32, P, P, i32, i32, P, P, P, P, i32]
         lib.oracle_sample_blocks.restype = i64
-        lib.oracle_attention.argtypes = [P, P, P, i32, i32, i32, i32, P, P, i32, P, P, P,
-                                         f64, P, i64, P, P, P]
+        lib.oracle_attention.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, i32, P, P, P,
+                                         i32, i32, i32, i32, f64, P, i64, P, P, P]
         lib.oracle_attention.restype = None
         lib.oracle_crm_rows.argtypes = [i32, P, i64, i32, f32, P, i32]
         lib.oracle_crm_rows.restype = None
@@ -210,18 +210,24 @@ def spectral_order(kv_idx, kv_cnt, n_kb, x0, iters):
 
 
 def attention(q, k, v, kv_idx, kv_cnt, log_w=None, q_map=None, kv_map=None, scale=0.0,
-              sel=None):
+              sel=None, causal=False, n_valid=0, window=0, sinks=0):
     """Block-sparse attention from the definition, fp64.
 
-    q, k, v: uint16 bf16 bit patterns [B, H, N, D] (or torch bf16 tensors on CPU).
+    q: uint16 bf16 bit patterns [B, H, N, D] (or a torch bf16 tensor on CPU);
+    k, v: [B, H_kv, N, D] with H a multiple of H_kv (grouped heads).
     kv_idx [B*H*nQB, max_kv], kv_cnt [B*H*nQB]; log_w like kv_idx or None;
-    q_map / kv_map int32 [B*H, N] or None.  ``sel`` lists the flat query blocks
-    (bh * nQB + qb) to evaluate (all when None).
+    q_map int32 [B*H, N] or None; kv_map int32 [B*H_kv, N] or None.
+    Token mask: key j is dropped for query i unless j < n_valid (n_valid <= 0:
+    N), (not causal or j <= i) and (window <= 0 or j > i - window or j < sinks).
+    ``sel`` lists the flat query blocks (bh * nQB + qb) to evaluate (all when None).
     Returns (O fp64 [nsel*128, D], LSE fp64 [nsel*128], tok int32 [nsel*128]),
     where row x belongs to original query token tok[x] of head sel[x // 128] // nQB.
     """
     q, k, v = (_as_u16(t) for t in (q, k, v))
     B, H, N, D = q.shape
+    H_kv = k.shape[1]
+    if H % H_kv or k.shape != v.shape or k.shape[0] != B or k.shape[2:] != (N, D):
+        raise ValueError("attention: k, v must be [B, H_kv, N, D] with H a multiple of H_kv")
     nqb = N // 128
     kv_idx = _c(kv_idx, np.int32)
     kv_cnt = _c(kv_cnt, np.int32)
@@ -234,9 +240,10 @@ def attention(q, k, v, kv_idx, kv_cnt, log_w=None, q_map=None, kv_map=None, scal
     O = np.empty((n * 128, D), np.float64)
     L = np.empty(n * 128, np.float64)
     tok = np.empty(n * 128, np.int32)
-    _load().oracle_attention(_ptr(q), _ptr(k), _ptr(v), B, H, N, D, _ptr(kv_idx), _ptr(kv_cnt),
-                             max_kv, _ptr(log_w), _ptr(q_map), _ptr(kv_map), float(scale),
-                             _ptr(sel), n, _ptr(O), _ptr(L), _ptr(tok))
+    _load().oracle_attention(_ptr(q), _ptr(k), _ptr(v), B, H, H_kv, N, D, _ptr(kv_idx),
+                             _ptr(kv_cnt), max_kv, _ptr(log_w), _ptr(q_map), _ptr(kv_map),
+                             int(bool(causal)), int(n_valid), int(window), int(sinks),
+                             float(scale), _ptr(sel), n, _ptr(O), _ptr(L), _ptr(tok))
     return O, L, tok
 
 

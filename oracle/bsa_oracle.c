@@ -283,7 +283,7 @@ int64_t oracle_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
 /* ------------------------------------------------------------------------- */
 /* Masked, log-weighted softmax attention from its definition.               */
 /*                                                                           */
-/* Tensors q, k, v are bf16 bit patterns laid out [B*H, N, D].  Gathered    */
+/* Tensor q is a bf16 bit pattern laid out [B*H, N, D].  Gathered           */
 /* position p of head bh holds query token q_map[bh][p] (p itself when       */
 /* q_map is NULL) and key/value token kv_map[bh][p] (likewise).  The query   */
 /* block of p is p / 128; its KV list is kv_idx[row][0..kv_cnt[row]) with   */
@@ -295,21 +295,36 @@ int64_t oracle_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
 /*     s_j   = (q_i . k_j) * scale + lw          over every listed key j     */
 /*     LSE_i = ln sum_j exp(s_j)                 (max-shifted)               */
 /*     O_i   = sum_j exp(s_j - LSE_i) v_j                                    */
-/* An empty list gives O_i = 0 and LSE_i = -inf.  Results go to              */
+/* Grouped keys/values (INTRA, "Attention Timing Comparison": 32 query      */
+/* heads over 8 key/value heads): k, v and kv_map hold H_kv heads per batch  */
+/* entry, and query head h of batch b reads key/value head                   */
+/* b * H_kv + h / (H / H_kv).                                                */
+/*                                                                           */
+/* Token mask (INTRA, "Mapping Back to INTRA" and "CQS-Aware Token-Sparse    */
+/* FlashAttention Kernel": causal masking inside packed tiles, sliding       */
+/* windows with sink tokens): key token j is dropped from query token i's   */
+/* sum unless                                                                */
+/*     j < n_valid                      (tail padding; n_valid <= 0: N)      */
+/*     and (!causal or j <= i)                                               */
+/*     and (window <= 0 or j > i - window or j < sinks).                     */
+/* An empty list, or a row whose listed keys are all dropped, gives          */
+/* O_i = 0 and LSE_i = -inf.  Results go to                                  */
 /* O[(i_sel*128 + r) * D + d], LSE[i_sel*128 + r], and tok[...] = i, the     */
 /* original token the row belongs to (the scatter-back target).             */
 /* scale <= 0 selects 1/sqrt(D).                                             */
 /* ------------------------------------------------------------------------- */
 void oracle_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                      int32_t B, int32_t H, int32_t N, int32_t D,
+                      int32_t B, int32_t H, int32_t H_kv, int32_t N, int32_t D,
                       const int32_t* kv_idx, const int32_t* kv_cnt, int32_t max_kv,
                       const float* log_w, const int32_t* q_map, const int32_t* kv_map,
+                      int32_t causal, int32_t n_valid, int32_t window, int32_t sinks,
                       double scale, const int64_t* sel, int64_t nsel,
                       double* O, double* LSE, int32_t* tok) {
     const int32_t nQB = N / ORACLE_BLOCK;
     if (scale <= 0.0) scale = 1.0 / sqrt((double)D);
+    if (n_valid <= 0) n_valid = N;
+    const int32_t group = H / H_kv;
     (void)B;
-    (void)H;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t w = 0; w < nsel * ORACLE_BLOCK; ++w) {
         const int64_t i_sel = w / ORACLE_BLOCK;
@@ -319,6 +334,7 @@ void oracle_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
         const int32_t qb = (int32_t)(row % nQB);
         const int32_t p = qb * ORACLE_BLOCK + r;
         const int32_t i = q_map ? q_map[bh * N + p] : p;
+        const int64_t kvh = (bh / H) * H_kv + (bh % H) / group; /* key/value head */
         const int32_t cnt = kv_cnt[row];
         double* o = O + w * D;
         tok[w] = i;
@@ -337,21 +353,31 @@ void oracle_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
             const double lw = log_w ? (double)log_w[row * max_kv + e] : 0.0;
             for (int32_t t = 0; t < ORACLE_BLOCK; ++t) {
                 const int32_t pos = kb * ORACLE_BLOCK + t;
-                const int32_t j = kv_map ? kv_map[bh * N + pos] : pos;
+                const int32_t j = kv_map ? kv_map[kvh * N + pos] : pos;
+                const int visible = j < n_valid && (!causal || j <= i) &&
+                                    (window <= 0 || j > i - window || j < sinks);
                 double dot = 0.0;
-                for (int32_t d = 0; d < D; ++d) dot += qi[d] * bf16_to_double(k[(bh * N + j) * D + d]);
-                s[e * ORACLE_BLOCK + t] = dot * scale + lw;
+                for (int32_t d = 0; d < D; ++d) dot += qi[d] * bf16_to_double(k[(kvh * N + j) * D + d]);
+                s[e * ORACLE_BLOCK + t] = visible ? dot * scale + lw : -INFINITY;
                 key[e * ORACLE_BLOCK + t] = j;
             }
         }
         double mx = -INFINITY;
         for (int64_t x = 0; x < nkeys; ++x) mx = s[x] > mx ? s[x] : mx;
+        if (mx == -INFINITY) { /* every listed key dropped */
+            LSE[w] = -INFINITY;
+            free(qi);
+            free(key);
+            free(s);
+            continue;
+        }
         double z = 0.0;
         for (int64_t x = 0; x < nkeys; ++x) z += exp(s[x] - mx);
         const double lse = mx + log(z);
         for (int64_t x = 0; x < nkeys; ++x) {
             const double a = exp(s[x] - lse);
-            const uint16_t* vj = v + (bh * N + key[x]) * D;
+            if (s[x] == -INFINITY) continue;
+            const uint16_t* vj = v + (kvh * N + key[x]) * D;
             for (int32_t d = 0; d < D; ++d) o[d] += a * bf16_to_double(vj[d]);
         }
         LSE[w] = lse;

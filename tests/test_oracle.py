@@ -604,3 +604,91 @@ def test_upscale_is_identity_at_scale_one_and_conservative_for_every_threshold()
                         assert out[h, u, v] <= p
                     nb = T[h, i0:min(i0 + 2, 9), j0:min(j0 + 2, 11)]
                     assert out[h, u, v] >= nb.min()
+
+
+# --------------------------------------------------------------------------
+# Token masks and grouped key/value heads (INTRA: causal masking inside packed
+# tiles, sliding windows with sinks, 32 query heads over 8 key/value heads).
+# --------------------------------------------------------------------------
+def _masked_dense(q, k, v, allowed):
+    """Matrix-form softmax attention of one head over an explicit [N, N]
+    boolean mask (rows: query tokens, columns: key tokens); fully masked rows
+    give O = 0, LSE = -inf."""
+    S = (q @ k.T) / math.sqrt(q.shape[1])
+    S = np.where(allowed, S, -np.inf)
+    mx = S.max(1, keepdims=True)
+    safe = np.where(np.isfinite(mx), mx, 0.0)
+    P = np.exp(S - safe)
+    z = P.sum(1, keepdims=True)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        O = np.where(z > 0, (P @ v) / np.where(z > 0, z, 1), 0.0)
+        L = np.where(z[:, 0] > 0, np.log(np.where(z[:, 0] > 0, z[:, 0], 1)) + safe[:, 0], -np.inf)
+    return O, L
+
+
+def _allowed(N, causal=False, n_valid=0, window=0, sinks=0):
+    i = np.arange(N)[:, None]
+    j = np.arange(N)[None, :]
+    a = np.broadcast_to(j < (n_valid if n_valid > 0 else N), (N, N)).copy()
+    if causal:
+        a &= j <= i
+    if window > 0:
+        a &= (j > i - window) | (j < sinks)
+    return a
+
+
+@pytest.mark.parametrize("kw", [dict(causal=True), dict(causal=True, window=100, sinks=16),
+                                dict(n_valid=300), dict(causal=True, n_valid=333)])
+def test_token_mask_all_blocks_equals_matrix_form(kw):
+    N, D, nb = 384, 16, 3
+    q, k, v = (_bf16((1, 1, N, D), s) for s in (81, 82, 83))
+    O, L, tok = oracle.attention(q, k, v, *_all_blocks(nb, nb), **kw)
+    o, lse = _by_token(O, L, tok, N)
+    Oref, Lref = _masked_dense(_f64(q[0, 0]), _f64(k[0, 0]), _f64(v[0, 0]), _allowed(N, **kw))
+    np.testing.assert_allclose(o, Oref, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(Lref))
+    fin = np.isfinite(Lref)
+    np.testing.assert_allclose(lse[fin], Lref[fin], rtol=0, atol=1e-12)
+
+
+def test_causal_mask_is_on_original_tokens_under_maps():
+    """With every block listed the kept set is every key whatever the maps, so
+    causal attention through arbitrary maps equals plain causal attention."""
+    N, D, nb = 384, 16, 3
+    q, k, v = (_bf16((1, 1, N, D), s) for s in (84, 85, 86))
+    g = np.random.default_rng(8)
+    qm, km = (g.permutation(N).astype(np.int32)[None] for _ in range(2))
+    O, L, tok = oracle.attention(q, k, v, *_all_blocks(nb, nb), q_map=qm, kv_map=km, causal=True)
+    o, lse = _by_token(O, L, tok, N)
+    Oref, Lref = _masked_dense(_f64(q[0, 0]), _f64(k[0, 0]), _f64(v[0, 0]), _allowed(N, causal=True))
+    np.testing.assert_allclose(o, Oref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, Lref, rtol=0, atol=1e-12)
+
+
+def test_fully_masked_row_is_empty():
+    N, D = 384, 16
+    q, k, v = (_bf16((1, 1, N, D), s) for s in (87, 88, 89))
+    idx = np.array([[2], [2], [1]], np.int32)  # blocks 0, 1 list only a later block
+    cnt = np.ones(3, np.int32)
+    O, L, tok = oracle.attention(q, k, v, idx, cnt, causal=True)
+    assert np.all(np.isneginf(L[:256])) and np.all(O[:256] == 0)
+    assert np.all(np.isfinite(L[256:]))
+
+
+def test_grouped_heads_equal_repeated_heads_and_matrix_form():
+    B, H, H_kv, N, D, nb = 2, 4, 2, 256, 16, 2
+    q = _bf16((B, H, N, D), 90)
+    k, v = _bf16((B, H_kv, N, D), 91), _bf16((B, H_kv, N, D), 92)
+    idx, cnt = _all_blocks(B * H * nb, nb)
+    O, L, tok = oracle.attention(q, k, v, idx, cnt, causal=True)
+    rep = lambda t: t.repeat_interleave(H // H_kv, dim=1)  # noqa: E731
+    O2, L2, _ = oracle.attention(q, rep(k), rep(v), idx, cnt, causal=True)
+    np.testing.assert_array_equal(O, O2)
+    np.testing.assert_array_equal(L, L2)
+    # query head 3 of batch 1 reads key/value head 1 of batch 1
+    bh = 1 * H + 3
+    rows = slice(bh * nb * 128, (bh + 1) * nb * 128)
+    o, lse = _by_token(O[rows], L[rows], tok[rows], N)
+    Oref, Lref = _masked_dense(_f64(q[1, 3]), _f64(k[1, 1]), _f64(v[1, 1]), _allowed(N, causal=True))
+    np.testing.assert_allclose(o, Oref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, Lref, rtol=0, atol=1e-12)
