@@ -192,6 +192,7 @@ class Path:
         if kv_gather == "auto":
             kv_gather = "kernel" if prob.diag_list else "hbm"
         self.pregather = self.kv_map is not None and kv_gather == "hbm" and not self.crm
+        self.masked = uses_masked_forward(prob)
         if self.pregather:
             self.kg, self.vg = torch.empty_like(self.k), torch.empty_like(self.v)
         self.launches_per_step = (1 + 2 * self.pregather + (self.mode is not None) + bool(prob.m_sample)
@@ -233,6 +234,12 @@ class Path:
         k, v, kv_map = self.k, self.v, self.kv_map
         if self.pregather:
             k, v, kv_map = self.kg, self.vg, None
+        if self.masked:
+            self.bsa.forward_masked(self.q, k, v, idx, cnt, self.o, self.lse, log_w=self.lw,
+                                    q_map=self.q_map, kv_map=kv_map,
+                                    row_perm=None if self.order == "identity" else self.row_perm,
+                                    **token_mask(self.prob))
+            return
         self.bsa.forward(self.q, k, v, idx, cnt, self.o, self.lse, log_w=self.lw,
                          q_map=self.q_map, kv_map=kv_map,
                          row_perm=None if self.order == "identity" else self.row_perm)
@@ -280,13 +287,21 @@ def time_oracle(prob, lists, budget_s: float, max_blocks: int | None = None, see
         sel = order[done:done + chunk]
         t0 = time.perf_counter()
         oracle.attention(prob.q, prob.k, prob.v, idx, cnt, log_w=lw, q_map=prob.q_map,
-                         kv_map=prob.kv_map, sel=sel)
+                         kv_map=prob.kv_map, sel=sel, **token_mask(prob))
         t_total += time.perf_counter() - t0
         fl += float(cnt[sel].sum()) * 4 * 128 * 128 * prob.D
         done += len(sel)
         if t_total >= budget_s or (max_blocks and done >= max_blocks):
             break
     return fl / t_total / 1e12, t_total, done, oracle.num_threads()
+
+
+def token_mask(prob):
+    return dict(causal=prob.causal, n_valid=prob.n_valid, window=prob.window, sinks=prob.sinks)
+
+
+def uses_masked_forward(prob):
+    return (prob.H_kv not in (None, prob.H)) or prob.causal or prob.window > 0 or prob.n_valid > 0
 
 
 def host_lists(prob):
@@ -315,7 +330,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6])
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8])
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller profiling case)")
     ap.add_argument("--order", default="reordered", choices=["reordered", "identity", "spectral"],
                     help="row order: NNZ-guided wave sort, identity, or spectral (stage 1) + wave sort")
@@ -372,7 +387,10 @@ def config_dict(prob, config, order, density, world):
             "parallelism": "one independent workload per GPU" if world > 1 else "single GPU",
             "scores": "from Q/K inside the step" if getattr(prob, "_scores_on_gpu", False) else "given",
             "kv_sets": "CRM bitmask rows" if getattr(prob, "_crm", False) else "index lists",
-            "kv_rows": getattr(prob, "_kv_rows", "contiguous")}
+            "kv_rows": getattr(prob, "_kv_rows", "contiguous"),
+            **({"H_kv": prob.H_kv or prob.H, "token_mask": token_mask(prob),
+                "flops": "listed blocks in full (masked keys inside a listed block are computed)"}
+               if uses_masked_forward(prob) else {})}
 
 
 def run_reference(args, world, rank):

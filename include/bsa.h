@@ -289,6 +289,41 @@ bsa_status bsa_forward(const void* q, const void* k, const void* v, int32_t B, i
                        float* lse, void* stream);
 
 /*
+ * bsa_forward_masked - bsa_forward with grouped key/value heads and a token
+ * mask inside the listed blocks.
+ *
+ * Defined by: INTRA, "Mapping Back to INTRA" (block-level sparse layers
+ * subject to causal masking; sliding windows with sink tokens), "CQS-Aware
+ * Token-Sparse FlashAttention Kernel" (masking within the packed tiles) and
+ * "Attention Timing Comparison" (32 query heads over 8 key/value heads).
+ *
+ * As bsa_forward, except:
+ *  - k and v hold H_kv heads per batch entry, [B, H_kv, N, D]; query head h
+ *    of batch entry b reads key/value head b*H_kv + h/(H/H_kv).  kv_map, if
+ *    given, is [B*H_kv, N].  H must be a multiple of H_kv.
+ *  - With i the original query token and j the original key token (after
+ *    the maps), key j is dropped from row i's softmax unless
+ *        j < n_valid                        (n_valid = 0: N)
+ *        and (causal == 0 or j <= i)
+ *        and (window == 0 or j > i - window or j < sinks).
+ *    A row whose listed keys are all dropped gets O = 0 and LSE = -inf.
+ *    Dropped keys still cost their block's work: list only blocks that hold
+ *    some visible key.
+ *  - Without a mask (causal = 0, window = 0, n_valid = 0 or N) the result is
+ *    bit-identical to bsa_forward on K/V heads repeated H/H_kv times.
+ *
+ *  H_kv      1 .. H, dividing H.
+ *  causal    0 or 1.   n_valid 0 .. N.   window >= 0.   sinks >= 0.
+ */
+bsa_status bsa_forward_masked(const void* q, const void* k, const void* v, int32_t B, int32_t H,
+                              int32_t H_kv, int32_t N, int32_t D, const int32_t* kv_idx,
+                              const int32_t* kv_cnt, int32_t max_kv, const float* log_w,
+                              const int32_t* q_map, const int32_t* kv_map,
+                              const int32_t* row_perm, int32_t causal, int32_t n_valid,
+                              int32_t window, int32_t sinks, float scale, void* o, float* lse,
+                              void* stream);
+
+/*
  * bsa_gather_rows - token rows permuted into gathered order in HBM:
  *     dst[bh][p][:] = src[bh][map[bh][p]][:]    for p in 0..N-1.
  *

@@ -24,6 +24,7 @@ from .binding import (  # noqa: F401
     effective_flops,
     forward,
     forward_crm,
+    forward_masked,
     gather_rows,
     lib_path,
     load_library,

@@ -24,7 +24,7 @@ EXPORTS = ("bsa_build_index", "bsa_build_crm", "bsa_forward_crm", "bsa_upscale_t
            "bsa_block_scores", "bsa_block_scores_workspace_size",
            "bsa_reorder_rows", "bsa_spectral_order",
            "bsa_spectral_order_workspace_size", "bsa_spectral_order_noalloc", "bsa_sample_blocks",
-           "bsa_forward", "bsa_gather_rows",
+           "bsa_forward", "bsa_forward_masked", "bsa_gather_rows",
            "bsa_device_status", "bsa_resident_ctas", "bsa_status_string", "bsa_selftest_exp2",
            "bsa_selftest_wait_timeout")
 
@@ -74,6 +74,9 @@ def load_library():
     lib.bsa_spectral_order_noalloc.argtypes = [P, P, i32, i64, i32, i32, i32, P, P, P, P, P]
     lib.bsa_spectral_order_noalloc.restype = i32
     lib.bsa_forward.argtypes = [P, P, P, i32, i32, i32, i32, P, P, i32, P, P, P, P, f32, P, P, P]
+    lib.bsa_forward_masked.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, i32, P, P, P, P,
+                                       i32, i32, i32, i32, f32, P, P, P]
+    lib.bsa_forward_masked.restype = i32
     lib.bsa_device_status.argtypes = [P, ctypes.POINTER(i32)]
     lib.bsa_resident_ctas.argtypes = [i32]
     lib.bsa_status_string.argtypes = [i32]
@@ -306,6 +309,26 @@ def forward(q, k, v, kv_idx, kv_cnt, o, lse, *, log_w=None, q_map=None, kv_map=N
     _check("bsa_forward", code)
 
 
+def forward_masked(q, k, v, kv_idx, kv_cnt, o, lse, *, causal: bool = False, n_valid: int = 0,
+                   window: int = 0, sinks: int = 0, log_w=None, q_map=None, kv_map=None,
+                   row_perm=None, scale: float = 0.0, stream=None):
+    """bsa_forward with grouped K/V heads (k, v [B, H_kv, N, D]) and a token mask (see bsa.h)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _dtype(t, n, torch.bfloat16)
+    _dtype(lse, "lse", torch.float32)
+    _dtype(log_w, "log_w", torch.float32)
+    B, H, N, D = q.shape
+    H_kv = k.shape[1]
+    if k.shape != (B, H_kv, N, D) or v.shape != k.shape or o.shape != q.shape:
+        raise ValueError("q, o [B, H, N, D]; k, v [B, H_kv, N, D]")
+    code = load_library().bsa_forward_masked(
+        _ptr(q), _ptr(k), _ptr(v), B, H, H_kv, N, D, _ptr(kv_idx), _ptr(kv_cnt), kv_idx.shape[1],
+        _ptr(log_w), _ptr(q_map), _ptr(kv_map), _ptr(row_perm), int(bool(causal)), int(n_valid),
+        int(window), int(sinks), float(scale), _ptr(o), _ptr(lse), _stream(stream))
+    _check("bsa_forward_masked", code)
+
+
 def device_status(stream=None) -> int:
     """Read and clear the device status word (synchronises the stream)."""
     out = ctypes.c_int32(0)
@@ -352,7 +375,7 @@ __all__ = ["BLOCK", "BsaError", "IDX_MASK_U8", "IDX_THRESHOLD_F32", "IDX_TOPK_F3
            "reorder_rows", "sample_blocks", "forward", "device_status", "resident_ctas",
            "effective_flops", "dense_attention_flops", "load_library", "lib_path", "EXPORTS",
            "block_scores", "SCORE_MEAN_DOT", "SCORE_CENTROID_EXP", "build_crm", "forward_crm",
-           "upscale_threshold", "gather_rows",
+           "upscale_threshold", "gather_rows", "forward_masked",
            "spectral_order", "spectral_order_workspace_size", "spectral_order_noalloc",
            "NOALLOC_SCRATCH_BYTES", "reorder_guard",
            "selftest_exp2", "selftest_wait_timeout", "math"]

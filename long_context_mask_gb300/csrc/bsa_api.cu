@@ -178,12 +178,17 @@ bsa_status bsa_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
     return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
-bsa_status bsa_forward(const void* q, const void* k, const void* v, int32_t B, int32_t H, int32_t N,
-                       int32_t D, const int32_t* kv_idx, const int32_t* kv_cnt, int32_t max_kv,
-                       const float* log_w, const int32_t* q_map, const int32_t* kv_map,
-                       const int32_t* row_perm, float scale, void* o, float* lse, void* stream) {
+namespace {
+
+// Host validation shared by bsa_forward and bsa_forward_masked.
+bsa_status check_forward(const void* q, const void* k, const void* v, int32_t B, int32_t H,
+                         int32_t H_kv, int32_t N, int32_t D, const int32_t* kv_idx,
+                         const int32_t* kv_cnt, int32_t max_kv, const float* log_w,
+                         const int32_t* q_map, const int32_t* kv_map, const int32_t* row_perm,
+                         const void* o, const float* lse) {
     if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
     if (B < 1 || H < 1 || N < 128 || (N % 128) != 0 || N > (1 << 24)) return BSA_ERR_INVALID_ARG;
+    if (H_kv < 1 || H_kv > H || H % H_kv != 0) return BSA_ERR_INVALID_ARG;
     const int64_t total_rows = (int64_t)B * H * N;
     if (total_rows >= ((int64_t)1 << 31) || (int64_t)B * H > 65535) return BSA_ERR_INVALID_ARG;
     const int32_t nKB = N / 128;
@@ -196,10 +201,47 @@ bsa_status bsa_forward(const void* q, const void* k, const void* v, int32_t B, i
         return BSA_ERR_INVALID_ARG;
     if ((q_map && !aligned(q_map, 16)) || (kv_map && !aligned(kv_map, 16)))
         return BSA_ERR_INVALID_ARG;
+    return BSA_OK;
+}
+
+}  // namespace
+
+bsa_status bsa_forward(const void* q, const void* k, const void* v, int32_t B, int32_t H, int32_t N,
+                       int32_t D, const int32_t* kv_idx, const int32_t* kv_cnt, int32_t max_kv,
+                       const float* log_w, const int32_t* q_map, const int32_t* kv_map,
+                       const int32_t* row_perm, float scale, void* o, float* lse, void* stream) {
+    const bsa_status c = check_forward(q, k, v, B, H, H, N, D, kv_idx, kv_cnt, max_kv, log_w, q_map,
+                                       kv_map, row_perm, o, lse);
+    if (c != BSA_OK) return c;
     int32_t* status = bsa::status_word_ptr();
     if (!status) return BSA_ERR_CUDA;
     bsa::ForwardArgs a{q,      k,      v,     B,     H,      N,        D,     kv_idx, kv_cnt,
                        max_kv, log_w, q_map, kv_map, row_perm, scale, o,     lse,    nullptr, 0};
+    return bsa::launch_forward(a, status, static_cast<cudaStream_t>(stream));
+}
+
+bsa_status bsa_forward_masked(const void* q, const void* k, const void* v, int32_t B, int32_t H,
+                              int32_t H_kv, int32_t N, int32_t D, const int32_t* kv_idx,
+                              const int32_t* kv_cnt, int32_t max_kv, const float* log_w,
+                              const int32_t* q_map, const int32_t* kv_map,
+                              const int32_t* row_perm, int32_t causal, int32_t n_valid,
+                              int32_t window, int32_t sinks, float scale, void* o, float* lse,
+                              void* stream) {
+    const bsa_status c = check_forward(q, k, v, B, H, H_kv, N, D, kv_idx, kv_cnt, max_kv, log_w,
+                                       q_map, kv_map, row_perm, o, lse);
+    if (c != BSA_OK) return c;
+    if ((causal != 0 && causal != 1) || n_valid < 0 || n_valid > N || window < 0 || sinks < 0)
+        return BSA_ERR_INVALID_ARG;
+    int32_t* status = bsa::status_word_ptr();
+    if (!status) return BSA_ERR_CUDA;
+    bsa::ForwardArgs a{q,      k,      v,     B,     H,      N,        D,     kv_idx, kv_cnt,
+                       max_kv, log_w, q_map, kv_map, row_perm, scale, o,     lse,    nullptr, 0};
+    a.H_kv = H_kv;
+    a.masked = causal != 0 || window > 0 || (n_valid > 0 && n_valid < N);
+    a.causal = causal;
+    a.n_valid = n_valid;
+    a.window = window;
+    a.sinks = sinks;
     return bsa::launch_forward(a, status, static_cast<cudaStream_t>(stream));
 }
 

@@ -135,6 +135,8 @@ struct Params {
     float* lse;
     int32_t* status;
     int32_t N, nQB, max_kv;
+    int32_t H, group;  // query heads per batch entry; query heads per key/value head
+    int32_t causal, n_valid, window, sinks;  // token mask (the kMask variant only)
     float scale_log2;
 };
 
@@ -234,8 +236,9 @@ struct CrmIter {
     }
 };
 
-template <int D, int kPoly, bool kCrm, bool kGather>
+template <int D, int kPoly, bool kCrm, bool kGather, bool kMask>
 __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const __grid_constant__ Params P) {
+    static_assert(!(kCrm && kMask), "the token mask reads block indices from the lists");
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -246,6 +249,8 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t bh = blockIdx.y;
+    // key/value head of this query head: b * H_kv + h / group (grouped heads)
+    const int64_t bh_kv = (bh / P.H) * (P.H / P.group) + (bh % P.H) / P.group;
     const int32_t N = P.N, nQB = P.nQB, max_kv = P.max_kv;
     const int32_t nKB = nQB;
 
@@ -384,7 +389,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
             for (int i = 0; i < n_prod; ++i) kb_q[i] = i < n_tiles ? tile_kb(i) : 0;
             int32_t tok[4] = {0, 0, 0, 0}, tok_next[4] = {0, 0, 0, 0};
             // lane l reads the tokens of rows l, l + 32, l + 64, l + 96
-            const int32_t* map_head = P.kv_map + bh * N + lane;
+            const int32_t* map_head = P.kv_map + bh_kv * N + lane;
             if constexpr (kGather) {
                 if (g < n_tiles) {
                     int32_t kb_g = kb_q[0];  // kb_q[g] without a dynamic register index
@@ -430,13 +435,13 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
                             raise_status(P.status, BSA_ERR_BOUNDS);
                             tok[j] = 0;
                         }
-                    copy_tile<D>(dst, is_v ? P.v : P.k, bh, N, lane, tok);
+                    copy_tile<D>(dst, is_v ? P.v : P.k, bh_kv, N, lane, tok);
                     cp_async_arrive_noinc(fb);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) tok[j] = tok_next[j];
                 } else if (lane == 0) {  // tile load
                     mbar_arrive_expect_tx(fb, C::kTile);
-                    tma_load_3d(dst, is_v ? &P.map_v : &P.map_k, 0, (int32_t)(bh * N) + kb * 128, 0, fb);
+                    tma_load_3d(dst, is_v ? &P.map_v : &P.map_k, 0, (int32_t)(bh_kv * N) + kb * 128, 0, fb);
                 }
                 issued = t + 1;
             }
@@ -533,6 +538,53 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
             const float lw2 = lw_next * kLog2e;
             lw_next = (lw_row && j + 1 < n) ? lw_row[j + 1] : 0.0f;
             const uint32_t sbuf = (uint32_t)(j % kSBuf) * 128u;
+            // Token mask: the key tokens of block j (column c of the tile is key
+            // 128 kb + c, or kv_map of it), read before the wait for S_j.  A
+            // row needs per-element masking only if some key of the block may
+            // be dropped for it (a conservative test on the block's key range).
+            int32_t kt[4] = {0, 0, 0, 0};  // with kv_map: keys of columns lane + 32 m
+            int32_t kbase = 0;
+            bool need_mask = false;
+            uint32_t vis_w[4] = {~0u, ~0u, ~0u, ~0u};
+            if constexpr (kMask) {
+                int32_t kb = list[j];
+                kb = (kb < 0 || kb >= nKB) ? 0 : kb;  // flagged by the producer
+                int32_t kmin, kmax;
+                if (P.kv_map != nullptr) {
+                    const int32_t* km = P.kv_map + bh_kv * N + (int64_t)kb * 128 + lane;
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) kt[x] = km[32 * x];
+                    kmin = __reduce_min_sync(0xffffffffu, min(min(kt[0], kt[1]), min(kt[2], kt[3])));
+                    kmax = __reduce_max_sync(0xffffffffu, max(max(kt[0], kt[1]), max(kt[2], kt[3])));
+                } else {
+                    kbase = kb * 128;
+                    kmin = kbase;
+                    kmax = kbase + 127;
+                }
+                need_mask = kmax >= P.n_valid || (P.causal && kmax > tok) ||
+                            (P.window > 0 && kmin <= tok - P.window && kmax >= P.sinks);
+                // visibility of the 128 columns as four 32-bit words, built
+                // before S_j arrives so that only the words stay live
+                if (__any_sync(0xffffffffu, need_mask)) {
+                    const int32_t nv = P.n_valid, win = P.window, sk = P.sinks;
+                    const bool causal = P.causal != 0;
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        uint32_t word = 0u;
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            const int32_t jt = P.kv_map != nullptr ? __shfl_sync(0xffffffffu, kt[x], c)
+                                                                   : kbase + 32 * x + c;
+                            const bool vis = jt < nv && (!causal || jt <= tok) &&
+                                             (win <= 0 || jt > tok - win || jt < sk);
+                            word |= (uint32_t)vis << c;
+                        }
+                        vis_w[x] = word;
+                    }
+                } else {
+                    need_mask = false;
+                }
+            }
             const int32_t pk = ring_pos_k(j);
             bool w = mbar_wait(smem_u32(&bars->empty[pk % C::kStages]), (uint32_t)(pk / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
             if (__any_sync(0xffffffffu, !w || aborted(bars))) {
@@ -546,6 +598,13 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
             tmem_ld32(t_lane + sbuf + 64, &s[64]);
             tmem_ld32(t_lane + sbuf + 96, &s[96]);
             tmem_wait_ld();
+            if constexpr (kMask) {
+                if (__any_sync(0xffffffffu, need_mask)) {
+                    const uint32_t ninf = __float_as_uint(-INFINITY);
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) s[c] = ((vis_w[c >> 5] >> (c & 31)) & 1u) ? s[c] : ninf;
+                }
+            }
             float mx0 = __uint_as_float(s[0]), mx1 = __uint_as_float(s[1]);
             float mx2 = __uint_as_float(s[2]), mx3 = __uint_as_float(s[3]);
 #pragma unroll
@@ -563,11 +622,14 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
                 m = mt;
             } else if (rescale) {
                 const float m_new = fmaxf(m, mt);
-                alpha = ex2(m - m_new);
+                // a row with every key so far dropped has l = 0 and O = 0
+                alpha = (kMask && m == -INFINITY) ? 0.0f : ex2(m - m_new);
                 l *= alpha;
                 m = m_new;
             }
-            const float bias = lw2 - m;
+            // a row with every key so far dropped keeps m = -inf: its exponentials
+            // are all 0 (avoid -inf - -inf)
+            const float bias = lw2 - ((kMask && m == -INFINITY) ? 0.0f : m);
             float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
             for (int c = 0; c < 128; c += 4) {
@@ -630,7 +692,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
                     if (lane == 0) set_abort(bars, P.status);
                 } else {
                     tc_fence_after();
-                    const float inv_l = 1.0f / l;
+                    const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;  // l = 0: every key dropped
 #pragma unroll
                     for (int c = 0; c < D; c += 32) {
                         uint32_t o[32];
@@ -648,7 +710,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
                                 dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                         }
                     }
-                    if (tok_ok) P.lse[bh * N + tok] = (m + log2f(l)) * kLn2;
+                    if (tok_ok) P.lse[bh * N + tok] = l > 0.0f ? (m + log2f(l)) * kLn2 : -INFINITY;
                 }
             }
         }
@@ -695,7 +757,7 @@ size_t smem_bytes() {
     return 1024 + Cfg<D>::kData + sizeof(Barriers);
 }
 
-template <int D, int kPoly, bool kCrm, bool kGather>
+template <int D, int kPoly, bool kCrm, bool kGather, bool kMask>
 cudaError_t prepare_kernel() {
     // Per device: opt in to the large dynamic shared-memory carve-out.
     static int done[64] = {0};
@@ -703,7 +765,7 @@ cudaError_t prepare_kernel() {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(k_bsa_forward<D, kPoly, kCrm, kGather>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k_bsa_forward<D, kPoly, kCrm, kGather, kMask>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem_bytes<D>());
     if (e == cudaSuccess && dev < 64) done[dev] = 1;
     return e;
@@ -721,10 +783,10 @@ int poly_setting() {
     return v;
 }
 
-template <int D, int kPoly, bool kCrm, bool kGather>
+template <int D, int kPoly, bool kCrm, bool kGather, bool kMask = false>
 bsa_status launch_dp(const Params& P, unsigned grid_x, unsigned grid_y, cudaStream_t stream) {
-    if (prepare_kernel<D, kPoly, kCrm, kGather>() != cudaSuccess) return BSA_ERR_CUDA;
-    k_bsa_forward<D, kPoly, kCrm, kGather>
+    if (prepare_kernel<D, kPoly, kCrm, kGather, kMask>() != cudaSuccess) return BSA_ERR_CUDA;
+    k_bsa_forward<D, kPoly, kCrm, kGather, kMask>
         <<<dim3(grid_x, grid_y), threads_for(kGather), smem_bytes<D>(), stream>>>(P);
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
@@ -733,9 +795,10 @@ template <int D>
 bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) {
     Params P;
     memset(&P, 0, sizeof(P));
-    const uint64_t rows = (uint64_t)a.B * a.H * a.N;
-    bool ok = encode_tile_map(&P.map_q, a.q, rows, D) && encode_tile_map(&P.map_k, a.k, rows, D) &&
-              encode_tile_map(&P.map_v, a.v, rows, D);
+    const int32_t H_kv = a.H_kv > 0 ? a.H_kv : a.H;
+    const uint64_t rows = (uint64_t)a.B * a.H * a.N, kv_rows = (uint64_t)a.B * H_kv * a.N;
+    bool ok = encode_tile_map(&P.map_q, a.q, rows, D) && encode_tile_map(&P.map_k, a.k, kv_rows, D) &&
+              encode_tile_map(&P.map_v, a.v, kv_rows, D);
     if (!ok) return BSA_ERR_CUDA;
     P.q = static_cast<const __nv_bfloat16*>(a.q);
     P.k = static_cast<const __nv_bfloat16*>(a.k);
@@ -754,10 +817,21 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
     P.N = a.N;
     P.nQB = a.N / 128;
     P.max_kv = a.max_kv;
+    P.H = a.H;
+    P.group = a.H / H_kv;
+    P.causal = a.causal;
+    P.n_valid = a.n_valid > 0 ? a.n_valid : a.N;
+    P.window = a.window;
+    P.sinks = a.sinks;
     const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
     P.scale_log2 = scale * kLog2e;
     const unsigned gx = (unsigned)P.nQB, gy = (unsigned)(a.B * a.H);
     const bool crm = a.crm != nullptr, gather = a.kv_map != nullptr;
+    if (a.masked) {
+        if (crm) return BSA_ERR_UNSUPPORTED;
+        return gather ? launch_dp<D, kDefaultPoly, false, true, true>(P, gx, gy, stream)
+                      : launch_dp<D, kDefaultPoly, false, false, true>(P, gx, gy, stream);
+    }
     if (gather)
         return crm ? launch_dp<D, kDefaultPoly, true, true>(P, gx, gy, stream)
                    : launch_dp<D, kDefaultPoly, false, true>(P, gx, gy, stream);
@@ -770,8 +844,8 @@ template <int D>
 int32_t occupancy() {
     int per_sm = 0;
     // every instantiation holds one block per SM (shared memory bound)
-    if (prepare_kernel<D, kDefaultPoly, false, false>() != cudaSuccess) return -1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bsa_forward<D, kDefaultPoly, false, false>,
+    if (prepare_kernel<D, kDefaultPoly, false, false, false>() != cudaSuccess) return -1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bsa_forward<D, kDefaultPoly, false, false, false>,
                                                       threads_for(false),
                                                       smem_bytes<D>()) != cudaSuccess)
         return -1;

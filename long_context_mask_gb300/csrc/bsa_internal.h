@@ -70,6 +70,9 @@ struct ForwardArgs {
     float* lse;
     const uint32_t* crm;  // non-NULL: CRM rows instead of kv_idx / kv_cnt
     int32_t crm_words;
+    int32_t H_kv = 0;     // key/value heads per batch entry (0: H)
+    bool masked = false;  // token mask below applies
+    int32_t causal = 0, n_valid = 0, window = 0, sinks = 0;
 };
 // Returns BSA_OK, BSA_ERR_CUDA (launch / descriptor failure) or BSA_ERR_UNSUPPORTED.
 bsa_status launch_forward(const ForwardArgs& a, int32_t* status, cudaStream_t stream);

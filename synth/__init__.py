@@ -76,7 +76,13 @@ class Problem:
     u: np.ndarray | None = None             # fp64 [B*H*nQB], systematic-PPS draw
     diag_list: bool = False                 # one KV block per query block: kb = qb
     q_map: np.ndarray | None = None         # int32 [B*H, N]
-    kv_map: np.ndarray | None = None        # int32 [B*H, N]
+    kv_map: np.ndarray | None = None        # int32 [B*H_kv, N]
+    # grouped key/value heads (k, v are [B, H_kv, N, D]) and the token mask
+    H_kv: int | None = None                 # None: H
+    causal: bool = False
+    n_valid: int = 0                        # 0: N
+    window: int = 0
+    sinks: int = 0
     extra: dict = field(default_factory=dict)
 
     @property
@@ -204,7 +210,38 @@ def diag_lists(rows: int, nqb: int):
     return idx, np.ones(rows, np.int32)
 
 
-CONFIGS = {1: tiny, 2: threshold, 3: scatter, 4: sampled, 5: dynamic, 6: long_video}
+def llm(seed: int = 7, B: int = 1, H: int = 32, H_kv: int = 8, N: int = 16384, D: int = 128,
+        layer: str = "block", window: int = 575, sinks: int = 64) -> Problem:
+    """Language-model prefill shapes (32 query heads over 8 key/value heads,
+    causal).  layer "block": every second 256-token block (128-blocks kb
+    with floor(kb / 2) even) up to the query block, plus the query's own
+    block; layer "window": the blocks that hold some key of the sliding
+    window of `window` tokens or of the first `sinks` tokens."""
+    g = _gen(seed)
+    q = normal_bf16(g, (B, H, N, D))
+    k, v = (normal_bf16(g, (B, H_kv, N, D)) for _ in range(2))
+    nb = N // BLOCK
+    qb = np.arange(nb)[:, None]
+    kb = np.arange(nb)[None, :]
+    if layer == "block":
+        keep = (kb <= qb) & (((kb // 2) % 2 == 0) | (kb == qb))
+        w = s_ = 0
+    else:
+        # rows 128 qb .. 128 qb + 127 see keys (128 qb - window, 128 qb + 127]
+        lo = (BLOCK * qb - window + 1) // BLOCK
+        keep = ((kb >= lo) & (kb <= qb)) | (kb * BLOCK < sinks)
+        w, s_ = window, sinks
+    m = np.broadcast_to(keep.astype(np.uint8), (B * H, nb, nb)).reshape(B * H * nb, nb).copy()
+    return Problem(f"llm-{layer}", B, H, N, D, q, k, v, mask=m, H_kv=H_kv, causal=True,
+                   window=w, sinks=s_)
+
+
+def llm_window(seed: int = 8, **kw) -> Problem:
+    return llm(seed=seed, layer="window", **kw)
+
+
+CONFIGS = {1: tiny, 2: threshold, 3: scatter, 4: sampled, 5: dynamic, 6: long_video, 7: llm,
+           8: llm_window}
 CONFIG_NAMES = {
     1: "tiny B1 H2 N2048 D64, Bernoulli(0.25) block mask + diagonal",
     2: "threshold-map mask B1 H12 N32768 D128, T~U(0,1) + frame band, p=0.15",
@@ -212,4 +249,6 @@ CONFIG_NAMES = {
     4: "permuted exact top-16 + 8 PPS-sampled blocks B1 H40 N75776 D128",
     5: "dynamic top-k (10-20%) of mean-pooled scores, 8 shuffled clusters, B1 H24 N118784 D128",
     6: "dynamic top-k (10-20%), 8 shuffled clusters, long video B1 H2 N401408 D128",
+    7: "causal block-level layer (every second 256-token block) B1 H32 H_kv8 N16384 D128",
+    8: "causal sliding window 575 + 64 sinks B1 H32 H_kv8 N16384 D128",
 }

@@ -73,15 +73,26 @@ def run_forward(prob, idx, cnt, lw=None, row_perm=None, q=None, k=None, v=None):
     return o, lse
 
 
-def compare(prob, o, lse, idx, cnt, lw=None, sel=None):
+def few_key_o_bound(v):
+    """Max-abs O bound for rows that see only a few keys (token masks).
+
+    P is rounded to bf16 before PV (relative error <= 2^-8 per weight) and O
+    is rounded to bf16 (<= 2^-8 |O|), so |O_gpu - O| <= 2^-8 (|O| + max_j
+    |v_j - O|) <= 3 * 2^-8 * max|v|.  A row averaging hundreds of keys stays
+    far below it; a row that sees two keys can reach a sizeable part of it."""
+    return 3 * 2.0 ** -8 * float(torch.as_tensor(v).float().abs().max())
+
+
+def compare(prob, o, lse, idx, cnt, lw=None, sel=None, o_max_abs=O_MAX_ABS, **mask):
     """Check GPU O / LSE against the oracle on the query blocks `sel` (all when None).
+    ``mask`` (causal, n_valid, window, sinks) goes to the oracle unchanged.
 
     Returns (max-abs O, mean-rel O, max-abs LSE)."""
     idx_h = idx.cpu().numpy()
     cnt_h = cnt.cpu().numpy()
     lw_h = None if lw is None else lw.cpu().numpy()
     O, L, tok = oracle.attention(prob.q, prob.k, prob.v, idx_h, cnt_h, log_w=lw_h,
-                                 q_map=prob.q_map, kv_map=prob.kv_map, sel=sel)
+                                 q_map=prob.q_map, kv_map=prob.kv_map, sel=sel, **mask)
     nqb = prob.nqb
     sel_arr = np.arange(prob.rows) if sel is None else np.asarray(sel)
     bh = np.repeat(sel_arr // nqb, 128)
@@ -95,7 +106,7 @@ def compare(prob, o, lse, idx, cnt, lw=None, sel=None):
     fin = np.isfinite(L)
     assert np.array_equal(np.isneginf(lg), np.isneginf(L)), "-inf LSE rows differ"
     lse_abs = float(np.abs(lg[fin] - L[fin]).max()) if fin.any() else 0.0
-    assert max_abs <= O_MAX_ABS, f"O max-abs {max_abs}"
+    assert max_abs <= o_max_abs, f"O max-abs {max_abs} > {o_max_abs}"
     assert mean_rel <= O_MEAN_REL, f"O mean-rel {mean_rel}"
     assert lse_abs <= LSE_MAX_ABS, f"LSE max-abs {lse_abs}"
     return max_abs, mean_rel, lse_abs

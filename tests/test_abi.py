@@ -110,6 +110,24 @@ def test_gather_rows_host_validation(lib):
     assert g(None, None, 0, 256, 128, None, None) == 0          # empty: nothing to do
 
 
+def test_forward_masked_host_validation(lib):
+    f = lib.bsa_forward_masked
+
+    def call(H=4, H_kv=2, N=256, D=128, causal=1, n_valid=0, window=0, sinks=0, k=FAKE):
+        return f(FAKE, k, FAKE, 1, H, H_kv, N, D, FAKE, FAKE, 2, None, None, None, None,
+                 causal, n_valid, window, sinks, 0.0, FAKE, FAKE, None)
+    assert call(D=96) == 2
+    assert call(H_kv=3) == 1           # H not a multiple of H_kv
+    assert call(H_kv=0) == 1
+    assert call(H_kv=8) == 1           # more key/value heads than query heads
+    assert call(causal=2) == 1
+    assert call(n_valid=257) == 1      # beyond N
+    assert call(n_valid=-1) == 1
+    assert call(window=-5) == 1
+    assert call(sinks=-1) == 1
+    assert call(k=FAKE_ODD) == 1
+
+
 def test_device_status_rejects_null_output(lib):
     assert lib.bsa_device_status(None, None) == 1
 
