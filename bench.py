@@ -59,15 +59,20 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(config_id):
+def recorded_traffic(args):
     """DRAM bytes per forward launch from a committed ncu capture, if it was
-    taken on the current kernel source (else None)."""
+    taken on the current kernel source and on this exact workload (the default
+    options of that configuration), else None."""
     p = os.path.join(ROOT, "profiles", "forward_traffic.json")
     if not os.path.exists(p):
         return None
+    default_run = (args.heads is None and not args.dense and not args.crm and not args.scores_on_gpu
+                   and args.order == "reordered" and args.kv_gather == "auto")
+    if not default_run:
+        return None
     with open(p) as f:
         d = json.load(f)
-    e = d.get(f"config{config_id}")
+    e = d.get(f"config{args.config}")
     if not e or e.get("kernel_hash") != kernel_source_hash():
         return None
     return e.get("dram_bytes_per_launch")
@@ -554,7 +559,7 @@ def main():
     fwd_avg_ms = sum(fwd_ms) / len(fwd_ms)
     achieved = flops / (fwd_avg_ms * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    traffic = recorded_traffic(args.config)
+    traffic = recorded_traffic(args)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic, "kernel": "k_bsa_forward",
                 "peak_source": f"{peak_src} bf16 burst", "ms_per_launch": fwd_avg_ms,
