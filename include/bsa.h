@@ -215,8 +215,9 @@ bsa_status bsa_spectral_order_noalloc(const int32_t* kv_idx, const int32_t* kv_c
  * pi = 1 are promoted (kept, weight 1).  The other m - |promoted| blocks are
  * drawn by systematic PPS in ascending block order with the row's uniform
  * u: block j is drawn when a point u + i falls in [C_{j-1}, C_j), C the
- * running sum of pi.  lambda, pi and C are fp64, summed in ascending block
- * order without fused multiply-adds, so the drawn set is reproducible.
+ * running sum of pi.  lambda, pi and C are fp32 (u is rounded to fp32),
+ * summed in ascending block order with IEEE round-to-nearest and no fused
+ * multiply-adds, so the drawn set is reproducible.
  *
  *  scores       device fp32 [rows, nKB], every entry > 0; or NULL for the
  *               uniform sampler (InstaGen Algorithm 1 steps 6-8): every
@@ -230,7 +231,7 @@ bsa_status bsa_spectral_order_noalloc(const int32_t* kv_idx, const int32_t* kv_c
  *               blocks merged in ascending order (tail -1).
  *  kv_cnt       device int32 [rows] out.
  *  log_w        device fp32 [rows, max_kv] out: 0 for exact and promoted
- *               entries, -log(pi_j) for drawn ones (tail 0).
+ *               entries, -log(pi_j) (fp32 log) for drawn ones (tail 0).
  *  max_kv       capacity; a longer merged list is truncated and raises
  *               BSA_ERR_OVERFLOW.
  *  Outputs must not alias inputs.  nKB <= 4096.

@@ -207,99 +207,155 @@ __global__ void __launch_bounds__(256) k_reorder_rows(const int32_t* __restrict_
 constexpr int kMaxSampleKB = 4096;
 constexpr int kWords = kMaxSampleKB / 32;
 
-__device__ __forceinline__ bool bit_get(const uint32_t* w, int32_t i) {
-    return (w[i >> 5] >> (i & 31)) & 1u;
-}
-__device__ __forceinline__ void bit_set(uint32_t* w, int32_t i) { w[i >> 5] |= 1u << (i & 31); }
 
-__global__ void __launch_bounds__(128) k_sample_blocks(
+// One thread per row, 64 rows per block.  The scores are read in 32 x 32 tiles
+// per warp (coalesced) and each lane then walks its own row in ascending block
+// order: the sums must run in that order, one row per thread, to match the
+// oracle bit for bit.  The exact / promoted set of each row is a bitset in
+// shared memory (word w of thread t at w * 64 + t: conflict-free).
+constexpr int kSampleThreads = 64;
+
+__global__ void __launch_bounds__(kSampleThreads) k_sample_blocks(
     const float* __restrict__ scores, int64_t rows, int32_t nKB, const int32_t* __restrict__ exact_idx,
     const int32_t* __restrict__ exact_cnt, int32_t exact_stride, int32_t m,
     const double* __restrict__ u, int32_t* __restrict__ kv_idx, int32_t* __restrict__ kv_cnt,
     float* __restrict__ log_w, int32_t max_kv, int32_t* status) {
-    const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (row >= rows) return;
-    // NULL scores: the uniform sampler, every residual block scored 1
-    const float* s = scores ? scores + row * (int64_t)nKB : nullptr;
-    uint32_t taken[kWords], drawn[kWords];  // exact + promoted / drawn
+    __shared__ float tile[kSampleThreads / 32][32][33];
+    __shared__ uint32_t taken_s[kWords * kSampleThreads];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t row0 = (int64_t)blockIdx.x * kSampleThreads;
+    const int64_t row = row0 + tid;
+    const bool active = row < rows;
     const int32_t nw = (nKB + 31) >> 5;
-    for (int32_t w = 0; w < nw; ++w) taken[w] = drawn[w] = 0u;
-    const int32_t ec = exact_cnt[row];
-    for (int32_t e = 0; e < ec; ++e) {
-        const int32_t kb = exact_idx[row * (int64_t)exact_stride + e];
-        if (kb < 0 || kb >= nKB) {
-            raise_status(status, BSA_ERR_BOUNDS);
-            continue;
+    auto taken = [&](int32_t kb) -> bool { return (taken_s[(kb >> 5) * kSampleThreads + tid] >> (kb & 31)) & 1u; };
+    auto take = [&](int32_t kb) { taken_s[(kb >> 5) * kSampleThreads + tid] |= 1u << (kb & 31); };
+    for (int32_t w = 0; w < nw; ++w) taken_s[w * kSampleThreads + tid] = 0u;
+    int32_t n_res = nKB;
+    if (active) {
+        const int32_t ec = exact_cnt[row];
+        for (int32_t e = 0; e < ec; ++e) {
+            const int32_t kb = exact_idx[row * (int64_t)exact_stride + e];
+            if (kb < 0 || kb >= nKB) {
+                raise_status(status, BSA_ERR_BOUNDS);
+                continue;
+            }
+            if (!taken(kb)) {
+                take(kb);
+                --n_res;
+            }
         }
-        bit_set(taken, kb);
     }
-    int32_t n_res = 0;
-    for (int32_t w = 0; w < nw; ++w) n_res += __popc(taken[w]);
-    n_res = nKB - n_res;
+    // Columns c0 .. c0 + 31 of this warp's 32 rows into its tile (1 for the
+    // uniform sampler); lane l then reads its row from tile[warp][l][*].
+    // The next chunk's 32 loads are issued before the current chunk is
+    // processed (one chunk in flight in registers), so their latency overlaps
+    // the sequential per-row work.
+    float pre[32];
+    auto fetch = [&](int32_t c0) {
+        const int32_t c = c0 + lane;
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr) {
+            const int64_t rw = row0 + warp * 32 + rr;
+            pre[rr] = (scores != nullptr && rw < rows && c < nKB) ? __ldg(scores + rw * nKB + c) : 1.0f;
+        }
+    };
+    auto load_tile = [&](int32_t c0) {  // chunk c0 (already fetched) into the tile; fetch the next
+        __syncwarp();
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr) tile[warp][rr][lane] = pre[rr];
+        __syncwarp();
+        fetch(c0 + 32 < nKB ? c0 + 32 : 0);  // wraps to the start for the next pass
+    };
+    fetch(0);
 
     // fp32 throughout, IEEE round-to-nearest without contraction, sums in
     // ascending block order: these values decide which blocks are drawn
+    const bool all_promoted = n_res <= m;  // the budget covers the residual: pi = 1 everywhere
     float lambda = 0.0f;
-    if (n_res <= m) {
-        for (int32_t w = 0; w < nw; ++w) taken[w] = 0xffffffffu;  // all residual blocks promoted
-    } else {
-        // eq. (4): cap at 1 and renormalise until the capped set is stable
-        int32_t n_cap = 0;
-        for (;;) {
-            float sum = 0.0f, smax = 0.0f;
-            for (int32_t kb = 0; kb < nKB; ++kb) {
-                if (bit_get(taken, kb)) continue;
-                const float x = s ? s[kb] : 1.0f;
-                sum = __fadd_rn(sum, x);
-                smax = fmaxf(smax, x);
-            }
-            lambda = __fdiv_rn((float)(m - n_cap), sum);
-            // rounding is monotone: if the largest score stays below 1, all do
-            if (__fmul_rn(lambda, smax) < 1.0f) break;
-            bool grew = false;
-            for (int32_t kb = 0; kb < nKB; ++kb) {
-                if (!bit_get(taken, kb) && __fmul_rn(lambda, s ? s[kb] : 1.0f) >= 1.0f) {
-                    bit_set(taken, kb);
-                    ++n_cap;
-                    grew = true;
+    int32_t n_cap = 0;
+    bool iterate = active && !all_promoted;
+    // eq. (4): cap at 1 and renormalise until the capped set is stable
+    while (__any_sync(0xffffffffu, iterate)) {
+        float sum = 0.0f, smax = 0.0f;
+        for (int32_t c0 = 0; c0 < nKB; c0 += 32) {
+            load_tile(c0);
+            if (iterate) {
+                // skipped blocks add +0 (x + 0 = x exactly), past-the-end columns too
+                const uint32_t tw = taken_s[(c0 >> 5) * kSampleThreads + tid];
+                const int32_t cn = nKB - c0 < 32 ? nKB - c0 : 32;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const bool skip = c >= cn || ((tw >> c) & 1u);
+                    const float x = skip ? 0.0f : tile[warp][lane][c];
+                    sum = __fadd_rn(sum, x);
+                    smax = fmaxf(smax, x);
                 }
             }
-            if (!grew) break;
         }
-        // systematic PPS over the uncapped residual, ascending block order
-        const int32_t m_rest = m - n_cap;
-        const float ur = __double2float_rn(u[row]);
-        float C = 0.0f;
-        int32_t nd = 0;
-        for (int32_t kb = 0; kb < nKB && nd < m_rest; ++kb) {
-            if (bit_get(taken, kb)) continue;
-            const float C_prev = C;
-            C = __fadd_rn(C, __fmul_rn(lambda, s ? s[kb] : 1.0f));
-            if (ceilf(__fsub_rn(C, ur)) > ceilf(__fsub_rn(C_prev, ur))) {
-                bit_set(drawn, kb);
-                ++nd;
+        if (iterate) {
+            lambda = __fdiv_rn((float)(m - n_cap), sum);
+            // rounding is monotone: if the largest score stays below 1, all do
+            if (__fmul_rn(lambda, smax) < 1.0f) iterate = false;
+        }
+        if (!__any_sync(0xffffffffu, iterate)) break;
+        bool grew = false;
+        for (int32_t c0 = 0; c0 < nKB; c0 += 32) {
+            load_tile(c0);
+            if (iterate) {
+                const int32_t cn = nKB - c0 < 32 ? nKB - c0 : 32;
+                for (int32_t c = 0; c < cn; ++c) {
+                    if (!taken(c0 + c) && __fmul_rn(lambda, tile[warp][lane][c]) >= 1.0f) {
+                        take(c0 + c);
+                        ++n_cap;
+                        grew = true;
+                    }
+                }
             }
         }
+        if (!grew) iterate = false;
     }
-    int32_t n = 0, total = 0;
+
+    // Systematic PPS over the uncapped residual in ascending block order,
+    // merged with the exact and promoted blocks into the output list.
+    const int32_t m_rest = m - n_cap;
+    const float ur = active ? __double2float_rn(u[row]) : 0.0f;
+    float C = 0.0f;
+    int32_t nd = 0, n = 0, total = 0;
     int32_t* out = kv_idx + row * (int64_t)max_kv;
     float* lw = log_w + row * (int64_t)max_kv;
-    for (int32_t w = 0; w < nw; ++w) {
-        uint32_t bits = taken[w] | drawn[w];
-        if (32 * w + 32 > nKB) bits &= (nKB - 32 * w >= 32) ? 0xffffffffu : ((1u << (nKB - 32 * w)) - 1u);
-        while (bits) {
-            const int32_t kb = 32 * w + __ffs(bits) - 1;
-            bits &= bits - 1u;
-            if (n < max_kv) {
-                out[n] = kb;
-                // drawn: -log(pi) evaluated in double from the fp32 pi
-                lw[n] = bit_get(drawn, kb) ? (float)(-log((double)__fmul_rn(lambda, s ? s[kb] : 1.0f)))
-                                           : 0.0f;
-                ++n;
+    auto emit = [&](int32_t kb, float w) {
+        if (n < max_kv) {
+            out[n] = kb;
+            lw[n] = w;
+            ++n;
+        }
+        ++total;
+    };
+    for (int32_t c0 = 0; c0 < nKB; c0 += 32) {
+        load_tile(c0);
+        if (!active) continue;
+        const int32_t cn = nKB - c0 < 32 ? nKB - c0 : 32;
+        const uint32_t tw = all_promoted ? ~0u : taken_s[(c0 >> 5) * kSampleThreads + tid];
+#pragma unroll 8
+        for (int32_t c = 0; c < cn; ++c) {
+            const int32_t kb = c0 + c;
+            if ((tw >> c) & 1u) {
+                emit(kb, 0.0f);
+                continue;
             }
-            ++total;
+            if (nd < m_rest) {
+                const float pj = __fmul_rn(lambda, tile[warp][lane][c]);
+                const float C_prev = C;
+                C = __fadd_rn(C, pj);
+                if (ceilf(__fsub_rn(C, ur)) > ceilf(__fsub_rn(C_prev, ur))) {
+                    // drawn: log-weight -log(pi) (fp32 log; fp64 issue is slow here)
+                    emit(kb, -logf(pj));
+                    ++nd;
+                }
+            }
         }
     }
+    if (!active) return;
     for (int32_t e = n; e < max_kv; ++e) {
         out[e] = -1;
         lw[e] = 0.0f;
@@ -378,8 +434,8 @@ cudaError_t launch_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
                                  int32_t* kv_idx, int32_t* kv_cnt, float* log_w, int32_t max_kv,
                                  int32_t* status, cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
-    const dim3 grid((unsigned)((rows + 127) / 128));
-    k_sample_blocks<<<grid, 128, 0, stream>>>(scores, rows, nKB, exact_idx, exact_cnt, exact_stride,
+    const dim3 grid((unsigned)((rows + kSampleThreads - 1) / kSampleThreads));
+    k_sample_blocks<<<grid, kSampleThreads, 0, stream>>>(scores, rows, nKB, exact_idx, exact_cnt, exact_stride,
                                               m, u, kv_idx, kv_cnt, log_w, max_kv, status);
     return cudaGetLastError();
 }
