@@ -119,6 +119,9 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// kRegs > 0: the row (nKB <= 32 * kRegs) is read once into registers, lane l
+// holding blocks l, l + 32, ...; kRegs = 0: every pass re-reads it (through L1).
+template <int kRegs>
 __global__ void __launch_bounds__(256) k_index_topk(const float* __restrict__ scores, int64_t rows,
                                                     int32_t nKB, const int32_t* __restrict__ k_per_row,
                                                     int32_t k_const, int32_t* __restrict__ kv_idx,
@@ -131,6 +134,16 @@ __global__ void __launch_bounds__(256) k_index_topk(const float* __restrict__ sc
     int32_t* out = kv_idx + row * (int64_t)max_kv;
     int32_t k = k_per_row ? k_per_row[row] : k_const;
     k = k < 0 ? 0 : (k > nKB ? nKB : k);
+    // keys of blocks lane + 32 i; 0 past the end (0 is below every candidate,
+    // which has a bit set, and the selection checks the bound)
+    uint32_t key[kRegs > 0 ? kRegs : 1];
+    if constexpr (kRegs > 0) {
+#pragma unroll
+        for (int i = 0; i < kRegs; ++i) {
+            const int32_t kb = lane + 32 * i;
+            key[i] = kb < nKB ? order_key(s[kb]) : 0u;
+        }
+    }
 
     int32_t n = 0;
     if (k > 0) {
@@ -139,26 +152,43 @@ __global__ void __launch_bounds__(256) k_index_topk(const float* __restrict__ sc
         for (int bit = 31; bit >= 0; --bit) {
             const uint32_t cand = T | (1u << bit);
             int32_t c = 0;
-            for (int32_t kb = lane; kb < nKB; kb += 32) c += order_key(s[kb]) >= cand;
-            c = __reduce_add_sync(kFull, c);
-            if (c >= k) T = cand;
+            if constexpr (kRegs > 0) {
+#pragma unroll
+                for (int i = 0; i < kRegs; ++i) c += key[i] >= cand;
+            } else {
+                for (int32_t kb = lane; kb < nKB; kb += 32) c += order_key(s[kb]) >= cand;
+            }
+            if (__reduce_add_sync(kFull, c) >= k) T = cand;
         }
         int32_t gt = 0;
-        for (int32_t kb = lane; kb < nKB; kb += 32) gt += order_key(s[kb]) > T;
+        if constexpr (kRegs > 0) {
+#pragma unroll
+            for (int i = 0; i < kRegs; ++i) gt += key[i] > T;
+        } else {
+            for (int32_t kb = lane; kb < nKB; kb += 32) gt += order_key(s[kb]) > T;
+        }
         gt = __reduce_add_sync(kFull, gt);
         const int32_t need_eq = k - gt;  // >= 1: equal keys taken from the lowest block up
         int32_t eq_seen = 0;
-        for (int32_t c = 0; c < nKB; c += 32) {
+        // blocks c .. c + 31 (this lane: c + lane, key kk), selected in
+        // ascending block order; ties resolved by the ballot of equal keys
+        auto pick = [&](int32_t c, uint32_t kk) {
             const int32_t kb = c + lane;
-            const uint32_t key = kb < nKB ? order_key(s[kb]) : 0u;
-            const bool eq = kb < nKB && key == T;
+            const bool eq = kb < nKB && kk == T;
             const uint32_t eq_word = __ballot_sync(kFull, eq);
-            const bool sel = kb < nKB && (key > T || (eq && eq_seen + __popc(eq_word & lanemask_lt()) < need_eq));
+            const bool sel = kb < nKB && (kk > T || (eq && eq_seen + __popc(eq_word & lanemask_lt()) < need_eq));
             eq_seen += __popc(eq_word);
             const uint32_t word = __ballot_sync(kFull, sel);
             const int32_t pos = n + __popc(word & lanemask_lt());
             if (sel && pos < max_kv) out[pos] = kb;
             n += __popc(word);
+        };
+        if constexpr (kRegs > 0) {
+#pragma unroll
+            for (int i = 0; i < kRegs; ++i)
+                if (32 * i < nKB) pick(32 * i, key[i]);
+        } else {
+            for (int32_t c = 0; c < nKB; c += 32) pick(c, c + lane < nKB ? order_key(s[c + lane]) : 0u);
         }
     }
     const int32_t kept = n < max_kv ? n : max_kv;
@@ -407,8 +437,12 @@ cudaError_t launch_index_topk(const float* scores, int64_t rows, int32_t nKB,
     if (rows == 0) return cudaSuccess;
     const int warps = 8;
     const dim3 grid((unsigned)((rows + warps - 1) / warps));
-    k_index_topk<<<grid, warps * 32, 0, stream>>>(scores, rows, nKB, k_per_row, k_const, kv_idx,
-                                                  kv_cnt, max_kv, status);
+    if (nKB <= 32 * 32)
+        k_index_topk<32><<<grid, warps * 32, 0, stream>>>(scores, rows, nKB, k_per_row, k_const, kv_idx,
+                                                          kv_cnt, max_kv, status);
+    else
+        k_index_topk<0><<<grid, warps * 32, 0, stream>>>(scores, rows, nKB, k_per_row, k_const, kv_idx,
+                                                         kv_cnt, max_kv, status);
     return cudaGetLastError();
 }
 
