@@ -64,6 +64,10 @@ def _load():
         lib.oracle_block_scores.restype = None
         lib.oracle_spectral_order.argtypes = [P, P, i32, i64, i32, i32, i32, P, P, P, P]
         lib.oracle_spectral_order.restype = None
+        lib.oracle_gather0_set.argtypes = [i32, i32, i32, i32, i64, P, P, P]
+        lib.oracle_gather0_set.restype = i64
+        lib.oracle_attention_set.argtypes = [P, P, P, i32, i32, i64, i64, i64, P, i64, P, f64, P, P]
+        lib.oracle_attention_set.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i32
         _lib = lib
@@ -245,6 +249,74 @@ def attention(q, k, v, kv_idx, kv_cnt, log_w=None, q_map=None, kv_map=None, scal
                              int(bool(causal)), int(n_valid), int(window), int(sinks),
                              float(scale), _ptr(sel), n, _ptr(O), _ptr(L), _ptr(tok))
     return O, L, tok
+
+
+def gather0_sets(img_h, img_w, n_text, groups):
+    """Query and key token sets of the INTRA Gather 0 layer.
+
+    Returns a list of (q_tok, k_tok) int32 arrays: the img_h*img_w/64 image
+    CQS in the page's order (8 x 8 query patch; text keys, then the clamped
+    16 x 16 window), then, when n_text > 0, the text queries of each of the
+    ``groups`` Scatter groups (text keys, then the group's image tokens).
+    """
+    hw = img_h * img_w
+    n_sets = hw // 64 + (groups if n_text > 0 else 0)
+    per = n_text // groups if n_text > 0 else 0
+    qcap = max(64, per)
+    kcap = n_text + max(256, hw // groups if n_text > 0 else 0)
+    lib = _load()
+    out = []
+    for sidx in range(n_sets):
+        qt = np.empty(qcap, np.int32)
+        kt = np.empty(kcap, np.int32)
+        nq = np.zeros(1, np.int64)
+        nk = lib.oracle_gather0_set(img_h, img_w, n_text, groups, sidx, _ptr(qt), _ptr(nq), _ptr(kt))
+        if nk < 0:
+            raise ValueError("gather0_sets: set index out of range")
+        out.append((qt[: int(nq[0])].copy(), kt[:nk].copy()))
+    return out
+
+
+def attention_set(q, k, v, bh, q_tok, k_tok, scale=0.0):
+    """Softmax attention of query tokens q_tok of query head bh (flat b*H + h)
+    over key tokens k_tok, fp64.  q [B, H, N, D], k/v [B, H_kv, N, D] (bf16
+    bit patterns or CPU bf16 tensors).  Returns (O [nq, D], LSE [nq])."""
+    q, k, v = (_as_u16(t) for t in (q, k, v))
+    B, H, N, D = q.shape
+    H_kv = k.shape[1]
+    kvh = (bh // H) * H_kv + (bh % H) // (H // H_kv)
+    q_tok = _c(q_tok, np.int32)
+    k_tok = _c(k_tok, np.int32)
+    O = np.empty((q_tok.shape[0], D), np.float64)
+    L = np.empty(q_tok.shape[0], np.float64)
+    _load().oracle_attention_set(_ptr(q), _ptr(k), _ptr(v), N, D, int(bh), int(kvh),
+                                 q_tok.shape[0], _ptr(q_tok), k_tok.shape[0], _ptr(k_tok),
+                                 float(scale), _ptr(O), _ptr(L))
+    return O, L
+
+
+def gather0_attention(q, k, v, img_h, img_w, n_text, groups, scale=0.0, heads=None, sets=None):
+    """The INTRA Gather 0 layer from its definition, fp64.
+
+    q [B, H, N, D] with N = n_text + img_h*img_w; k, v [B, H_kv, N, D].
+    ``heads`` lists flat query heads (all when None) and ``sets`` indexes
+    gather0_sets (all when None).  Returns (O [len(heads), N, D], LSE
+    [len(heads), N]); rows of query tokens outside the chosen sets are NaN.
+    """
+    q_u = _as_u16(q)
+    B, H, N, D = q_u.shape
+    all_sets = gather0_sets(img_h, img_w, n_text, groups)
+    chosen = range(len(all_sets)) if sets is None else sets
+    heads = range(B * H) if heads is None else heads
+    O = np.full((len(heads), N, D), np.nan)
+    L = np.full((len(heads), N), np.nan)
+    for hi, bh in enumerate(heads):
+        for sidx in chosen:
+            qt, kt = all_sets[sidx]
+            o, lse = attention_set(q_u, k, v, bh, qt, kt, scale)
+            O[hi, qt] = o
+            L[hi, qt] = lse
+    return O, L
 
 
 def _as_u16(t):

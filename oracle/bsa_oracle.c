@@ -38,6 +38,14 @@
  *                          keys); INTRA, "CQS-Aware Token-Sparse
  *                          FlashAttention Kernel" (keys and queries reached
  *                          through index maps, outputs scattered back).
+ *   oracle_gather0_set     INTRA, appendix "Sparse Pattern Index Function",
+ *                          Gather 0 (8 x 8 query patch, 16 x 16 key window
+ *                          shifted inward at the edges, text tokens first)
+ *                          and "Mapping Back to INTRA" (text queries keep
+ *                          their Scatter image-key groups; Scatter groups
+ *                          same-position tokens, "Why Scatter Is Uniform").
+ *   oracle_attention_set   the softmax attention of one query set over one
+ *                          key set (InstaGen section 3.1 eqs. (1)-(3)).
  */
 #include <math.h>
 #include <stdint.h>
@@ -383,6 +391,103 @@ void oracle_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
         LSE[w] = lse;
         free(qi);
         free(key);
+        free(s);
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* INTRA Gather 0: the query set and key set of one CQS.                     */
+/*                                                                           */
+/* The sequence is n_text text tokens followed by an img_h x img_w image in  */
+/* zero-based row-major order: pixel (y, x) is token n_text + y*img_w + x.   */
+/* Sets 0 .. img_h*img_w/64 - 1 are the image CQS in the page's order: for   */
+/* CQS index i, r = i / (img_w/8) and c = i mod (img_w/8); its 64 queries   */
+/* are the 8 x 8 patch                                                       */
+/*     i_l^q -> pixel (8r + i_l^q / 8, 8c + i_l^q mod 8),   0 <= i_l^q < 64  */
+/* and its 256 image keys the 16 x 16 window with top-left corner            */
+/*     (r0, c0) = (clamp(8r - 4, 0, img_h - 16), clamp(8c - 4, 0, img_w - 16))*/
+/*     i_l^k -> pixel (r0 + i_l^k / 16, c0 + i_l^k mod 16), 0 <= i_l^k < 256 */
+/* (the page's four 64-key tiles i_l^k = 64t + j cover rows r0 + 4t ..      */
+/* r0 + 4t + 3, i.e. the same order), preceded by every text key.  The page  */
+/* prints neither equation; the window centred on the patch and clamped      */
+/* inside the image is the plain reading of "shifted inward at image         */
+/* boundaries" with every index in [0, HW).                                  */
+/* Sets img_h*img_w/64 + g (0 <= g < groups, only when n_text > 0) are the   */
+/* text queries of Scatter group g, i = g*(n_text/groups) .. +n_text/groups  */
+/* - 1, with every text key and the image tokens of Scatter group g: with   */
+/* image token index u = t*groups + g (neighbourhood t, local index g), the  */
+/* tokens n_text + t*groups + g for t = 0 .. img_h*img_w/groups - 1.        */
+/* Writes *nq query tokens to q_tok and returns the number of key tokens     */
+/* written to k_tok (-1 for a set index out of range).                       */
+/* ------------------------------------------------------------------------- */
+static int64_t clamp64(int64_t x, int64_t lo, int64_t hi) { return x < lo ? lo : (x > hi ? hi : x); }
+
+int64_t oracle_gather0_set(int32_t img_h, int32_t img_w, int32_t n_text, int32_t groups,
+                           int64_t set, int32_t* q_tok, int64_t* nq, int32_t* k_tok) {
+    const int64_t hw = (int64_t)img_h * img_w, n_img = hw / 64;
+    int64_t nk = 0;
+    if (set >= 0 && set < n_img) {
+        const int64_t r = set / (img_w / 8), c = set % (img_w / 8);
+        for (int64_t il = 0; il < 64; ++il)
+            q_tok[il] = (int32_t)(n_text + (8 * r + il / 8) * img_w + 8 * c + il % 8);
+        *nq = 64;
+        for (int64_t j = 0; j < n_text; ++j) k_tok[nk++] = (int32_t)j;
+        const int64_t r0 = clamp64(8 * r - 4, 0, img_h - 16), c0 = clamp64(8 * c - 4, 0, img_w - 16);
+        for (int64_t lk = 0; lk < 256; ++lk)
+            k_tok[nk++] = (int32_t)(n_text + (r0 + lk / 16) * img_w + c0 + lk % 16);
+        return nk;
+    }
+    const int64_t g = set - n_img;
+    if (n_text <= 0 || groups <= 0 || g < 0 || g >= groups) return -1;
+    const int64_t per = n_text / groups;
+    for (int64_t i = 0; i < per; ++i) q_tok[i] = (int32_t)(g * per + i);
+    *nq = per;
+    for (int64_t j = 0; j < n_text; ++j) k_tok[nk++] = (int32_t)j;
+    for (int64_t t = 0; t < hw / groups; ++t) k_tok[nk++] = (int32_t)(n_text + t * groups + g);
+    return nk;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Softmax attention of the query tokens q_tok[0..nq) of query head bh over  */
+/* the key tokens k_tok[0..nk) of key/value head kvh (tensors [heads, N, D]  */
+/* as bf16 bit patterns):                                                    */
+/*     s_j = (q_i . k_j) * scale,  LSE_i = ln sum_j exp(s_j),                */
+/*     O_i = sum_j exp(s_j - LSE_i) v_j.                                     */
+/* Row x of O [nq, D] and LSE [nq] belongs to query token q_tok[x].  nk = 0  */
+/* gives O = 0, LSE = -inf.  scale <= 0 selects 1/sqrt(D).                   */
+/* ------------------------------------------------------------------------- */
+void oracle_attention_set(const uint16_t* q, const uint16_t* k, const uint16_t* v, int32_t N,
+                          int32_t D, int64_t bh, int64_t kvh, int64_t nq, const int32_t* q_tok,
+                          int64_t nk, const int32_t* k_tok, double scale, double* O, double* LSE) {
+    if (scale <= 0.0) scale = 1.0 / sqrt((double)D);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t x = 0; x < nq; ++x) {
+        const int64_t i = q_tok[x];
+        double* o = O + x * D;
+        for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
+        if (nk <= 0) {
+            LSE[x] = -INFINITY;
+            continue;
+        }
+        double* s = (double*)malloc(sizeof(double) * (size_t)nk);
+        double mx = -INFINITY;
+        for (int64_t e = 0; e < nk; ++e) {
+            const int64_t j = k_tok[e];
+            double dot = 0.0;
+            for (int32_t d = 0; d < D; ++d)
+                dot += bf16_to_double(q[(bh * N + i) * D + d]) * bf16_to_double(k[(kvh * N + j) * D + d]);
+            s[e] = dot * scale;
+            mx = s[e] > mx ? s[e] : mx;
+        }
+        double z = 0.0;
+        for (int64_t e = 0; e < nk; ++e) z += exp(s[e] - mx);
+        const double lse = mx + log(z);
+        for (int64_t e = 0; e < nk; ++e) {
+            const double a = exp(s[e] - lse);
+            const uint16_t* vj = v + (kvh * N + k_tok[e]) * D;
+            for (int32_t d = 0; d < D; ++d) o[d] += a * bf16_to_double(vj[d]);
+        }
+        LSE[x] = lse;
         free(s);
     }
 }
