@@ -325,6 +325,94 @@ bsa_status bsa_forward_masked(const void* q, const void* k, const void* v, int32
                               void* stream);
 
 /*
+ * bsa_forward_packed - bsa_forward_masked over key/value tiles packed
+ * through a map that may repeat tokens, with per-quadrant visibility.
+ *
+ * Defined by: INTRA, "CQS-Aware Token-Sparse FlashAttention Kernel" (the
+ * kernel loads the selected key/value tokens through an index mapping and
+ * packs them into dense tiles; masking within the packed tiles) and
+ * appendix "Sparse Pattern Index Function", Gather 0 (overlapping 16 x 16
+ * key windows packed as key tiles).
+ *
+ * As bsa_forward_masked, except:
+ *  - kv_map is [B*H_kv, N_kv] (N_kv a multiple of 128, not tied to N): key
+ *    tile t of a key/value head holds tokens kv_map[.., 128 t .. 128 t + 127].
+ *    Tiles may overlap (a token may appear in several tiles).  List entries
+ *    name tiles 0 .. N_kv/128 - 1.  kv_map entries must lie in [0, N).
+ *  - quad_mask (optional, NULL = all set) is uint8 [B*H*nQB, max_kv]: bit g
+ *    of entry (row, j) set means query rows 32 g .. 32 g + 31 of the row's
+ *    query tile see listed tile j; with the bit clear every key of that tile
+ *    is dropped for those 32 rows (they skip its exponentials; the tile's
+ *    matrix products still run for the whole query tile).  Bits 4..7 are
+ *    ignored.  The token mask (causal, n_valid, window, sinks) applies on
+ *    top, to the original key tokens.
+ *  - Without quad_mask or token mask and with N_kv = N the result is
+ *    bit-identical to bsa_forward_masked.
+ *
+ *  kv_map    required, 16-byte aligned.
+ *  N_kv      128 .. 2^26, a multiple of 128; B*H_kv*N_kv < 2^40.
+ *  max_kv    1 .. N_kv/128.
+ */
+bsa_status bsa_forward_packed(const void* q, const void* k, const void* v, int32_t B, int32_t H,
+                              int32_t H_kv, int32_t N, int32_t D, const int32_t* kv_idx,
+                              const int32_t* kv_cnt, int32_t max_kv, const float* log_w,
+                              const int32_t* q_map, const int32_t* kv_map, int32_t N_kv,
+                              const uint8_t* quad_mask, const int32_t* row_perm, int32_t causal,
+                              int32_t n_valid, int32_t window, int32_t sinks, float scale, void* o,
+                              float* lse, void* stream);
+
+/*
+ * bsa_gather0_sizes / bsa_gather0_layout - the INTRA Gather 0 image layer as
+ * maps, lists and quadrant masks for bsa_forward_packed.
+ *
+ * Defined by: INTRA, appendix "Sparse Pattern Index Function", Gather 0,
+ * and "Mapping Back to INTRA" (FLUX.1-dev: 512 text tokens ahead of the
+ * image, Scatter with 8 groups).  The sequence is n_text text tokens
+ * followed by an img_h x img_w image in row-major order (token n_text +
+ * y*img_w + x).  Each 8 x 8 patch of image queries (patch row r, column c)
+ * attends to the 16 x 16 window of image keys with top-left corner
+ *     (clamp(8r - 4, 0, img_h - 16), clamp(8c - 4, 0, img_w - 16))
+ * (the window centred on the patch, shifted inward at the image edges) and
+ * to every text key.  Text query i belongs to Scatter group
+ * g = i / (n_text / groups) and attends to every text key and to the image
+ * tokens n_text + t*groups + g (t = 0 .. img_h*img_w/groups - 1).
+ *
+ * Layout (per head; heads identical copies):
+ *  - query tiles 0 .. n_text/128 - 1 are the text tokens in order; query
+ *    tile n_text/128 + s*(img_w/8) + c holds patch (2s, c) in rows 0..63 and
+ *    patch (2s+1, c) in rows 64..127, each patch row-major;
+ *  - key tiles 0 .. n_text/128 - 1 are the text tokens; then four tile
+ *    slots per query tile pair for its windows' 8-row x 16-column bands
+ *    (two per window; shared bands of the two windows stored once, so 2-4
+ *    slots used); then, when n_text > 0, the Scatter groups, 128 tokens per
+ *    tile in group order;
+ *  - each list holds the text tiles (seen by all rows) and then the row's
+ *    window bands or Scatter-group tiles in increasing tile order, with
+ *    quad_mask giving the 32-row quadrants that see each;
+ *  - unused list entries are 0 with quad_mask 0.
+ *
+ * bsa_gather0_sizes (host only) writes N = n_text + img_h*img_w, N_kv
+ * (= n_text + 4*img_h*img_w, plus img_h*img_w when n_text > 0) and the
+ * list capacity max_kv the layout needs.  bsa_gather0_layout writes the
+ * device arrays q_map [heads, N], kv_map [heads, N_kv], kv_idx
+ * [heads*N/128, max_kv], kv_cnt [heads*N/128], quad_mask [heads*N/128,
+ * max_kv] (int32 arrays 16-byte aligned).  For grouped heads pass the first
+ * B*H_kv copies of kv_map.
+ *
+ *  img_h     16 .. 4096, a multiple of 16 (two patch rows per query tile).
+ *  img_w     16 .. 4096, a multiple of 8.
+ *  n_text    0 .. 2^20, a multiple of 128.
+ *  groups    with n_text > 0: n_text/groups a multiple of 32 and
+ *            img_h*img_w/groups a multiple of 128; ignored when n_text = 0.
+ *  heads     0 .. 65535 (0: nothing to do); max_kv >= the size returned.
+ */
+bsa_status bsa_gather0_sizes(int32_t img_h, int32_t img_w, int32_t n_text, int32_t groups,
+                             int32_t* N, int32_t* N_kv, int32_t* max_kv);
+bsa_status bsa_gather0_layout(int32_t img_h, int32_t img_w, int32_t n_text, int32_t groups,
+                              int64_t heads, int32_t* q_map, int32_t* kv_map, int32_t* kv_idx,
+                              int32_t* kv_cnt, uint8_t* quad_mask, int32_t max_kv, void* stream);
+
+/*
  * bsa_gather_rows - token rows permuted into gathered order in HBM:
  *     dst[bh][p][:] = src[bh][map[bh][p]][:]    for p in 0..N-1.
  *

@@ -25,6 +25,9 @@ from .binding import (  # noqa: F401
     forward,
     forward_crm,
     forward_masked,
+    forward_packed,
+    gather0_layout,
+    gather0_sizes,
     gather_rows,
     lib_path,
     load_library,

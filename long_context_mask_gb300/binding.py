@@ -24,7 +24,8 @@ EXPORTS = ("bsa_build_index", "bsa_build_crm", "bsa_forward_crm", "bsa_upscale_t
            "bsa_block_scores", "bsa_block_scores_workspace_size",
            "bsa_reorder_rows", "bsa_spectral_order",
            "bsa_spectral_order_workspace_size", "bsa_spectral_order_noalloc", "bsa_sample_blocks",
-           "bsa_forward", "bsa_forward_masked", "bsa_gather_rows",
+           "bsa_forward", "bsa_forward_masked", "bsa_forward_packed", "bsa_gather_rows",
+           "bsa_gather0_sizes", "bsa_gather0_layout",
            "bsa_device_status", "bsa_resident_ctas", "bsa_status_string", "bsa_selftest_exp2",
            "bsa_selftest_wait_timeout")
 
@@ -77,6 +78,14 @@ def load_library():
     lib.bsa_forward_masked.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, i32, P, P, P, P,
                                        i32, i32, i32, i32, f32, P, P, P]
     lib.bsa_forward_masked.restype = i32
+    lib.bsa_forward_packed.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, i32, P, P, P, i32, P,
+                                       P, i32, i32, i32, i32, f32, P, P, P]
+    lib.bsa_forward_packed.restype = i32
+    lib.bsa_gather0_sizes.argtypes = [i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                      ctypes.POINTER(i32)]
+    lib.bsa_gather0_sizes.restype = i32
+    lib.bsa_gather0_layout.argtypes = [i32, i32, i32, i32, i64, P, P, P, P, P, i32, P]
+    lib.bsa_gather0_layout.restype = i32
     lib.bsa_device_status.argtypes = [P, ctypes.POINTER(i32)]
     lib.bsa_resident_ctas.argtypes = [i32]
     lib.bsa_status_string.argtypes = [i32]
@@ -329,6 +338,62 @@ def forward_masked(q, k, v, kv_idx, kv_cnt, o, lse, *, causal: bool = False, n_v
     _check("bsa_forward_masked", code)
 
 
+def forward_packed(q, k, v, kv_idx, kv_cnt, kv_map, o, lse, *, quad_mask=None, causal: bool = False,
+                   n_valid: int = 0, window: int = 0, sinks: int = 0, log_w=None, q_map=None,
+                   row_perm=None, scale: float = 0.0, stream=None):
+    """bsa_forward_masked over key tiles packed through kv_map [B*H_kv, N_kv]
+    (tokens may repeat across tiles) with optional quad_mask uint8
+    [B*H*nQB, max_kv] (see bsa.h)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _dtype(t, n, torch.bfloat16)
+    _dtype(lse, "lse", torch.float32)
+    _dtype(log_w, "log_w", torch.float32)
+    _dtype(quad_mask, "quad_mask", torch.uint8)
+    B, H, N, D = q.shape
+    H_kv = k.shape[1]
+    if k.shape != (B, H_kv, N, D) or v.shape != k.shape or o.shape != q.shape:
+        raise ValueError("q, o [B, H, N, D]; k, v [B, H_kv, N, D]")
+    if kv_map is None:
+        raise ValueError("forward_packed needs kv_map")
+    N_kv = kv_map.shape[-1]
+    if quad_mask is not None and tuple(quad_mask.shape) != tuple(kv_idx.shape):
+        raise ValueError("quad_mask must have kv_idx's shape")
+    code = load_library().bsa_forward_packed(
+        _ptr(q), _ptr(k), _ptr(v), B, H, H_kv, N, D, _ptr(kv_idx), _ptr(kv_cnt), kv_idx.shape[1],
+        _ptr(log_w), _ptr(q_map), _ptr(kv_map), int(N_kv), _ptr(quad_mask), _ptr(row_perm),
+        int(bool(causal)), int(n_valid), int(window), int(sinks), float(scale), _ptr(o), _ptr(lse),
+        _stream(stream))
+    _check("bsa_forward_packed", code)
+
+
+def gather0_sizes(img_h: int, img_w: int, n_text: int = 0, groups: int = 1):
+    """(N, N_kv, max_kv) of the INTRA Gather 0 layout (host only)."""
+    N, N_kv, mk = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+    _check("bsa_gather0_sizes", load_library().bsa_gather0_sizes(
+        img_h, img_w, n_text, groups, ctypes.byref(N), ctypes.byref(N_kv), ctypes.byref(mk)))
+    return N.value, N_kv.value, mk.value
+
+
+def gather0_layout(img_h: int, img_w: int, n_text: int, groups: int, heads: int, *, device=None,
+                   stream=None):
+    """The INTRA Gather 0 layer's q_map [heads, N], kv_map [heads, N_kv],
+    kv_idx / quad_mask [heads*N/128, max_kv] and kv_cnt, built on the GPU."""
+    import torch
+    N, N_kv, max_kv = gather0_sizes(img_h, img_w, n_text, groups)
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    rows = heads * (N // BLOCK)
+    q_map = torch.empty((heads, N), dtype=torch.int32, device=dev)
+    kv_map = torch.empty((heads, N_kv), dtype=torch.int32, device=dev)
+    kv_idx = torch.empty((rows, max_kv), dtype=torch.int32, device=dev)
+    kv_cnt = torch.empty(rows, dtype=torch.int32, device=dev)
+    quad_mask = torch.empty((rows, max_kv), dtype=torch.uint8, device=dev)
+    _check("bsa_gather0_layout", load_library().bsa_gather0_layout(
+        img_h, img_w, n_text, groups, heads, _ptr(q_map), _ptr(kv_map), _ptr(kv_idx), _ptr(kv_cnt),
+        _ptr(quad_mask), max_kv, _stream(stream)))
+    return q_map, kv_map, kv_idx, kv_cnt, quad_mask
+
+
 def device_status(stream=None) -> int:
     """Read and clear the device status word (synchronises the stream)."""
     out = ctypes.c_int32(0)
@@ -375,7 +440,8 @@ __all__ = ["BLOCK", "BsaError", "IDX_MASK_U8", "IDX_THRESHOLD_F32", "IDX_TOPK_F3
            "reorder_rows", "sample_blocks", "forward", "device_status", "resident_ctas",
            "effective_flops", "dense_attention_flops", "load_library", "lib_path", "EXPORTS",
            "block_scores", "SCORE_MEAN_DOT", "SCORE_CENTROID_EXP", "build_crm", "forward_crm",
-           "upscale_threshold", "gather_rows", "forward_masked",
+           "upscale_threshold", "gather_rows", "forward_masked", "forward_packed", "gather0_sizes",
+           "gather0_layout",
            "spectral_order", "spectral_order_workspace_size", "spectral_order_noalloc",
            "NOALLOC_SCRATCH_BYTES", "reorder_guard",
            "selftest_exp2", "selftest_wait_timeout", "math"]

@@ -180,18 +180,19 @@ bsa_status bsa_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
 
 namespace {
 
-// Host validation shared by bsa_forward and bsa_forward_masked.
+// Host validation shared by bsa_forward, bsa_forward_masked and
+// bsa_forward_packed.  nKB: key/value tiles a list entry may name (0: N/128).
 bsa_status check_forward(const void* q, const void* k, const void* v, int32_t B, int32_t H,
                          int32_t H_kv, int32_t N, int32_t D, const int32_t* kv_idx,
                          const int32_t* kv_cnt, int32_t max_kv, const float* log_w,
                          const int32_t* q_map, const int32_t* kv_map, const int32_t* row_perm,
-                         const void* o, const float* lse) {
+                         const void* o, const float* lse, int32_t nKB = 0) {
     if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
     if (B < 1 || H < 1 || N < 128 || (N % 128) != 0 || N > (1 << 24)) return BSA_ERR_INVALID_ARG;
     if (H_kv < 1 || H_kv > H || H % H_kv != 0) return BSA_ERR_INVALID_ARG;
     const int64_t total_rows = (int64_t)B * H * N;
     if (total_rows >= ((int64_t)1 << 31) || (int64_t)B * H > 65535) return BSA_ERR_INVALID_ARG;
-    const int32_t nKB = N / 128;
+    if (nKB <= 0) nKB = N / 128;
     if (max_kv < 1 || max_kv > nKB) return BSA_ERR_INVALID_ARG;
     if (!q || !k || !v || !kv_idx || !kv_cnt || !o || !lse) return BSA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
@@ -243,6 +244,61 @@ bsa_status bsa_forward_masked(const void* q, const void* k, const void* v, int32
     a.window = window;
     a.sinks = sinks;
     return bsa::launch_forward(a, status, static_cast<cudaStream_t>(stream));
+}
+
+bsa_status bsa_forward_packed(const void* q, const void* k, const void* v, int32_t B, int32_t H,
+                              int32_t H_kv, int32_t N, int32_t D, const int32_t* kv_idx,
+                              const int32_t* kv_cnt, int32_t max_kv, const float* log_w,
+                              const int32_t* q_map, const int32_t* kv_map, int32_t N_kv,
+                              const uint8_t* quad_mask, const int32_t* row_perm, int32_t causal,
+                              int32_t n_valid, int32_t window, int32_t sinks, float scale, void* o,
+                              float* lse, void* stream) {
+    if (kv_map == nullptr || N_kv < 128 || (N_kv % 128) != 0 || N_kv > (1 << 26))
+        return BSA_ERR_INVALID_ARG;
+    if (B >= 1 && H_kv >= 1 && (int64_t)B * H_kv * N_kv >= ((int64_t)1 << 40)) return BSA_ERR_INVALID_ARG;
+    const bsa_status c = check_forward(q, k, v, B, H, H_kv, N, D, kv_idx, kv_cnt, max_kv, log_w,
+                                       q_map, kv_map, row_perm, o, lse, N_kv / 128);
+    if (c != BSA_OK) return c;
+    if ((causal != 0 && causal != 1) || n_valid < 0 || n_valid > N || window < 0 || sinks < 0)
+        return BSA_ERR_INVALID_ARG;
+    int32_t* status = bsa::status_word_ptr();
+    if (!status) return BSA_ERR_CUDA;
+    bsa::ForwardArgs a{q,      k,      v,     B,     H,      N,        D,     kv_idx, kv_cnt,
+                       max_kv, log_w, q_map, kv_map, row_perm, scale, o,     lse,    nullptr, 0};
+    a.H_kv = H_kv;
+    a.masked = quad_mask != nullptr || causal != 0 || window > 0 || (n_valid > 0 && n_valid < N);
+    a.causal = causal;
+    a.n_valid = n_valid;
+    a.window = window;
+    a.sinks = sinks;
+    a.n_kv = N_kv;
+    a.quad_mask = quad_mask;
+    return bsa::launch_forward(a, status, static_cast<cudaStream_t>(stream));
+}
+
+bsa_status bsa_gather0_sizes(int32_t img_h, int32_t img_w, int32_t n_text, int32_t groups,
+                             int32_t* N, int32_t* N_kv, int32_t* max_kv) {
+    bsa::Gather0Geom g;
+    if (!bsa::gather0_geometry(img_h, img_w, n_text, groups, &g)) return BSA_ERR_INVALID_ARG;
+    if (N) *N = g.N;
+    if (N_kv) *N_kv = g.N_kv;
+    if (max_kv) *max_kv = g.max_kv;
+    return BSA_OK;
+}
+
+bsa_status bsa_gather0_layout(int32_t img_h, int32_t img_w, int32_t n_text, int32_t groups,
+                              int64_t heads, int32_t* q_map, int32_t* kv_map, int32_t* kv_idx,
+                              int32_t* kv_cnt, uint8_t* quad_mask, int32_t max_kv, void* stream) {
+    bsa::Gather0Geom g;
+    if (!bsa::gather0_geometry(img_h, img_w, n_text, groups, &g)) return BSA_ERR_INVALID_ARG;
+    if (heads < 0 || heads > 65535 || max_kv < g.max_kv || max_kv > (1 << 20)) return BSA_ERR_INVALID_ARG;
+    if (heads == 0) return BSA_OK;
+    if (!q_map || !kv_map || !kv_idx || !kv_cnt || !quad_mask) return BSA_ERR_INVALID_ARG;
+    if (!aligned(q_map, 16) || !aligned(kv_map, 16) || !aligned(kv_idx, 16) || !aligned(kv_cnt, 16))
+        return BSA_ERR_INVALID_ARG;
+    cudaError_t e = bsa::launch_gather0_layout(g, heads, q_map, kv_map, kv_idx, kv_cnt, quad_mask, max_kv,
+                                               static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
 bsa_status bsa_forward_crm(const void* q, const void* k, const void* v, int32_t B, int32_t H,

@@ -128,6 +128,7 @@ struct Params {
     const float* log_w;
     const int32_t* q_map;
     const int32_t* kv_map;
+    const uint8_t* quad_mask;  // [rows, max_kv] quadrant visibility (the kMask variant only)
     const int32_t* row_perm;
     const uint32_t* crm;  // CRM rows [rows, crm_words] (the CRM variant only)
     int32_t crm_words;
@@ -135,6 +136,7 @@ struct Params {
     float* lse;
     int32_t* status;
     int32_t N, nQB, max_kv;
+    int32_t n_kv;      // kv_map entries per key/value head (a multiple of 128)
     int32_t H, group;  // query heads per batch entry; query heads per key/value head
     int32_t causal, n_valid, window, sinks;  // token mask (the kMask variant only)
     float scale_log2;
@@ -252,7 +254,8 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
     // key/value head of this query head: b * H_kv + h / group (grouped heads)
     const int64_t bh_kv = (bh / P.H) * (P.H / P.group) + (bh % P.H) / P.group;
     const int32_t N = P.N, nQB = P.nQB, max_kv = P.max_kv;
-    const int32_t nKB = nQB;
+    // key/value tiles: blocks of the sequence, or 128-entry groups of kv_map
+    const int32_t nKB = P.kv_map != nullptr ? P.n_kv / 128 : nQB;
 
     // A block of this launch (or an unread earlier one) timed out: abandon.
     if (*reinterpret_cast<const volatile int32_t*>(P.status) == BSA_ERR_TIMEOUT) return;
@@ -389,7 +392,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
             for (int i = 0; i < n_prod; ++i) kb_q[i] = i < n_tiles ? tile_kb(i) : 0;
             int32_t tok[4] = {0, 0, 0, 0}, tok_next[4] = {0, 0, 0, 0};
             // lane l reads the tokens of rows l, l + 32, l + 64, l + 96
-            const int32_t* map_head = P.kv_map + bh_kv * N + lane;
+            const int32_t* map_head = P.kv_map + bh_kv * P.n_kv + lane;
             if constexpr (kGather) {
                 if (g < n_tiles) {
                     int32_t kb_g = kb_q[0];  // kb_q[g] without a dynamic register index
@@ -531,6 +534,9 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
         }
         const float sl2 = P.scale_log2;
         const float* lw_row = P.log_w ? P.log_w + row * max_kv : nullptr;
+        // quadrant visibility of the listed blocks: bit qd of entry j says
+        // whether this warp's 32 rows see block j at all
+        const uint8_t* qm_row = (kMask && P.quad_mask != nullptr) ? P.quad_mask + row * max_kv : nullptr;
         float m = -INFINITY, l = 0.0f;
         bool ok = true;
         float lw_next = (lw_row && n > 0) ? lw_row[0] : 0.0f;
@@ -546,12 +552,14 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
             int32_t kbase = 0;
             bool need_mask = false;
             uint32_t vis_w[4] = {~0u, ~0u, ~0u, ~0u};
-            if constexpr (kMask) {
+            bool hidden = false;  // warp-uniform: no row of this warp sees block j
+            if constexpr (kMask) hidden = qm_row != nullptr && ((qm_row[j] >> qd) & 1u) == 0u;
+            if (kMask && !hidden) {
                 int32_t kb = list[j];
                 kb = (kb < 0 || kb >= nKB) ? 0 : kb;  // flagged by the producer
                 int32_t kmin, kmax;
                 if (P.kv_map != nullptr) {
-                    const int32_t* km = P.kv_map + bh_kv * N + (int64_t)kb * 128 + lane;
+                    const int32_t* km = P.kv_map + bh_kv * P.n_kv + (int64_t)kb * 128 + lane;
 #pragma unroll
                     for (int x = 0; x < 4; ++x) kt[x] = km[32 * x];
                     kmin = __reduce_min_sync(0xffffffffu, min(min(kt[0], kt[1]), min(kt[2], kt[3])));
@@ -592,6 +600,18 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
                 break;
             }
             tc_fence_after();
+            if (kMask && hidden) {
+                // P_j = 0 for these rows; m, l and O are unchanged
+                uint32_t z[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) z[c] = 0u;
+                tmem_st32(t_lane + sbuf + 0, z);
+                tmem_st32(t_lane + sbuf + 32, z);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars->p_full[j % kSBuf]));
+                continue;
+            }
             uint32_t s[128];
             tmem_ld32(t_lane + sbuf + 0, &s[0]);
             tmem_ld32(t_lane + sbuf + 32, &s[32]);
@@ -808,6 +828,7 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
     P.log_w = a.log_w;
     P.q_map = a.q_map;
     P.kv_map = a.kv_map;
+    P.quad_mask = a.quad_mask;
     P.row_perm = a.row_perm;
     P.crm = a.crm;
     P.crm_words = a.crm_words;
@@ -817,6 +838,7 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
     P.N = a.N;
     P.nQB = a.N / 128;
     P.max_kv = a.max_kv;
+    P.n_kv = a.n_kv > 0 ? a.n_kv : a.N;
     P.H = a.H;
     P.group = a.H / H_kv;
     P.causal = a.causal;

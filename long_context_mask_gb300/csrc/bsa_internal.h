@@ -27,6 +27,16 @@ cudaError_t launch_crm_rows(bsa_idx_mode mode, const void* src, int64_t rows, in
 // dst[bh][p] = src[bh][map[bh][p]] for bf16 rows of D elements (bsa_gather.cu).
 cudaError_t launch_gather_rows(const void* src, const int32_t* map, int64_t heads, int32_t N,
                                int32_t D, void* dst, int32_t* status, cudaStream_t stream);
+// The INTRA Gather 0 layer's sizes (host; false: arguments out of range) and
+// its maps, lists and quadrant masks (bsa_gather.cu).
+struct Gather0Geom {
+    int32_t img_h, img_w, n_text, groups;
+    int32_t N, N_kv, max_kv;
+};
+bool gather0_geometry(int32_t img_h, int32_t img_w, int32_t n_text, int32_t groups, Gather0Geom* out);
+cudaError_t launch_gather0_layout(const Gather0Geom& geo, int64_t heads, int32_t* q_map, int32_t* kv_map,
+                                  int32_t* kv_idx, int32_t* kv_cnt, uint8_t* quad_mask, int32_t max_kv,
+                                  cudaStream_t stream);
 cudaError_t launch_upscale_threshold(const float* T, int64_t heads, int32_t Ub, int32_t Vb,
                                      int32_t Ut, int32_t Vt, float* out, cudaStream_t stream);
 cudaError_t launch_reorder_rows(const int32_t* kv_cnt, const int32_t* order_in, int64_t heads,
@@ -73,6 +83,8 @@ struct ForwardArgs {
     int32_t H_kv = 0;     // key/value heads per batch entry (0: H)
     bool masked = false;  // token mask below applies
     int32_t causal = 0, n_valid = 0, window = 0, sinks = 0;
+    int32_t n_kv = 0;                     // kv_map entries per key/value head (0: N)
+    const uint8_t* quad_mask = nullptr;   // [rows, max_kv] 32-row quadrant visibility
 };
 // Returns BSA_OK, BSA_ERR_CUDA (launch / descriptor failure) or BSA_ERR_UNSUPPORTED.
 bsa_status launch_forward(const ForwardArgs& a, int32_t* status, cudaStream_t stream);

@@ -30,6 +30,11 @@ structure the pages describe):
                  per-row k ~ U{ceil(0.10 nB) .. floor(0.20 nB)}.
 * ``long_video`` the same at N401408 (401 latent frames), H2: one head's K/V
                  exceeds the L2 (WaveAlign's longest Wan2.1 workload).
+* ``llm``, ``llm_window``  LLaMA-3.1-8B prefill shapes (32 query heads over 8
+                 key/value heads, causal): every second 256-token block, or a
+                 575-token sliding window with 64 sinks (INTRA section 4.7).
+* ``image_gather0`` FLUX.1-dev image layer: H24 D128, 512 text tokens and a
+                 128 x 128 latent image (INTRA appendix, Gather 0).
 """
 from __future__ import annotations
 
@@ -83,6 +88,12 @@ class Problem:
     n_valid: int = 0                        # 0: N
     window: int = 0
     sinks: int = 0
+    # image layer (INTRA Gather 0): n_text text tokens, then an img_h x img_w
+    # image; the maps and lists come from the layout, not from here
+    img_h: int = 0
+    img_w: int = 0
+    n_text: int = 0
+    groups: int = 1
     extra: dict = field(default_factory=dict)
 
     @property
@@ -240,8 +251,20 @@ def llm_window(seed: int = 8, **kw) -> Problem:
     return llm(seed=seed, layer="window", **kw)
 
 
+def image_gather0(seed: int = 9, B: int = 1, H: int = 24, img_h: int = 128, img_w: int = 128,
+                  n_text: int = 512, groups: int = 8, D: int = 128) -> Problem:
+    """FLUX.1-dev image layer shape: 24 heads of 128, 512 text tokens ahead of
+    a 128 x 128 latent image (2048 x 2048 pixels), N(0,1) bf16 Q/K/V; the
+    Gather 0 pattern itself is built by the library's layout call."""
+    g = _gen(seed)
+    N = n_text + img_h * img_w
+    q, k, v = (normal_bf16(g, (B, H, N, D)) for _ in range(3))
+    return Problem("image-gather0", B, H, N, D, q, k, v, img_h=img_h, img_w=img_w, n_text=n_text,
+                   groups=groups)
+
+
 CONFIGS = {1: tiny, 2: threshold, 3: scatter, 4: sampled, 5: dynamic, 6: long_video, 7: llm,
-           8: llm_window}
+           8: llm_window, 9: image_gather0}
 CONFIG_NAMES = {
     1: "tiny B1 H2 N2048 D64, Bernoulli(0.25) block mask + diagonal",
     2: "threshold-map mask B1 H12 N32768 D128, T~U(0,1) + frame band, p=0.15",
@@ -251,4 +274,5 @@ CONFIG_NAMES = {
     6: "dynamic top-k (10-20%), 8 shuffled clusters, long video B1 H2 N401408 D128",
     7: "causal block-level layer (every second 256-token block) B1 H32 H_kv8 N16384 D128",
     8: "causal sliding window 575 + 64 sinks B1 H32 H_kv8 N16384 D128",
+    9: "INTRA Gather 0 image layer: 512 text + 128x128 image, 16x16 windows, B1 H24 N16896 D128",
 }

@@ -128,6 +128,53 @@ def test_forward_masked_host_validation(lib):
     assert call(k=FAKE_ODD) == 1
 
 
+def test_forward_packed_host_validation(lib):
+    f = lib.bsa_forward_packed
+
+    def call(N=256, N_kv=1024, max_kv=2, kv_map=FAKE, causal=0, H_kv=2):
+        return f(FAKE, FAKE, FAKE, 1, 4, H_kv, N, 128, FAKE, FAKE, max_kv, None, None, kv_map, N_kv,
+                 FAKE, None, causal, 0, 0, 0, 0.0, FAKE, FAKE, None)
+    assert call(kv_map=None) == 1      # the packed tiles need a map
+    assert call(N_kv=0) == 1
+    assert call(N_kv=1000) == 1        # not a multiple of 128
+    assert call(N_kv=1 << 27) == 1     # beyond 2^26
+    assert call(max_kv=9) == 1         # more entries than packed tiles (8)
+    assert call(H_kv=3) == 1
+    assert call(causal=2) == 1
+    assert call(kv_map=FAKE_ODD) == 1  # kv_map not 16-byte aligned
+
+
+def test_gather0_sizes_and_layout_validation(lib):
+    i32 = ctypes.c_int32
+    N, N_kv, mk = i32(0), i32(0), i32(0)
+
+    def sizes(h, w, nt, g):
+        return lib.bsa_gather0_sizes(h, w, nt, g, ctypes.byref(N), ctypes.byref(N_kv), ctypes.byref(mk))
+    # FLUX.1-dev shapes (INTRA, "Sparse Pattern Index Function", Gather 0):
+    # 512 text tokens, 128 x 128 or 64 x 64 image, 8 Scatter groups
+    assert sizes(128, 128, 512, 8) == 0
+    assert (N.value, N_kv.value, mk.value) == (16896, 512 + 5 * 16384, 4 + 2 * 16)
+    assert sizes(64, 64, 512, 8) == 0
+    assert (N.value, N_kv.value, mk.value) == (4608, 512 + 5 * 4096, 4 + 2 * 4)
+    assert sizes(16, 24, 0, 1) == 0                     # one row of tile pairs: two bands each
+    assert (N.value, N_kv.value, mk.value) == (384, 4 * 384, 2)
+    assert sizes(48, 16, 256, 2) == 0                   # 128 text queries per group
+    assert (N.value, N_kv.value, mk.value) == (1024, 256 + 5 * 768, 2 + 4)  # edge pairs: 4 bands
+    assert sizes(24, 16, 0, 1) == 1                     # height not a multiple of 16
+    assert sizes(32, 12, 0, 1) == 1                     # width not a multiple of 8
+    assert sizes(8, 16, 0, 1) == 1                      # smaller than a window
+    assert sizes(32, 32, 100, 1) == 1                   # text not a multiple of 128
+    assert sizes(32, 32, 128, 8) == 1                   # 16 text queries per group
+    assert sizes(32, 32, 128, 3) == 1
+    assert sizes(16, 16, 128, 4) == 1                   # 64 image tokens per group
+    lay = lib.bsa_gather0_layout
+    assert lay(32, 32, 0, 1, 2, FAKE, FAKE, FAKE, FAKE, FAKE, 3, None) == 1      # max_kv < 4
+    assert lay(32, 32, 0, 1, 70000, FAKE, FAKE, FAKE, FAKE, FAKE, 4, None) == 1  # heads > 65535
+    assert lay(32, 32, 0, 1, 2, None, FAKE, FAKE, FAKE, FAKE, 4, None) == 1
+    assert lay(32, 32, 0, 1, 2, FAKE_ODD, FAKE, FAKE, FAKE, FAKE, 4, None) == 1
+    assert lay(32, 32, 0, 1, 0, None, None, None, None, None, 4, None) == 0      # nothing to do
+
+
 def test_device_status_rejects_null_output(lib):
     assert lib.bsa_device_status(None, None) == 1
 
