@@ -152,7 +152,15 @@ class Path:
         self.q_map, self.kv_map = cu(prob.q_map), cu(prob.kv_map)
         rows, nqb = prob.rows, prob.nqb
         self.heads = prob.B * prob.H
-        if prob.mask is not None:
+        self.image = is_image_layer(prob)
+        self.quad_mask = None
+        if self.image:
+            # the static Gather 0 pattern: maps, lists and quadrant masks built
+            # once on the GPU (the layer's fixed index functions)
+            self.q_map, self.kv_map, self.idx, self.cnt, self.quad_mask = bsa.gather0_layout(
+                prob.img_h, prob.img_w, prob.n_text, prob.groups, self.heads, device=dev)
+            self.mode, self.src, self.max_kv = None, None, self.idx.shape[1]
+        elif prob.mask is not None:
             self.mode, self.src, self.max_kv = bsa.IDX_MASK_U8, cu(prob.mask), nqb
         elif prob.T is not None:
             self.mode, self.src, self.max_kv = bsa.IDX_THRESHOLD_F32, cu(prob.T), nqb
@@ -168,9 +176,10 @@ class Path:
             self.score_ws = torch.empty(max(1, bsa.load_library().bsa_block_scores_workspace_size(
                 prob.B, prob.H, prob.N, prob.D)), dtype=torch.uint8, device=dev)
         self.u = cu(prob.u)
-        self.idx = torch.empty((rows, self.max_kv), dtype=torch.int32, device=dev)
-        self.cnt = torch.empty(rows, dtype=torch.int32, device=dev)
-        if self.mode is None:  # one KV block per query block (Scatter / Gather layers)
+        if not self.image:
+            self.idx = torch.empty((rows, self.max_kv), dtype=torch.int32, device=dev)
+            self.cnt = torch.empty(rows, dtype=torch.int32, device=dev)
+        if self.mode is None and not self.image:  # one KV block per query block (Scatter / Gather layers)
             self.idx.copy_(torch.arange(rows, device=dev, dtype=torch.int32).remainder(nqb)[:, None])
             self.cnt.fill_(1)
         self.lw = None
@@ -195,7 +204,9 @@ class Path:
         # gather rows inside the forward kernel when each block is used once
         # (the Scatter layer's one block per query block).
         if kv_gather == "auto":
-            kv_gather = "kernel" if prob.diag_list else "hbm"
+            kv_gather = "kernel" if (prob.diag_list or self.image) else "hbm"
+        if self.image:
+            kv_gather = "kernel"  # packed key tiles overlap: no N-row gathered copy exists
         self.pregather = self.kv_map is not None and kv_gather == "hbm" and not self.crm
         self.masked = uses_masked_forward(prob)
         if self.pregather:
@@ -230,7 +241,19 @@ class Path:
             _, cnt = self.lists()
             bsa.reorder_rows(cnt.reshape(self.heads, p.nqb), self.wave, self.row_perm)
 
+    def host_inputs(self):
+        """Tensors a step takes from the host (end-to-end leg); the image
+        layer's layout is static and stays on the device."""
+        ts = (self.q, self.k, self.v) if self.image else (
+            self.q, self.k, self.v, self.src, self.q_map, self.kv_map, self.k_per_row, self.u)
+        return [t for t in ts if t is not None]
+
     def attend(self):
+        if self.image:
+            self.bsa.forward_packed(self.q, self.k, self.v, self.idx, self.cnt, self.kv_map, self.o,
+                                    self.lse, quad_mask=self.quad_mask, q_map=self.q_map,
+                                    row_perm=None if self.order == "identity" else self.row_perm)
+            return
         if self.crm:
             self.bsa.forward_crm(self.q, self.k, self.v, self.words, self.o, self.lse,
                                  q_map=self.q_map, kv_map=self.kv_map)
@@ -261,6 +284,8 @@ class Path:
         self.attend()
 
     def effective_flops(self):
+        if self.image:
+            return image_useful_flops(self.prob)
         if self.crm:
             self.bsa.build_index(self.mode, self.src, self.idx, self.cnt, p=self.prob.p or 0.0)
         _, cnt = self.lists()
@@ -283,6 +308,8 @@ def time_oracle(prob, lists, budget_s: float, max_blocks: int | None = None, see
     """Oracle on a bounded sample of query blocks (spread over heads, seeded).
     Returns (effective TFLOP/s, seconds, blocks, threads)."""
     import oracle
+    if is_image_layer(prob):
+        return time_oracle_image(prob, budget_s, seed)
     idx, cnt, lw = lists
     g = np.random.default_rng(seed)
     order = g.permutation(prob.rows)
@@ -301,17 +328,57 @@ def time_oracle(prob, lists, budget_s: float, max_blocks: int | None = None, see
     return fl / t_total / 1e12, t_total, done, oracle.num_threads()
 
 
+def is_image_layer(prob):
+    return prob.img_h > 0
+
+
+def image_visible_pairs(prob):
+    """Query-key pairs the Gather 0 layer attends, per head: every image query
+    sees the text keys and its 16 x 16 window; every text query the text keys
+    and its Scatter group's image tokens."""
+    hw = prob.img_h * prob.img_w
+    text = prob.n_text * (prob.n_text + hw // prob.groups) if prob.n_text else 0
+    return hw * (prob.n_text + 256) + text
+
+
+def image_useful_flops(prob):
+    return 4.0 * prob.D * prob.B * prob.H * image_visible_pairs(prob)
+
+
+def time_oracle_image(prob, budget_s: float, seed: int = 0):
+    """The Gather 0 oracle on a bounded, seeded sample of (head, CQS) pairs.
+    Returns (TFLOP/s over visible pairs, seconds, sets, threads)."""
+    import oracle
+    sets = oracle.gather0_sets(prob.img_h, prob.img_w, prob.n_text, prob.groups)
+    order = np.random.default_rng(seed).permutation(prob.B * prob.H * len(sets))
+    done, fl, t_total = 0, 0.0, 0.0
+    for x in order:
+        bh, si = divmod(int(x), len(sets))
+        qt, kt = sets[si]
+        t0 = time.perf_counter()
+        oracle.attention_set(prob.q, prob.k, prob.v, bh, qt, kt)
+        t_total += time.perf_counter() - t0
+        fl += 4.0 * prob.D * len(qt) * len(kt)
+        done += 1
+        if t_total >= budget_s:
+            break
+    return fl / t_total / 1e12, t_total, done, oracle.num_threads()
+
+
 def token_mask(prob):
     return dict(causal=prob.causal, n_valid=prob.n_valid, window=prob.window, sinks=prob.sinks)
 
 
 def uses_masked_forward(prob):
-    return (prob.H_kv not in (None, prob.H)) or prob.causal or prob.window > 0 or prob.n_valid > 0
+    return ((prob.H_kv not in (None, prob.H)) or prob.causal or prob.window > 0 or prob.n_valid > 0
+            or is_image_layer(prob))
 
 
 def host_lists(prob):
     """Index lists for the oracle, from the oracle (reference arm / CPU leg only)."""
     import oracle
+    if is_image_layer(prob):
+        return None  # the Gather 0 oracle works from the layer's definition
     if prob.diag_list:
         idx, cnt = synth.diag_lists(prob.rows, prob.nqb)
         return idx, cnt, None
@@ -335,7 +402,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8])
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9])
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller profiling case)")
     ap.add_argument("--order", default="reordered", choices=["reordered", "identity", "spectral"],
                     help="row order: NNZ-guided wave sort, identity, or spectral (stage 1) + wave sort")
@@ -395,7 +462,26 @@ def config_dict(prob, config, order, density, world):
             "kv_rows": getattr(prob, "_kv_rows", "contiguous"),
             **({"H_kv": prob.H_kv or prob.H, "token_mask": token_mask(prob),
                 "flops": "listed blocks in full (masked keys inside a listed block are computed)"}
-               if uses_masked_forward(prob) else {})}
+               if uses_masked_forward(prob) and not is_image_layer(prob) else {}),
+            **({"image": f"{prob.img_h}x{prob.img_w}", "n_text": prob.n_text,
+                "scatter_groups": prob.groups,
+                "layout": "two 8x8 query patches per 128-row tile; 16x16 windows as packed "
+                          "8x16 key bands; 32-row quadrant masks (built once on the GPU)",
+                "flops": "attended query-key pairs only (4 D per pair); products of tiles "
+                         "hidden from a quadrant are extra work, not counted"}
+               if is_image_layer(prob) else {})}
+
+
+def sample_unit(prob):
+    return "(head, CQS) query sets" if is_image_layer(prob) else "query blocks"
+
+
+def workload_density(prob, listed_blocks):
+    """Fraction of the dense attention computed: listed blocks over all
+    blocks, or (image layer) attended query-key pairs over N^2."""
+    if is_image_layer(prob):
+        return image_visible_pairs(prob) / float(prob.N) ** 2
+    return float(listed_blocks) / (prob.rows * prob.nqb)
 
 
 def run_reference(args, world, rank):
@@ -403,7 +489,7 @@ def run_reference(args, world, rank):
         return
     prob = make_problem(args.config, args.heads, args.dense)
     lists = host_lists(prob)
-    density = float(lists[1].sum()) / (prob.rows * prob.nqb)
+    density = workload_density(prob, None if lists is None else lists[1].sum())
     # each step: the oracle on a bounded sample (about 1 s of CPU work)
     budget = 1.0
     for _ in range(args.warmup):
@@ -422,7 +508,7 @@ def run_reference(args, world, rank):
             "data": "synthetic", "impl": "reference",
             "config": config_dict(prob, args.config, args.order, density, 1),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{blocks} query blocks over {args.steps} steps "
+                             "sample": f"{blocks} {sample_unit(prob)} over {args.steps} steps "
                                        f"(~{budget:.0f} s of oracle CPU time per step)"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -463,7 +549,7 @@ def main():
         path.step()
     torch.cuda.synchronize()
     flops = path.effective_flops()
-    density = float(path.lists()[1].sum()) / (prob.rows * prob.nqb)
+    density = workload_density(prob, path.lists()[1].sum())
     if path.crm:
         args.order = "identity"
 
@@ -509,10 +595,7 @@ def main():
     pin = lambda t: t.cpu().pin_memory()  # noqa: E731
     paths = [path, Path(prob, dev, args.order, args.scores_on_gpu, args.crm, args.kv_gather)]
 
-    def inputs(pth):
-        return [t for t in (pth.q, pth.k, pth.v, pth.src, pth.q_map, pth.kv_map, pth.k_per_row,
-                            pth.u) if t is not None]
-    d_ins = [inputs(pth) for pth in paths]
+    d_ins = [pth.host_inputs() for pth in paths]
     h_in = [pin(t) for t in d_ins[0]]
     h_o = [torch.empty_like(path.o, device="cpu").pin_memory() for _ in range(2)]
     h_l = [torch.empty_like(path.lse, device="cpu").pin_memory() for _ in range(2)]
@@ -571,7 +654,8 @@ def main():
     if not args.no_cpu_baseline:
         v, s, b, threads = time_oracle(prob, host_lists(prob), args.cpu_budget)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"{b} of {prob.rows} query blocks (seeded), {s:.1f} s fp64 on host cores"}
+               "sample": f"{b} {sample_unit(prob)} (seeded sample of the workload), "
+                         f"{s:.1f} s fp64 on host cores"}
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
             "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
             "ms_per_step_median": statistics.median(step_ms) if world == 1 else None,
