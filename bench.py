@@ -206,7 +206,12 @@ class Path:
         if kv_gather == "auto":
             kv_gather = "kernel" if (prob.diag_list or self.image) else "hbm"
         if self.image:
-            kv_gather = "kernel"  # packed key tiles overlap: no N-row gathered copy exists
+            # packed key tiles overlap (no N-row gathered copy exists): fetch
+            # them as boxes of the image (auto), or row by row through kv_map
+            if kv_gather == "hbm":
+                raise SystemExit("--kv-gather hbm does not apply to the image layer")
+            self.image_boxes = kv_gather != "kernel"
+            kv_gather = "kernel"
         self.pregather = self.kv_map is not None and kv_gather == "hbm" and not self.crm
         self.masked = uses_masked_forward(prob)
         if self.pregather:
@@ -250,9 +255,15 @@ class Path:
 
     def attend(self):
         if self.image:
-            self.bsa.forward_packed(self.q, self.k, self.v, self.idx, self.cnt, self.kv_map, self.o,
-                                    self.lse, quad_mask=self.quad_mask, q_map=self.q_map,
-                                    row_perm=None if self.order == "identity" else self.row_perm)
+            perm = None if self.order == "identity" else self.row_perm
+            p = self.prob
+            if self.image_boxes:
+                self.bsa.forward_gather0(self.q, self.k, self.v, p.img_h, p.img_w, p.n_text, p.groups,
+                                         self.idx, self.cnt, self.o, self.lse, quad_mask=self.quad_mask,
+                                         row_perm=perm)
+            else:
+                self.bsa.forward_packed(self.q, self.k, self.v, self.idx, self.cnt, self.kv_map, self.o,
+                                        self.lse, quad_mask=self.quad_mask, q_map=self.q_map, row_perm=perm)
             return
         if self.crm:
             self.bsa.forward_crm(self.q, self.k, self.v, self.words, self.o, self.lse,
@@ -416,7 +427,8 @@ def parse():
     ap.add_argument("--kv-gather", default="auto", choices=["auto", "kernel", "hbm"],
                     help="index-mapped K/V: gather rows inside the forward kernel, or copy them "
                          "into gathered order in HBM first (auto: HBM unless each block is "
-                         "listed once)")
+                         "listed once; the image layer: tiles as boxes of the image, 'kernel' "
+                         "rows through kv_map)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle CPU time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -533,7 +545,11 @@ def main():
     prob._scores_on_gpu = args.scores_on_gpu and prob.scores is not None
     prob._crm = args.crm and (prob.mask is not None or prob.T is not None)
     path = Path(prob, dev, args.order, args.scores_on_gpu, args.crm, args.kv_gather)
-    if path.kv_map is not None:
+    if path.image:
+        prob._kv_rows = ("tiles fetched as TMA boxes of the image / Scatter-group views "
+                         "(bsa_forward_gather0)" if path.image_boxes else
+                         "gathered through kv_map inside the forward kernel (bsa_forward_packed)")
+    elif path.kv_map is not None:
         prob._kv_rows = ("copied into gathered order in HBM each step (bsa_gather_rows)"
                          if path.pregather else "gathered through kv_map inside the forward kernel")
     path.step()

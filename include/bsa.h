@@ -413,6 +413,35 @@ bsa_status bsa_gather0_layout(int32_t img_h, int32_t img_w, int32_t n_text, int3
                               int32_t* kv_cnt, uint8_t* quad_mask, int32_t max_kv, void* stream);
 
 /*
+ * bsa_forward_gather0 - the INTRA Gather 0 image layer, with every tile
+ * fetched as one tensor-memory-access box computed from the layer's index
+ * functions instead of through maps.
+ *
+ * Defined by: INTRA, appendix "Sparse Pattern Index Function", Gather 0
+ * (query patches, 16 x 16 windows shifted inward at the edges, text keys)
+ * and "CQS-Aware Token-Sparse FlashAttention Kernel" (index mappings
+ * computed at run time, outputs scattered back).
+ *
+ * Same result as bsa_forward_packed (bit for bit) on the maps of
+ * bsa_gather0_layout, without reading them: a query tile of two patches is
+ * a 16-row x 8-column box of the image, a window band an 8-row x 16-column
+ * box, a Scatter-group tile 128 tokens at stride groups, a text tile 128
+ * consecutive tokens.  O and LSE rows go to the original tokens.
+ *
+ *  q, o      device bf16 [B, H, N, D], N = n_text + img_h*img_w.
+ *  k, v      device bf16 [B, H_kv, N, D].
+ *  kv_idx, kv_cnt, quad_mask   from bsa_gather0_layout with the same
+ *            img_h, img_w, n_text, groups (quad_mask may be NULL: every
+ *            quadrant sees every listed tile); max_kv their row stride.
+ *  Geometry arguments as bsa_gather0_layout; other arguments as bsa_forward.
+ */
+bsa_status bsa_forward_gather0(const void* q, const void* k, const void* v, int32_t B, int32_t H,
+                               int32_t H_kv, int32_t D, int32_t img_h, int32_t img_w, int32_t n_text,
+                               int32_t groups, const int32_t* kv_idx, const int32_t* kv_cnt,
+                               const uint8_t* quad_mask, int32_t max_kv, const int32_t* row_perm,
+                               float scale, void* o, float* lse, void* stream);
+
+/*
  * bsa_gather_rows - token rows permuted into gathered order in HBM:
  *     dst[bh][p][:] = src[bh][map[bh][p]][:]    for p in 0..N-1.
  *

@@ -24,6 +24,7 @@ from .binding import (  # noqa: F401
     effective_flops,
     forward,
     forward_crm,
+    forward_gather0,
     forward_masked,
     forward_packed,
     gather0_layout,

@@ -25,7 +25,7 @@ EXPORTS = ("bsa_build_index", "bsa_build_crm", "bsa_forward_crm", "bsa_upscale_t
            "bsa_reorder_rows", "bsa_spectral_order",
            "bsa_spectral_order_workspace_size", "bsa_spectral_order_noalloc", "bsa_sample_blocks",
            "bsa_forward", "bsa_forward_masked", "bsa_forward_packed", "bsa_gather_rows",
-           "bsa_gather0_sizes", "bsa_gather0_layout",
+           "bsa_gather0_sizes", "bsa_gather0_layout", "bsa_forward_gather0",
            "bsa_device_status", "bsa_resident_ctas", "bsa_status_string", "bsa_selftest_exp2",
            "bsa_selftest_wait_timeout")
 
@@ -86,6 +86,9 @@ def load_library():
     lib.bsa_gather0_sizes.restype = i32
     lib.bsa_gather0_layout.argtypes = [i32, i32, i32, i32, i64, P, P, P, P, P, i32, P]
     lib.bsa_gather0_layout.restype = i32
+    lib.bsa_forward_gather0.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, P, P, P, i32,
+                                        P, f32, P, P, P]
+    lib.bsa_forward_gather0.restype = i32
     lib.bsa_device_status.argtypes = [P, ctypes.POINTER(i32)]
     lib.bsa_resident_ctas.argtypes = [i32]
     lib.bsa_status_string.argtypes = [i32]
@@ -394,6 +397,28 @@ def gather0_layout(img_h: int, img_w: int, n_text: int, groups: int, heads: int,
     return q_map, kv_map, kv_idx, kv_cnt, quad_mask
 
 
+def forward_gather0(q, k, v, img_h: int, img_w: int, n_text: int, groups: int, kv_idx, kv_cnt, o, lse,
+                    *, quad_mask=None, row_perm=None, scale: float = 0.0, stream=None):
+    """The INTRA Gather 0 layer with tiles fetched by geometry (see bsa.h);
+    kv_idx / kv_cnt / quad_mask from gather0_layout."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _dtype(t, n, torch.bfloat16)
+    _dtype(lse, "lse", torch.float32)
+    _dtype(quad_mask, "quad_mask", torch.uint8)
+    B, H, N, D = q.shape
+    H_kv = k.shape[1]
+    if k.shape != (B, H_kv, N, D) or v.shape != k.shape or o.shape != q.shape:
+        raise ValueError("q, o [B, H, N, D]; k, v [B, H_kv, N, D]")
+    if N != n_text + img_h * img_w:
+        raise ValueError("N must be n_text + img_h * img_w")
+    code = load_library().bsa_forward_gather0(
+        _ptr(q), _ptr(k), _ptr(v), B, H, H_kv, D, img_h, img_w, n_text, groups, _ptr(kv_idx),
+        _ptr(kv_cnt), _ptr(quad_mask), kv_idx.shape[1], _ptr(row_perm), float(scale), _ptr(o),
+        _ptr(lse), _stream(stream))
+    _check("bsa_forward_gather0", code)
+
+
 def device_status(stream=None) -> int:
     """Read and clear the device status word (synchronises the stream)."""
     out = ctypes.c_int32(0)
@@ -440,7 +465,7 @@ __all__ = ["BLOCK", "BsaError", "IDX_MASK_U8", "IDX_THRESHOLD_F32", "IDX_TOPK_F3
            "reorder_rows", "sample_blocks", "forward", "device_status", "resident_ctas",
            "effective_flops", "dense_attention_flops", "load_library", "lib_path", "EXPORTS",
            "block_scores", "SCORE_MEAN_DOT", "SCORE_CENTROID_EXP", "build_crm", "forward_crm",
-           "upscale_threshold", "gather_rows", "forward_masked", "forward_packed", "gather0_sizes",
+           "upscale_threshold", "gather_rows", "forward_masked", "forward_packed", "forward_gather0", "gather0_sizes",
            "gather0_layout",
            "spectral_order", "spectral_order_workspace_size", "spectral_order_noalloc",
            "NOALLOC_SCRATCH_BYTES", "reorder_guard",

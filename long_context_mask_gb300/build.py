@@ -21,7 +21,7 @@ LIB = os.path.join(HERE, "libbsa.so")
 SOURCES = ["bsa_api.cu", "bsa_index.cu", "bsa_scores.cu", "bsa_order.cu", "bsa_attn.cu",
            "bsa_selftest.cu",
            "bsa_noalloc.cu", "bsa_gather.cu"]
-HEADERS = ["bsa_internal.h", "bsa_ptx.cuh", "bsa_math.cuh"]
+HEADERS = ["bsa_internal.h", "bsa_ptx.cuh", "bsa_math.cuh", "bsa_gather0.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

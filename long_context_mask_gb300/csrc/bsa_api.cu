@@ -301,6 +301,29 @@ bsa_status bsa_gather0_layout(int32_t img_h, int32_t img_w, int32_t n_text, int3
     return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
+bsa_status bsa_forward_gather0(const void* q, const void* k, const void* v, int32_t B, int32_t H,
+                               int32_t H_kv, int32_t D, int32_t img_h, int32_t img_w, int32_t n_text,
+                               int32_t groups, const int32_t* kv_idx, const int32_t* kv_cnt,
+                               const uint8_t* quad_mask, int32_t max_kv, const int32_t* row_perm,
+                               float scale, void* o, float* lse, void* stream) {
+    bsa::Gather0Geom g;
+    if (!bsa::gather0_geometry(img_h, img_w, n_text, groups, &g)) return BSA_ERR_INVALID_ARG;
+    if (B >= 1 && H_kv >= 1 && (int64_t)B * H_kv * g.N_kv >= ((int64_t)1 << 40)) return BSA_ERR_INVALID_ARG;
+    const bsa_status c = check_forward(q, k, v, B, H, H_kv, g.N, D, kv_idx, kv_cnt, max_kv, nullptr,
+                                       nullptr, nullptr, row_perm, o, lse, g.N_kv / 128);
+    if (c != BSA_OK) return c;
+    int32_t* status = bsa::status_word_ptr();
+    if (!status) return BSA_ERR_CUDA;
+    bsa::ForwardArgs a{q,      k,       v,       B,        H,     g.N, D,   kv_idx, kv_cnt,
+                       max_kv, nullptr, nullptr, nullptr, row_perm, scale, o, lse, nullptr, 0};
+    a.H_kv = H_kv;
+    a.masked = true;
+    a.n_kv = g.N_kv;
+    a.quad_mask = quad_mask;
+    a.gather0 = &g;
+    return bsa::launch_forward(a, status, static_cast<cudaStream_t>(stream));
+}
+
 bsa_status bsa_forward_crm(const void* q, const void* k, const void* v, int32_t B, int32_t H,
                            int32_t N, int32_t D, const uint32_t* crm, int32_t crm_words,
                            const int32_t* q_map, const int32_t* kv_map, const int32_t* row_perm,

@@ -70,6 +70,7 @@
 
 #include <mutex>
 
+#include "bsa_gather0.cuh"
 #include "bsa_internal.h"
 #include "bsa_math.cuh"
 #include "bsa_ptx.cuh"
@@ -120,6 +121,11 @@ struct Params {
     // column halves) so that one copy brings a whole 128-row tile, reading
     // each 2D-byte row in full, and lands it as D/64 swizzled 16 KB boxes.
     CUtensorMap map_q, map_k, map_v;     // 3D box 64 x 128 rows x D/64
+    // Gather 0 geometry mode: the image as (64, x, y, D/64, head) with boxes
+    // of 8 x 16 (queries) and 16 x 8 (key/value bands) pixels, and the
+    // Scatter groups as (64, group, t, D/64, head) with boxes of 1 x 128
+    CUtensorMap map_qi, map_ki, map_vi, map_kg, map_vg;
+    g0::Geom geo;
     const __nv_bfloat16* q;              // gathered rows are copied with cp.async
     const __nv_bfloat16* k;
     const __nv_bfloat16* v;
@@ -238,9 +244,10 @@ struct CrmIter {
     }
 };
 
-template <int D, int kPoly, bool kCrm, bool kGather, bool kMask>
+template <int D, int kPoly, bool kCrm, bool kGather, bool kMask, bool kGeom>
 __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const __grid_constant__ Params P) {
     static_assert(!(kCrm && kMask), "the token mask reads block indices from the lists");
+    static_assert(!kGeom || (kMask && !kGather && !kCrm), "the geometry mode loads tiles by TMA boxes");
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -255,7 +262,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
     const int64_t bh_kv = (bh / P.H) * (P.H / P.group) + (bh % P.H) / P.group;
     const int32_t N = P.N, nQB = P.nQB, max_kv = P.max_kv;
     // key/value tiles: blocks of the sequence, or 128-entry groups of kv_map
-    const int32_t nKB = P.kv_map != nullptr ? P.n_kv / 128 : nQB;
+    const int32_t nKB = (kGeom || P.kv_map != nullptr) ? P.n_kv / 128 : nQB;
 
     // A block of this launch (or an unread earlier one) timed out: abandon.
     if (*reinterpret_cast<const volatile int32_t*>(P.status) == BSA_ERR_TIMEOUT) return;
@@ -314,6 +321,14 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
             prefetch_tensormap(&P.map_k);
             prefetch_tensormap(&P.map_v);
         }
+        if constexpr (kGeom) {
+            prefetch_tensormap(&P.map_ki);
+            prefetch_tensormap(&P.map_vi);
+            if (P.geo.nt > 0) {
+                prefetch_tensormap(&P.map_kg);
+                prefetch_tensormap(&P.map_vg);
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -333,7 +348,14 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
             int32_t issued = 0;
             if (g == 0 && P.q_map == nullptr && lane == 0) {  // gathered Q: the softmax warps
                 mbar_arrive_expect_tx(smem_u32(&bars->q_full), C::kTile);
-                tma_load_3d(s_q, &P.map_q, 0, (int32_t)(bh * N) + qb * 128, 0, smem_u32(&bars->q_full));
+                if (kGeom && qb >= P.geo.nT) {
+                    // two vertically adjacent 8 x 8 patches: 16 image rows x 8 columns
+                    const int32_t pq = qb - P.geo.nT;
+                    tma_load_5d(s_q, &P.map_qi, 0, 8 * (pq % P.geo.pw), 16 * (pq / P.geo.pw), 0, (int32_t)bh,
+                                smem_u32(&bars->q_full));
+                } else {
+                    tma_load_3d(s_q, &P.map_q, 0, (int32_t)(bh * N) + qb * 128, 0, smem_u32(&bars->q_full));
+                }
             }
             // Load order = MMA consumption order: K_0, K_1, K_2, then V_i, K_{i+3}.
             // The list is read 32 entries at a time with one coalesced load and
@@ -444,7 +466,22 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
                     for (int j = 0; j < 4; ++j) tok[j] = tok_next[j];
                 } else if (lane == 0) {  // tile load
                     mbar_arrive_expect_tx(fb, C::kTile);
-                    tma_load_3d(dst, is_v ? &P.map_v : &P.map_k, 0, (int32_t)(bh_kv * N) + kb * 128, 0, fb);
+                    if (kGeom && kb >= P.geo.nT) {
+                        const int32_t pk = kb - P.geo.nT;
+                        if (pk < 4 * P.geo.P) {
+                            // a window band: 8 image rows x 16 columns
+                            int32_t c0;
+                            const int32_t y0 = g0::band_top(P.geo, pk / 4, pk % 4, c0);
+                            tma_load_5d(dst, is_v ? &P.map_vi : &P.map_ki, 0, c0, y0, 0, (int32_t)bh_kv, fb);
+                        } else {
+                            // 128 tokens of one Scatter group
+                            const int32_t v = pk - 4 * P.geo.P;
+                            tma_load_5d(dst, is_v ? &P.map_vg : &P.map_kg, 0, v / P.geo.G, 128 * (v % P.geo.G), 0,
+                                        (int32_t)bh_kv, fb);
+                        }
+                    } else {
+                        tma_load_3d(dst, is_v ? &P.map_v : &P.map_k, 0, (int32_t)(bh_kv * N) + kb * 128, 0, fb);
+                    }
                 }
                 issued = t + 1;
             }
@@ -521,6 +558,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
         const int32_t p = qb * 128 + r;
         int32_t tok = p;
         bool tok_ok = true;
+        if constexpr (kGeom) tok = g0::query_token(P.geo, p);
         if (P.q_map != nullptr) {
             tok = P.q_map[bh * N + p];
             if (tok < 0 || tok >= N) {
@@ -554,7 +592,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
             uint32_t vis_w[4] = {~0u, ~0u, ~0u, ~0u};
             bool hidden = false;  // warp-uniform: no row of this warp sees block j
             if constexpr (kMask) hidden = qm_row != nullptr && ((qm_row[j] >> qd) & 1u) == 0u;
-            if (kMask && !hidden) {
+            if (kMask && !kGeom && !hidden) {
                 int32_t kb = list[j];
                 kb = (kb < 0 || kb >= nKB) ? 0 : kb;  // flagged by the producer
                 int32_t kmin, kmax;
@@ -772,12 +810,33 @@ bool encode_tile_map(CUtensorMap* map, const void* base, uint64_t rows, int D) {
     return r == CUDA_SUCCESS;
 }
 
+// Gather 0 views of a [heads, N, D] tensor whose tokens n_text .. N-1 are an
+// img_h x img_w image: (64 columns, x, y, D/64 halves, head) with a
+// 64 x bx x by x D/64 x 1 box, or with group = true the Scatter groups
+// (64, g, t, D/64, head) for token n_text + t*groups + g, box 64 x 1 x 128.
+bool encode_image_map(CUtensorMap* map, const void* base, uint64_t heads, int32_t N, int D,
+                      const g0::Geom& g, bool group, uint32_t bx, uint32_t by) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    const uint64_t row = (uint64_t)D * 2;
+    const void* img = static_cast<const uint8_t*>(base) + (uint64_t)g.nt * row;
+    cuuint64_t dims[5] = {64, (cuuint64_t)(group ? g.groups : g.w), (cuuint64_t)(group ? g.hw / g.groups : g.h),
+                          (cuuint64_t)(D / 64), (cuuint64_t)heads};
+    cuuint64_t strides[4] = {row, (cuuint64_t)(group ? g.groups : g.w) * row, 128, (cuuint64_t)N * row};
+    cuuint32_t box[5] = {64, group ? 1u : bx, group ? 128u : by, (cuuint32_t)(D / 64), 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(img), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <int D>
 size_t smem_bytes() {
     return 1024 + Cfg<D>::kData + sizeof(Barriers);
 }
 
-template <int D, int kPoly, bool kCrm, bool kGather, bool kMask>
+template <int D, int kPoly, bool kCrm, bool kGather, bool kMask, bool kGeom = false>
 cudaError_t prepare_kernel() {
     // Per device: opt in to the large dynamic shared-memory carve-out.
     static int done[64] = {0};
@@ -785,7 +844,7 @@ cudaError_t prepare_kernel() {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(k_bsa_forward<D, kPoly, kCrm, kGather, kMask>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k_bsa_forward<D, kPoly, kCrm, kGather, kMask, kGeom>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem_bytes<D>());
     if (e == cudaSuccess && dev < 64) done[dev] = 1;
     return e;
@@ -803,10 +862,10 @@ int poly_setting() {
     return v;
 }
 
-template <int D, int kPoly, bool kCrm, bool kGather, bool kMask = false>
+template <int D, int kPoly, bool kCrm, bool kGather, bool kMask = false, bool kGeom = false>
 bsa_status launch_dp(const Params& P, unsigned grid_x, unsigned grid_y, cudaStream_t stream) {
-    if (prepare_kernel<D, kPoly, kCrm, kGather, kMask>() != cudaSuccess) return BSA_ERR_CUDA;
-    k_bsa_forward<D, kPoly, kCrm, kGather, kMask>
+    if (prepare_kernel<D, kPoly, kCrm, kGather, kMask, kGeom>() != cudaSuccess) return BSA_ERR_CUDA;
+    k_bsa_forward<D, kPoly, kCrm, kGather, kMask, kGeom>
         <<<dim3(grid_x, grid_y), threads_for(kGather), smem_bytes<D>(), stream>>>(P);
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
@@ -848,6 +907,24 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
     const float scale = a.scale > 0.f ? a.scale : 1.0f / sqrtf((float)D);
     P.scale_log2 = scale * kLog2e;
     const unsigned gx = (unsigned)P.nQB, gy = (unsigned)(a.B * a.H);
+    if (a.gather0 != nullptr) {
+        // Gather 0 geometry mode: tiles are TMA boxes of the image views
+        const Gather0Geom& q0 = *a.gather0;
+        const g0::Geom g = g0::make(q0.img_h, q0.img_w, q0.n_text, q0.groups, q0.N, q0.N_kv);
+        P.geo = g;
+        P.n_kv = g.N_kv;
+        P.q_map = nullptr;
+        P.kv_map = nullptr;
+        const uint64_t qh = (uint64_t)a.B * a.H, kh = (uint64_t)a.B * H_kv;
+        ok = encode_image_map(&P.map_qi, a.q, qh, a.N, D, g, false, 8, 16) &&
+             encode_image_map(&P.map_ki, a.k, kh, a.N, D, g, false, 16, 8) &&
+             encode_image_map(&P.map_vi, a.v, kh, a.N, D, g, false, 16, 8);
+        if (ok && g.nt > 0)
+            ok = encode_image_map(&P.map_kg, a.k, kh, a.N, D, g, true, 0, 0) &&
+                 encode_image_map(&P.map_vg, a.v, kh, a.N, D, g, true, 0, 0);
+        if (!ok) return BSA_ERR_CUDA;
+        return launch_dp<D, kDefaultPoly, false, false, true, true>(P, gx, gy, stream);
+    }
     const bool crm = a.crm != nullptr, gather = a.kv_map != nullptr;
     if (a.masked) {
         if (crm) return BSA_ERR_UNSUPPORTED;
@@ -867,7 +944,7 @@ int32_t occupancy() {
     int per_sm = 0;
     // every instantiation holds one block per SM (shared memory bound)
     if (prepare_kernel<D, kDefaultPoly, false, false, false>() != cudaSuccess) return -1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bsa_forward<D, kDefaultPoly, false, false, false>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bsa_forward<D, kDefaultPoly, false, false, false, false>,
                                                       threads_for(false),
                                                       smem_bytes<D>()) != cudaSuccess)
         return -1;

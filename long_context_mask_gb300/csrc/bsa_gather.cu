@@ -18,6 +18,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "bsa_gather0.cuh"
 #include "bsa_internal.h"
 
 namespace bsa {
@@ -62,82 +63,15 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather_rows(const uint4* __r
 }
 
 // ---------------------------------------------------------------- Gather 0
-// INTRA, appendix "Sparse Pattern Index Function", Gather 0: an 8 x 8 patch of
-// image queries attends to the 16 x 16 window centred on it, shifted inward
-// at the image edges, and to every text key; text queries attend to every
-// text key and to their Scatter group's image tokens ("Mapping Back to
-// INTRA").  Two vertically adjacent patches share one 128-row query tile;
-// their windows are stored as 8-row x 16-column key bands (the band the two
-// windows share is stored once) and each listed band carries the 32-row
+// Maps, lists and quadrant masks of the INTRA Gather 0 layer; the index
+// functions are in bsa_gather0.cuh.  Two vertically adjacent patches share
+// one 128-row query tile; each listed window band carries the 32-row
 // quadrants that see it.
 
 constexpr int kLayoutThreads = 256;
+using g0::Geom;
 
-struct G0 {
-    int32_t h, w, nt, groups;
-    int32_t hw, pw;     // image tokens; patch columns (w / 8)
-    int32_t nT, P, G;   // text tiles; query tile pairs; key tiles per Scatter group
-    int32_t per;        // text queries per Scatter group
-    int32_t N, N_kv, nQB;
-};
-
-__device__ __forceinline__ int32_t clampi(int32_t x, int32_t lo, int32_t hi) {
-    return x < lo ? lo : (x > hi ? hi : x);
-}
-
-// Key bands of query tile pair p: top rows y0[0..cnt) ascending, the shared
-// left column c0, and the window tops ra (upper patch) and rb (lower patch).
-__device__ int pair_bands(const G0& g, int32_t p, int32_t (&y0)[4], int32_t& c0, int32_t& ra,
-                          int32_t& rb) {
-    const int32_t s = p / g.pw, c = p % g.pw;
-    ra = clampi(16 * s - 4, 0, g.h - 16);
-    rb = clampi(16 * s + 4, 0, g.h - 16);
-    c0 = clampi(8 * c - 4, 0, g.w - 16);
-    const int32_t cand[4] = {ra, ra + 8, rb, rb + 8};
-    int cnt = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        // insert cand[i] into the sorted prefix unless present
-        bool dup = false;
-        for (int j = 0; j < cnt; ++j) dup |= y0[j] == cand[i];
-        if (dup) continue;
-        int j = cnt++;
-        while (j > 0 && y0[j - 1] > cand[i]) {
-            y0[j] = y0[j - 1];
-            --j;
-        }
-        y0[j] = cand[i];
-    }
-    return cnt;
-}
-
-__device__ int32_t g0_query_token(const G0& g, int32_t pos) {
-    if (pos < g.nt) return pos;
-    const int32_t u = pos - g.nt, p = u / 128, i = u % 128;
-    const int32_t s = p / g.pw, c = p % g.pw;
-    const int32_t y = 16 * s + 8 * (i / 64) + (i % 64) / 8, x = 8 * c + i % 8;
-    return g.nt + y * g.w + x;
-}
-
-__device__ int32_t g0_key_token(const G0& g, int32_t pos) {
-    if (pos < g.nt) return pos;
-    const int32_t u = pos - g.nt;
-    if (u < 4 * g.hw) {
-        const int32_t slot = u / 128, e = u % 128;
-        int32_t y0[4] = {0, 0, 0, 0}, c0, ra, rb;
-        const int cnt = pair_bands(g, slot / 4, y0, c0, ra, rb);
-        int k = slot % 4;
-        k = k < cnt ? k : 0;  // unused slot: a copy of the first band (never listed)
-        int32_t yk = y0[0];
-#pragma unroll
-        for (int i = 1; i < 4; ++i) yk = i == k ? y0[i] : yk;
-        return g.nt + (yk + e / 16) * g.w + c0 + e % 16;
-    }
-    const int32_t v = u - 4 * g.hw, per_group = g.hw / g.groups;
-    return g.nt + (v % per_group) * g.groups + v / per_group;
-}
-
-__global__ void __launch_bounds__(kLayoutThreads) k_gather0_layout(G0 g, int32_t* __restrict__ q_map,
+__global__ void __launch_bounds__(kLayoutThreads) k_gather0_layout(Geom g, int32_t* __restrict__ q_map,
                                                                    int32_t* __restrict__ kv_map,
                                                                    int32_t* __restrict__ kv_idx,
                                                                    int32_t* __restrict__ kv_cnt,
@@ -148,12 +82,12 @@ __global__ void __launch_bounds__(kLayoutThreads) k_gather0_layout(G0 g, int32_t
     for (int64_t e = (int64_t)blockIdx.x * kLayoutThreads + threadIdx.x; e < per_head;
          e += (int64_t)gridDim.x * kLayoutThreads) {
         if (e < g.N) {
-            q_map[h * g.N + e] = g0_query_token(g, (int32_t)e);
+            q_map[h * g.N + e] = g0::query_token(g, (int32_t)e);
             continue;
         }
         if (e < (int64_t)g.N + g.N_kv) {
             const int32_t pos = (int32_t)(e - g.N);
-            kv_map[h * g.N_kv + pos] = g0_key_token(g, pos);
+            kv_map[h * g.N_kv + pos] = g0::key_token(g, pos);
             continue;
         }
         // one query tile's list
@@ -185,7 +119,7 @@ __global__ void __launch_bounds__(kLayoutThreads) k_gather0_layout(G0 g, int32_t
         } else {
             const int32_t p = qb - g.nT;
             int32_t y0[4] = {0, 0, 0, 0}, c0, ra, rb;
-            const int cnt = pair_bands(g, p, y0, c0, ra, rb);
+            const int cnt = g0::pair_bands(g, p, y0, c0, ra, rb);
             for (int u = 0; u < cnt; ++u, ++n) {
                 idx[n] = g.nT + 4 * p + u;
                 const bool upper = y0[u] == ra || y0[u] == ra + 8;
@@ -242,20 +176,7 @@ bool gather0_geometry(int32_t img_h, int32_t img_w, int32_t n_text, int32_t grou
 cudaError_t launch_gather0_layout(const Gather0Geom& geo, int64_t heads, int32_t* q_map, int32_t* kv_map,
                                   int32_t* kv_idx, int32_t* kv_cnt, uint8_t* quad_mask, int32_t max_kv,
                                   cudaStream_t stream) {
-    G0 g;
-    g.h = geo.img_h;
-    g.w = geo.img_w;
-    g.nt = geo.n_text;
-    g.groups = geo.groups;
-    g.hw = geo.img_h * geo.img_w;
-    g.pw = geo.img_w / 8;
-    g.nT = geo.n_text / 128;
-    g.P = g.hw / 128;
-    g.G = g.hw / g.groups / 128;
-    g.per = geo.n_text > 0 ? geo.n_text / geo.groups : 1;
-    g.N = geo.N;
-    g.N_kv = geo.N_kv;
-    g.nQB = geo.N / 128;
+    const Geom g = g0::make(geo.img_h, geo.img_w, geo.n_text, geo.groups, geo.N, geo.N_kv);
     const int64_t per_head = (int64_t)g.N + g.N_kv + g.nQB;
     const int64_t want = (per_head + kLayoutThreads - 1) / kLayoutThreads;
     const unsigned gx = (unsigned)(want < 4096 ? want : 4096);

@@ -175,6 +175,22 @@ def test_gather0_sizes_and_layout_validation(lib):
     assert lay(32, 32, 0, 1, 0, None, None, None, None, None, 4, None) == 0      # nothing to do
 
 
+def test_forward_gather0_host_validation(lib):
+    f = lib.bsa_forward_gather0
+
+    def call(img_h=32, img_w=32, n_text=128, groups=2, max_kv=9, H_kv=2, D=128, q=FAKE):
+        return f(q, FAKE, FAKE, 1, 4, H_kv, D, img_h, img_w, n_text, groups, FAKE, FAKE, FAKE, max_kv,
+                 None, 0.0, FAKE, FAKE, None)
+    assert call(D=96) == 2
+    assert call(img_h=24) == 1          # not a multiple of 16
+    assert call(n_text=100) == 1
+    assert call(groups=3) == 1
+    assert call(max_kv=0) == 1
+    assert call(max_kv=42) == 1         # beyond the 41 packed tiles
+    assert call(H_kv=3) == 1
+    assert call(q=FAKE_ODD) == 1
+
+
 def test_device_status_rejects_null_output(lib):
     assert lib.bsa_device_status(None, None) == 1
 

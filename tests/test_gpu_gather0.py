@@ -149,3 +149,70 @@ def test_forward_flux_shape_sampled():
     all_sets = oracle.gather0_sets(img_h, img_w, n_text, groups)
     rows = np.concatenate([all_sets[s][0] for s in sets])
     _check(o, lse, O_ref, L_ref, heads, rows)
+
+
+def _run_both(prob, heads_kv=None, row_perm=True):
+    """The packed forward on the layout's maps and the geometry-mode forward
+    on the same lists; returns both results and the inputs used."""
+    img_h, img_w, n_text, groups = prob.img_h, prob.img_w, prob.n_text, prob.groups
+    BH = prob.B * prob.H
+    k_h = prob.k if heads_kv is None else prob.k[:, :heads_kv].contiguous()
+    v_h = prob.v if heads_kv is None else prob.v[:, :heads_kv].contiguous()
+    q_map, kv_map, idx, cnt, qm = _layout(img_h, img_w, n_text, groups, BH)
+    perm = None
+    if row_perm:
+        perm = torch.empty((BH, prob.N // 128), dtype=torch.int32, device="cuda")
+        bsa.reorder_rows(cnt.view(BH, -1), bsa.resident_ctas(prob.D), perm)
+    q, k, v = prob.q.cuda(), k_h.cuda(), v_h.cuda()
+    kvh = k.shape[0] * k.shape[1]
+    o1, o2 = torch.empty_like(q), torch.empty_like(q)
+    l1 = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    l2 = torch.empty_like(l1)
+    bsa.forward_packed(q, k, v, idx, cnt, kv_map[:kvh].contiguous(), o1, l1, quad_mask=qm, q_map=q_map,
+                       row_perm=perm)
+    bsa.forward_gather0(q, k, v, img_h, img_w, n_text, groups, idx, cnt, o2, l2, quad_mask=qm,
+                        row_perm=perm)
+    torch.cuda.synchronize()
+    status_ok()
+    return (o1, l1), (o2, l2), (k_h, v_h)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("img_h,img_w,n_text,groups", SHAPES)
+def test_geometry_mode_small(img_h, img_w, n_text, groups, D):
+    """Tiles fetched as boxes of the image give the packed path's result bit
+    for bit, and match the oracle on every row."""
+    prob = synth.image_gather0(seed=40 + img_h, B=1, H=2, img_h=img_h, img_w=img_w, n_text=n_text,
+                               groups=groups, D=D)
+    (o1, l1), (o2, l2), _ = _run_both(prob, row_perm=False)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    O_ref, L_ref = oracle.gather0_attention(prob.q, prob.k, prob.v, img_h, img_w, n_text, groups)
+    _check(o2, l2, O_ref, L_ref, [0, 1], np.arange(prob.N))
+
+
+def test_geometry_mode_grouped_heads():
+    prob = synth.image_gather0(seed=41, B=2, H=4, img_h=48, img_w=16, n_text=256, groups=2, D=128)
+    (o1, l1), (o2, l2), (k_h, v_h) = _run_both(prob, heads_kv=2)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    O_ref, L_ref = oracle.gather0_attention(prob.q, k_h, v_h, prob.img_h, prob.img_w, prob.n_text,
+                                            prob.groups)
+    _check(o2, l2, O_ref, L_ref, list(range(8)), np.arange(prob.N))
+
+
+def test_geometry_mode_flux_shape():
+    """The benchmark's launch configuration (FLUX.1-dev shape, reordered rows):
+    bit-identical to the packed path everywhere, and against the oracle on
+    sampled CQS of the first and last head."""
+    prob = synth.image_gather0()
+    (o1, l1), (o2, l2), _ = _run_both(prob)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    img_h, img_w, n_text, groups = prob.img_h, prob.img_w, prob.n_text, prob.groups
+    n_img = img_h * img_w // 64
+    pw = img_w // 8
+    sets = [0, pw, 2 * pw + 5, n_img // 3, n_img - pw - 1, n_img - 1, n_img + 1, n_img + groups - 2]
+    heads = [0, prob.B * prob.H - 1]
+    O_ref, L_ref = oracle.gather0_attention(prob.q, prob.k, prob.v, img_h, img_w, n_text, groups,
+                                            heads=heads, sets=sets)
+    all_sets = oracle.gather0_sets(img_h, img_w, n_text, groups)
+    rows = np.concatenate([all_sets[s][0] for s in sets])
+    _check(o2, l2, O_ref, L_ref, heads, rows)
