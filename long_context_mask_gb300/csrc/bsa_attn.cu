@@ -121,11 +121,6 @@ struct Params {
     // column halves) so that one copy brings a whole 128-row tile, reading
     // each 2D-byte row in full, and lands it as D/64 swizzled 16 KB boxes.
     CUtensorMap map_q, map_k, map_v;     // 3D box 64 x 128 rows x D/64
-    // Gather 0 geometry mode: the image as (64, x, y, D/64, head) with boxes
-    // of 8 x 16 (queries) and 16 x 8 (key/value bands) pixels, and the
-    // Scatter groups as (64, group, t, D/64, head) with boxes of 1 x 128
-    CUtensorMap map_qi, map_ki, map_vi, map_kg, map_vg;
-    g0::Geom geo;
     const __nv_bfloat16* q;              // gathered rows are copied with cp.async
     const __nv_bfloat16* k;
     const __nv_bfloat16* v;
@@ -134,7 +129,6 @@ struct Params {
     const float* log_w;
     const int32_t* q_map;
     const int32_t* kv_map;
-    const uint8_t* quad_mask;  // [rows, max_kv] quadrant visibility (the kMask variant only)
     const int32_t* row_perm;
     const uint32_t* crm;  // CRM rows [rows, crm_words] (the CRM variant only)
     int32_t crm_words;
@@ -142,14 +136,27 @@ struct Params {
     float* lse;
     int32_t* status;
     int32_t N, nQB, max_kv;
-    int32_t n_kv;      // kv_map entries per key/value head (a multiple of 128)
     int32_t H, group;  // query heads per batch entry; query heads per key/value head
     int32_t causal, n_valid, window, sinks;  // token mask (the kMask variant only)
     float scale_log2;
+    // packed key tiles and quadrant masks (the kQuad variants)
+    int32_t n_kv;      // kv_map entries per key/value head (a multiple of 128)
+    const uint8_t* quad_mask;  // [rows, max_kv] quadrant visibility
+    // Gather 0 geometry mode: the image as (64, x, y, D/64, head) with boxes
+    // of 8 x 16 (queries) and 16 x 8 (key/value bands) pixels, and the
+    // Scatter groups as (64, group, t, D/64, head) with boxes of 1 x 128
+    g0::Geom geo;
+    CUtensorMap map_qi, map_ki, map_vi, map_kg, map_vg;
 };
 
 __device__ __forceinline__ void raise_status(int32_t* status, int32_t code) {
     atomicCAS(status, 0, code);
+}
+
+// Bits lo .. hi-1 of a 32-bit word, the bounds clamped to [0, 32].
+__device__ __forceinline__ uint32_t run_bits(int32_t lo, int32_t hi) {
+    const uint32_t l = (uint32_t)min(max(lo, 0), 32), h = (uint32_t)min(max(hi, 0), 32);
+    return h > l ? (uint32_t)(((1ull << h) - 1ull) ^ ((1ull << l) - 1ull)) : 0u;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -244,10 +251,11 @@ struct CrmIter {
     }
 };
 
-template <int D, int kPoly, bool kCrm, bool kGather, bool kMask, bool kGeom>
+template <int D, int kPoly, bool kCrm, bool kGather, bool kMask, bool kGeom, bool kQuad>
 __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const __grid_constant__ Params P) {
     static_assert(!(kCrm && kMask), "the token mask reads block indices from the lists");
-    static_assert(!kGeom || (kMask && !kGather && !kCrm), "the geometry mode loads tiles by TMA boxes");
+    static_assert(!kGeom || (kMask && kQuad && !kGather && !kCrm), "the geometry mode loads tiles by TMA boxes");
+    static_assert(!kQuad || kMask, "quadrant masks live in the masked variant");
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -262,7 +270,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
     const int64_t bh_kv = (bh / P.H) * (P.H / P.group) + (bh % P.H) / P.group;
     const int32_t N = P.N, nQB = P.nQB, max_kv = P.max_kv;
     // key/value tiles: blocks of the sequence, or 128-entry groups of kv_map
-    const int32_t nKB = (kGeom || P.kv_map != nullptr) ? P.n_kv / 128 : nQB;
+    const int32_t nKB = (kGeom || kGather) ? P.n_kv / 128 : nQB;
 
     // A block of this launch (or an unread earlier one) timed out: abandon.
     if (*reinterpret_cast<const volatile int32_t*>(P.status) == BSA_ERR_TIMEOUT) return;
@@ -574,7 +582,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
         const float* lw_row = P.log_w ? P.log_w + row * max_kv : nullptr;
         // quadrant visibility of the listed blocks: bit qd of entry j says
         // whether this warp's 32 rows see block j at all
-        const uint8_t* qm_row = (kMask && P.quad_mask != nullptr) ? P.quad_mask + row * max_kv : nullptr;
+        const uint8_t* qm_row = (kQuad && P.quad_mask != nullptr) ? P.quad_mask + row * max_kv : nullptr;
         float m = -INFINITY, l = 0.0f;
         bool ok = true;
         float lw_next = (lw_row && n > 0) ? lw_row[0] : 0.0f;
@@ -591,7 +599,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
             bool need_mask = false;
             uint32_t vis_w[4] = {~0u, ~0u, ~0u, ~0u};
             bool hidden = false;  // warp-uniform: no row of this warp sees block j
-            if constexpr (kMask) hidden = qm_row != nullptr && ((qm_row[j] >> qd) & 1u) == 0u;
+            if constexpr (kQuad) hidden = qm_row != nullptr && ((qm_row[j] >> qd) & 1u) == 0u;
             if (kMask && !kGeom && !hidden) {
                 int32_t kb = list[j];
                 kb = (kb < 0 || kb >= nKB) ? 0 : kb;  // flagged by the producer
@@ -611,7 +619,23 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
                             (P.window > 0 && kmin <= tok - P.window && kmax >= P.sinks);
                 // visibility of the 128 columns as four 32-bit words, built
                 // before S_j arrives so that only the words stay live
-                if (__any_sync(0xffffffffu, need_mask)) {
+                if (__any_sync(0xffffffffu, need_mask) && P.kv_map == nullptr) {
+                    // contiguous keys kbase .. kbase + 127: the visible ones form
+                    // at most two runs, [tok - window + 1, hi) and [0, min(sinks, hi))
+                    // with hi = min(n_valid, tok + 1) (causal) or n_valid; each word
+                    // is the union of the runs' bits in its 32 columns
+                    const int32_t hi_g = P.causal ? min(P.n_valid, tok + 1) : P.n_valid;
+                    int32_t a1 = -kbase, a2 = 0, b2 = 0;
+                    if (P.window > 0) {
+                        a1 = tok - P.window + 1 - kbase;
+                        a2 = -kbase;
+                        b2 = min(P.sinks, hi_g) - kbase;
+                    }
+                    const int32_t b1 = hi_g - kbase;
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+                        vis_w[x] = run_bits(a1 - 32 * x, b1 - 32 * x) | run_bits(a2 - 32 * x, b2 - 32 * x);
+                } else if (__any_sync(0xffffffffu, need_mask)) {
                     const int32_t nv = P.n_valid, win = P.window, sk = P.sinks;
                     const bool causal = P.causal != 0;
 #pragma unroll
@@ -638,7 +662,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
                 break;
             }
             tc_fence_after();
-            if (kMask && hidden) {
+            if (kQuad && hidden) {
                 // P_j = 0 for these rows; m, l and O are unchanged
                 uint32_t z[32];
 #pragma unroll
@@ -836,7 +860,7 @@ size_t smem_bytes() {
     return 1024 + Cfg<D>::kData + sizeof(Barriers);
 }
 
-template <int D, int kPoly, bool kCrm, bool kGather, bool kMask, bool kGeom = false>
+template <int D, int kPoly, bool kCrm, bool kGather, bool kMask, bool kGeom = false, bool kQuad = false>
 cudaError_t prepare_kernel() {
     // Per device: opt in to the large dynamic shared-memory carve-out.
     static int done[64] = {0};
@@ -844,7 +868,7 @@ cudaError_t prepare_kernel() {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(k_bsa_forward<D, kPoly, kCrm, kGather, kMask, kGeom>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k_bsa_forward<D, kPoly, kCrm, kGather, kMask, kGeom, kQuad>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem_bytes<D>());
     if (e == cudaSuccess && dev < 64) done[dev] = 1;
     return e;
@@ -862,10 +886,10 @@ int poly_setting() {
     return v;
 }
 
-template <int D, int kPoly, bool kCrm, bool kGather, bool kMask = false, bool kGeom = false>
+template <int D, int kPoly, bool kCrm, bool kGather, bool kMask = false, bool kGeom = false, bool kQuad = false>
 bsa_status launch_dp(const Params& P, unsigned grid_x, unsigned grid_y, cudaStream_t stream) {
-    if (prepare_kernel<D, kPoly, kCrm, kGather, kMask, kGeom>() != cudaSuccess) return BSA_ERR_CUDA;
-    k_bsa_forward<D, kPoly, kCrm, kGather, kMask, kGeom>
+    if (prepare_kernel<D, kPoly, kCrm, kGather, kMask, kGeom, kQuad>() != cudaSuccess) return BSA_ERR_CUDA;
+    k_bsa_forward<D, kPoly, kCrm, kGather, kMask, kGeom, kQuad>
         <<<dim3(grid_x, grid_y), threads_for(kGather), smem_bytes<D>(), stream>>>(P);
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
@@ -923,11 +947,14 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
             ok = encode_image_map(&P.map_kg, a.k, kh, a.N, D, g, true, 0, 0) &&
                  encode_image_map(&P.map_vg, a.v, kh, a.N, D, g, true, 0, 0);
         if (!ok) return BSA_ERR_CUDA;
-        return launch_dp<D, kDefaultPoly, false, false, true, true>(P, gx, gy, stream);
+        return launch_dp<D, kDefaultPoly, false, false, true, true, true>(P, gx, gy, stream);
     }
     const bool crm = a.crm != nullptr, gather = a.kv_map != nullptr;
     if (a.masked) {
         if (crm) return BSA_ERR_UNSUPPORTED;
+        if (gather && P.quad_mask != nullptr)
+            return launch_dp<D, kDefaultPoly, false, true, true, false, true>(P, gx, gy, stream);
+        if (P.quad_mask != nullptr) return BSA_ERR_UNSUPPORTED;  // packed tiles need kv_map
         return gather ? launch_dp<D, kDefaultPoly, false, true, true>(P, gx, gy, stream)
                       : launch_dp<D, kDefaultPoly, false, false, true>(P, gx, gy, stream);
     }
@@ -944,7 +971,7 @@ int32_t occupancy() {
     int per_sm = 0;
     // every instantiation holds one block per SM (shared memory bound)
     if (prepare_kernel<D, kDefaultPoly, false, false, false>() != cudaSuccess) return -1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bsa_forward<D, kDefaultPoly, false, false, false, false>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bsa_forward<D, kDefaultPoly, false, false, false, false, false>,
                                                       threads_for(false),
                                                       smem_bytes<D>()) != cudaSuccess)
         return -1;
