@@ -53,7 +53,7 @@ def load_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("bsa_attn.cu", "bsa_ptx.cuh"):
+    for f in ("bsa_attn.cu", "bsa_ptx.cuh", "bsa_math.cuh", "bsa_gather0.cuh"):
         with open(os.path.join(ROOT, "long_context_mask_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

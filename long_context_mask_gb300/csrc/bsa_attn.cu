@@ -586,9 +586,16 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
         float m = -INFINITY, l = 0.0f;
         bool ok = true;
         float lw_next = (lw_row && n > 0) ? lw_row[0] : 0.0f;
+        // The row's quadrant masks, 32 at a time (lane e holds entry base + e),
+        // loaded ahead so that no iteration waits on a global load before it
+        // knows whether its warp sees the block.
+        uint32_t qm_chunk = 0xFu;
+        if constexpr (kQuad) qm_chunk = (qm_row != nullptr && lane < n) ? qm_row[lane] : 0xFu;
         for (int32_t j = 0; j < n; ++j) {
             const float lw2 = lw_next * kLog2e;
             lw_next = (lw_row && j + 1 < n) ? lw_row[j + 1] : 0.0f;
+            if (kQuad && j > 0 && (j & 31) == 0)
+                qm_chunk = (qm_row != nullptr && j + lane < n) ? qm_row[j + lane] : 0xFu;
             const uint32_t sbuf = (uint32_t)(j % kSBuf) * 128u;
             // Token mask: the key tokens of block j (column c of the tile is key
             // 128 kb + c, or kv_map of it), read before the wait for S_j.  A
@@ -599,7 +606,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
             bool need_mask = false;
             uint32_t vis_w[4] = {~0u, ~0u, ~0u, ~0u};
             bool hidden = false;  // warp-uniform: no row of this warp sees block j
-            if constexpr (kQuad) hidden = qm_row != nullptr && ((qm_row[j] >> qd) & 1u) == 0u;
+            if constexpr (kQuad) hidden = ((__shfl_sync(0xffffffffu, qm_chunk, j & 31) >> qd) & 1u) == 0u;
             if (kMask && !kGeom && !hidden) {
                 int32_t kb = list[j];
                 kb = (kb < 0 || kb >= nKB) ? 0 : kb;  // flagged by the producer
