@@ -203,15 +203,16 @@ class Path:
         # (one HBM pass) when blocks are listed by many query blocks each, or
         # gather rows inside the forward kernel when each block is used once
         # (the Scatter layer's one block per query block).
-        if kv_gather == "auto":
-            kv_gather = "kernel" if (prob.diag_list or self.image) else "hbm"
+        self.image_boxes = False
         if self.image:
             # packed key tiles overlap (no N-row gathered copy exists): fetch
             # them as boxes of the image (auto), or row by row through kv_map
             if kv_gather == "hbm":
                 raise SystemExit("--kv-gather hbm does not apply to the image layer")
-            self.image_boxes = kv_gather != "kernel"
+            self.image_boxes = kv_gather == "auto"
             kv_gather = "kernel"
+        if kv_gather == "auto":
+            kv_gather = "kernel" if prob.diag_list else "hbm"
         self.pregather = self.kv_map is not None and kv_gather == "hbm" and not self.crm
         self.masked = uses_masked_forward(prob)
         if self.pregather:
