@@ -204,6 +204,8 @@ class Path:
         # gather rows inside the forward kernel when each block is used once
         # (the Scatter layer's one block per query block).
         self.image_boxes = False
+        # the Scatter layer: tiles as strided boxes (auto), or rows through the maps
+        self.scatter_boxes = prob.scatter_R > 0 and kv_gather == "auto"
         if self.image:
             # packed key tiles overlap (no N-row gathered copy exists): fetch
             # them as boxes of the image (auto), or row by row through kv_map
@@ -248,13 +250,20 @@ class Path:
             bsa.reorder_rows(cnt.reshape(self.heads, p.nqb), self.wave, self.row_perm)
 
     def host_inputs(self):
-        """Tensors a step takes from the host (end-to-end leg); the image
-        layer's layout is static and stays on the device."""
-        ts = (self.q, self.k, self.v) if self.image else (
+        """Tensors a step takes from the host (end-to-end leg); the static
+        patterns of the image and Scatter layers (layout, maps) stay on the
+        device, and their geometry modes do not read maps at all."""
+        ts = (self.q, self.k, self.v) if (self.image or self.scatter_boxes) else (
             self.q, self.k, self.v, self.src, self.q_map, self.kv_map, self.k_per_row, self.u)
         return [t for t in ts if t is not None]
 
     def attend(self):
+        if self.scatter_boxes:
+            idx, cnt = self.lists()
+            self.bsa.forward_scatter(self.q, self.k, self.v, self.prob.scatter_R, idx, cnt, self.o, self.lse,
+                                     log_w=self.lw,
+                                     row_perm=None if self.order == "identity" else self.row_perm)
+            return
         if self.image:
             perm = None if self.order == "identity" else self.row_perm
             p = self.prob
@@ -550,6 +559,8 @@ def main():
         prob._kv_rows = ("tiles fetched as TMA boxes of the image / Scatter-group views "
                          "(bsa_forward_gather0)" if path.image_boxes else
                          "gathered through kv_map inside the forward kernel (bsa_forward_packed)")
+    elif path.scatter_boxes:
+        prob._kv_rows = "Scatter tiles fetched as strided TMA boxes (bsa_forward_scatter)"
     elif path.kv_map is not None:
         prob._kv_rows = ("copied into gathered order in HBM each step (bsa_gather_rows)"
                          if path.pregather else "gathered through kv_map inside the forward kernel")

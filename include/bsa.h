@@ -442,6 +442,31 @@ bsa_status bsa_forward_gather0(const void* q, const void* k, const void* v, int3
                                float scale, void* o, float* lse, void* stream);
 
 /*
+ * bsa_forward_scatter - block-sparse attention over the Scatter layer's
+ * gathered order, with every tile fetched as one tensor-memory-access box.
+ *
+ * Defined by: INTRA, "Why Scatter Is Uniform and Non-Contiguous" (N = R*T
+ * tokens as (t, r) = t*R + r in T neighbourhoods of R; group S_r = {(t, r)})
+ * and "CQS-Aware Token-Sparse FlashAttention Kernel" (mappings computed at
+ * run time, outputs scattered back).
+ *
+ * The result is bsa_forward_masked without a token mask on the maps
+ *     q_map[bh][p] = kv_map[bh][p] = (p mod T)*R + p / T,   T = N / R,
+ * for every head (gathered position p = r*T + t holds token t*R + r), bit
+ * for bit, without reading maps: a 128-position tile is 128 tokens of one
+ * group at stride R.  List entries name gathered blocks 0 .. N/128 - 1 (block
+ * b covers group b / (T/128)); O and LSE rows go to the original tokens.
+ *
+ *  R         1 .. N, dividing N, with N / R a multiple of 128.
+ *  k, v      device bf16 [B, H_kv, N, D] (H_kv dividing H).
+ *  Other arguments as bsa_forward.
+ */
+bsa_status bsa_forward_scatter(const void* q, const void* k, const void* v, int32_t B, int32_t H,
+                               int32_t H_kv, int32_t N, int32_t D, int32_t R, const int32_t* kv_idx,
+                               const int32_t* kv_cnt, int32_t max_kv, const float* log_w,
+                               const int32_t* row_perm, float scale, void* o, float* lse, void* stream);
+
+/*
  * bsa_gather_rows - token rows permuted into gathered order in HBM:
  *     dst[bh][p][:] = src[bh][map[bh][p]][:]    for p in 0..N-1.
  *

@@ -27,6 +27,7 @@ from .binding import (  # noqa: F401
     forward_gather0,
     forward_masked,
     forward_packed,
+    forward_scatter,
     gather0_layout,
     gather0_sizes,
     gather_rows,

@@ -26,6 +26,7 @@ EXPORTS = ("bsa_build_index", "bsa_build_crm", "bsa_forward_crm", "bsa_upscale_t
            "bsa_spectral_order_workspace_size", "bsa_spectral_order_noalloc", "bsa_sample_blocks",
            "bsa_forward", "bsa_forward_masked", "bsa_forward_packed", "bsa_gather_rows",
            "bsa_gather0_sizes", "bsa_gather0_layout", "bsa_forward_gather0",
+           "bsa_forward_scatter",
            "bsa_device_status", "bsa_resident_ctas", "bsa_status_string", "bsa_selftest_exp2",
            "bsa_selftest_wait_timeout")
 
@@ -89,6 +90,8 @@ def load_library():
     lib.bsa_forward_gather0.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, P, P, P, i32,
                                         P, f32, P, P, P]
     lib.bsa_forward_gather0.restype = i32
+    lib.bsa_forward_scatter.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, P, P, i32, P, P, f32, P, P, P]
+    lib.bsa_forward_scatter.restype = i32
     lib.bsa_device_status.argtypes = [P, ctypes.POINTER(i32)]
     lib.bsa_resident_ctas.argtypes = [i32]
     lib.bsa_status_string.argtypes = [i32]
@@ -419,6 +422,25 @@ def forward_gather0(q, k, v, img_h: int, img_w: int, n_text: int, groups: int, k
     _check("bsa_forward_gather0", code)
 
 
+def forward_scatter(q, k, v, R: int, kv_idx, kv_cnt, o, lse, *, log_w=None, row_perm=None,
+                    scale: float = 0.0, stream=None):
+    """The Scatter layer with tiles fetched by geometry (see bsa.h): lists over
+    gathered blocks, p = r*T + t holding token t*R + r."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _dtype(t, n, torch.bfloat16)
+    _dtype(lse, "lse", torch.float32)
+    _dtype(log_w, "log_w", torch.float32)
+    B, H, N, D = q.shape
+    H_kv = k.shape[1]
+    if k.shape != (B, H_kv, N, D) or v.shape != k.shape or o.shape != q.shape:
+        raise ValueError("q, o [B, H, N, D]; k, v [B, H_kv, N, D]")
+    code = load_library().bsa_forward_scatter(
+        _ptr(q), _ptr(k), _ptr(v), B, H, H_kv, N, D, int(R), _ptr(kv_idx), _ptr(kv_cnt),
+        kv_idx.shape[1], _ptr(log_w), _ptr(row_perm), float(scale), _ptr(o), _ptr(lse), _stream(stream))
+    _check("bsa_forward_scatter", code)
+
+
 def device_status(stream=None) -> int:
     """Read and clear the device status word (synchronises the stream)."""
     out = ctypes.c_int32(0)
@@ -465,7 +487,7 @@ __all__ = ["BLOCK", "BsaError", "IDX_MASK_U8", "IDX_THRESHOLD_F32", "IDX_TOPK_F3
            "reorder_rows", "sample_blocks", "forward", "device_status", "resident_ctas",
            "effective_flops", "dense_attention_flops", "load_library", "lib_path", "EXPORTS",
            "block_scores", "SCORE_MEAN_DOT", "SCORE_CENTROID_EXP", "build_crm", "forward_crm",
-           "upscale_threshold", "gather_rows", "forward_masked", "forward_packed", "forward_gather0", "gather0_sizes",
+           "upscale_threshold", "gather_rows", "forward_masked", "forward_packed", "forward_gather0", "forward_scatter", "gather0_sizes",
            "gather0_layout",
            "spectral_order", "spectral_order_workspace_size", "spectral_order_noalloc",
            "NOALLOC_SCRATCH_BYTES", "reorder_guard",

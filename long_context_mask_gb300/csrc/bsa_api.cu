@@ -324,6 +324,23 @@ bsa_status bsa_forward_gather0(const void* q, const void* k, const void* v, int3
     return bsa::launch_forward(a, status, static_cast<cudaStream_t>(stream));
 }
 
+bsa_status bsa_forward_scatter(const void* q, const void* k, const void* v, int32_t B, int32_t H,
+                               int32_t H_kv, int32_t N, int32_t D, int32_t R, const int32_t* kv_idx,
+                               const int32_t* kv_cnt, int32_t max_kv, const float* log_w,
+                               const int32_t* row_perm, float scale, void* o, float* lse, void* stream) {
+    if (R < 1 || N < 128 || (N % R) != 0 || ((N / R) % 128) != 0) return BSA_ERR_INVALID_ARG;
+    const bsa_status c = check_forward(q, k, v, B, H, H_kv, N, D, kv_idx, kv_cnt, max_kv, log_w,
+                                       nullptr, nullptr, row_perm, o, lse);
+    if (c != BSA_OK) return c;
+    int32_t* status = bsa::status_word_ptr();
+    if (!status) return BSA_ERR_CUDA;
+    bsa::ForwardArgs a{q,      k,     v,       B,       H,        N,     D, kv_idx, kv_cnt,
+                       max_kv, log_w, nullptr, nullptr, row_perm, scale, o, lse,    nullptr, 0};
+    a.H_kv = H_kv;
+    a.scatter_R = R;
+    return bsa::launch_forward(a, status, static_cast<cudaStream_t>(stream));
+}
+
 bsa_status bsa_forward_crm(const void* q, const void* k, const void* v, int32_t B, int32_t H,
                            int32_t N, int32_t D, const uint32_t* crm, int32_t crm_words,
                            const int32_t* q_map, const int32_t* kv_map, const int32_t* row_perm,

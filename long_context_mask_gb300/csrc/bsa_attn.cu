@@ -147,6 +147,7 @@ struct Params {
     // Scatter groups as (64, group, t, D/64, head) with boxes of 1 x 128
     g0::Geom geo;
     CUtensorMap map_qi, map_ki, map_vi, map_kg, map_vg;
+    CUtensorMap map_qg;  // Scatter layer: queries as (64, group, t, D/64, head), box 1 x 128
 };
 
 __device__ __forceinline__ void raise_status(int32_t* status, int32_t code) {
@@ -254,7 +255,7 @@ struct CrmIter {
 template <int D, int kPoly, bool kCrm, bool kGather, bool kMask, bool kGeom, bool kQuad>
 __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const __grid_constant__ Params P) {
     static_assert(!(kCrm && kMask), "the token mask reads block indices from the lists");
-    static_assert(!kGeom || (kMask && kQuad && !kGather && !kCrm), "the geometry mode loads tiles by TMA boxes");
+    static_assert(!kGeom || (!kGather && !kCrm), "the geometry mode loads tiles by TMA boxes");
     static_assert(!kQuad || kMask, "quadrant masks live in the masked variant");
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -332,7 +333,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
         if constexpr (kGeom) {
             prefetch_tensormap(&P.map_ki);
             prefetch_tensormap(&P.map_vi);
-            if (P.geo.nt > 0) {
+            if (P.geo.nt > 0 || P.geo.scatter) {
                 prefetch_tensormap(&P.map_kg);
                 prefetch_tensormap(&P.map_vg);
             }
@@ -356,7 +357,11 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
             int32_t issued = 0;
             if (g == 0 && P.q_map == nullptr && lane == 0) {  // gathered Q: the softmax warps
                 mbar_arrive_expect_tx(smem_u32(&bars->q_full), C::kTile);
-                if (kGeom && qb >= P.geo.nT) {
+                if (kGeom && P.geo.scatter) {
+                    // 128 queries of one Scatter group at stride R
+                    tma_load_5d(s_q, &P.map_qg, 0, qb / P.geo.G, 128 * (qb % P.geo.G), 0, (int32_t)bh,
+                                smem_u32(&bars->q_full));
+                } else if (kGeom && qb >= P.geo.nT) {
                     // two vertically adjacent 8 x 8 patches: 16 image rows x 8 columns
                     const int32_t pq = qb - P.geo.nT;
                     tma_load_5d(s_q, &P.map_qi, 0, 8 * (pq % P.geo.pw), 16 * (pq / P.geo.pw), 0, (int32_t)bh,
@@ -955,6 +960,21 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
                  encode_image_map(&P.map_vg, a.v, kh, a.N, D, g, true, 0, 0);
         if (!ok) return BSA_ERR_CUDA;
         return launch_dp<D, kDefaultPoly, false, false, true, true, true>(P, gx, gy, stream);
+    }
+    if (a.scatter_R > 0) {
+        // Scatter geometry mode: every query and key/value tile is 128 tokens
+        // of one group at stride R, one TMA box each
+        const g0::Geom g = g0::make_scatter(a.N, a.scatter_R);
+        P.geo = g;
+        P.n_kv = g.N_kv;
+        P.q_map = nullptr;
+        P.kv_map = nullptr;
+        const uint64_t qh = (uint64_t)a.B * a.H, kh = (uint64_t)a.B * H_kv;
+        ok = encode_image_map(&P.map_qg, a.q, qh, a.N, D, g, true, 0, 0) &&
+             encode_image_map(&P.map_kg, a.k, kh, a.N, D, g, true, 0, 0) &&
+             encode_image_map(&P.map_vg, a.v, kh, a.N, D, g, true, 0, 0);
+        if (!ok) return BSA_ERR_CUDA;
+        return launch_dp<D, kDefaultPoly, false, false, false, true, false>(P, gx, gy, stream);
     }
     const bool crm = a.crm != nullptr, gather = a.kv_map != nullptr;
     if (a.masked) {

@@ -1,5 +1,6 @@
-// Index functions of the INTRA Gather 0 image layer, shared by the layout
-// kernel (bsa_gather.cu) and the forward kernel's geometry mode (bsa_attn.cu).
+// Index functions of the INTRA Gather 0 image layer and of the Scatter layer,
+// shared by the layout kernel (bsa_gather.cu) and the forward kernel's
+// geometry mode (bsa_attn.cu).
 //
 // INTRA, appendix "Sparse Pattern Index Function", Gather 0: an 8 x 8 patch of
 // image queries attends to the 16 x 16 window centred on it, shifted inward
@@ -12,6 +13,12 @@
 // slots per query tile pair for its windows' 8-row x 16-column bands (the band
 // the two windows share stored once); then the Scatter groups, 128 tokens per
 // tile.
+//
+// Scatter layer (INTRA, "Why Scatter Is Uniform and Non-Contiguous"): N = R*T
+// tokens, token (t, r) = t*R + r; group S_r = {(t, r) : t} in gathered order,
+// position p = r*T + t.  A 128-position tile is 128 tokens at stride R, and
+// the same geometry serves queries and keys.  It is described here with no
+// text and no image: every key tile is a group tile.
 #pragma once
 
 #include <stdint.h>
@@ -25,6 +32,7 @@ struct Geom {
     int32_t nT, P, G;   // text tiles; query tile pairs; key tiles per Scatter group
     int32_t per;        // text queries per Scatter group
     int32_t N, N_kv, nQB;
+    int32_t scatter;    // 1: the Scatter layer (groups = R, hw = N, no text, no image)
 };
 
 inline Geom make(int32_t h, int32_t w, int32_t nt, int32_t groups, int32_t N, int32_t N_kv) {
@@ -42,6 +50,24 @@ inline Geom make(int32_t h, int32_t w, int32_t nt, int32_t groups, int32_t N, in
     g.N = N;
     g.N_kv = N_kv;
     g.nQB = N / 128;
+    g.scatter = 0;
+    return g;
+}
+
+inline Geom make_scatter(int32_t N, int32_t R) {
+    Geom g;
+    g.h = g.w = g.nt = 0;
+    g.groups = R;
+    g.hw = N;
+    g.pw = 1;
+    g.nT = 0;
+    g.P = 0;
+    g.G = N / R / 128;
+    g.per = 1;
+    g.N = N;
+    g.N_kv = N;
+    g.nQB = N / 128;
+    g.scatter = 1;
     return g;
 }
 
@@ -79,6 +105,10 @@ __device__ __forceinline__ int32_t band_top(const Geom& g, int32_t p, int32_t u,
 
 // Original token of query position pos (the query map).
 __device__ __forceinline__ int32_t query_token(const Geom& g, int32_t pos) {
+    if (g.scatter) {
+        const int32_t T = g.hw / g.groups;
+        return (pos % T) * g.groups + pos / T;
+    }
     if (pos < g.nt) return pos;
     const int32_t u = pos - g.nt, p = u / 128, i = u % 128;
     const int32_t s = p / g.pw, c = p % g.pw;

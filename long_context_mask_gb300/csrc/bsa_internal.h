@@ -86,6 +86,7 @@ struct ForwardArgs {
     int32_t n_kv = 0;                     // kv_map entries per key/value head (0: N)
     const uint8_t* quad_mask = nullptr;   // [rows, max_kv] 32-row quadrant visibility
     const Gather0Geom* gather0 = nullptr;  // non-NULL: Gather 0 tiles by geometry
+    int32_t scatter_R = 0;                 // > 0: Scatter layer tiles by geometry (R groups)
 };
 // Returns BSA_OK, BSA_ERR_CUDA (launch / descriptor failure) or BSA_ERR_UNSUPPORTED.
 bsa_status launch_forward(const ForwardArgs& a, int32_t* status, cudaStream_t stream);

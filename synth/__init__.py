@@ -94,6 +94,7 @@ class Problem:
     img_w: int = 0
     n_text: int = 0
     groups: int = 1
+    scatter_R: int = 0                      # > 0: q_map = kv_map = scatter_map(N, scatter_R)
     extra: dict = field(default_factory=dict)
 
     @property
@@ -152,6 +153,7 @@ def scatter(seed: int = 3, B: int = 1, H: int = 24, N: int = 16384, D: int = 128
     if layer == "scatter":
         m = np.broadcast_to(scatter_map(N), (B * H, N)).copy()
         prob.q_map, prob.kv_map = m, m
+        prob.scatter_R = BLOCK
     return prob
 
 

@@ -191,6 +191,20 @@ def test_forward_gather0_host_validation(lib):
     assert call(q=FAKE_ODD) == 1
 
 
+def test_forward_scatter_host_validation(lib):
+    f = lib.bsa_forward_scatter
+
+    def call(N=2048, R=16, max_kv=2, H_kv=2, D=128):
+        return f(FAKE, FAKE, FAKE, 1, 4, H_kv, N, D, R, FAKE, FAKE, max_kv, None, None, 0.0, FAKE, FAKE, None)
+    assert call(D=96) == 2
+    assert call(R=0) == 1
+    assert call(R=3) == 1               # does not divide N
+    assert call(R=32) == 1              # N / R = 64 is not a multiple of 128
+    assert call(N=2000) == 1
+    assert call(max_kv=17) == 1         # more entries than blocks
+    assert call(H_kv=3) == 1
+
+
 def test_device_status_rejects_null_output(lib):
     assert lib.bsa_device_status(None, None) == 1
 
