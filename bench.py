@@ -494,6 +494,14 @@ def config_dict(prob, config, order, density, world):
                if is_image_layer(prob) else {})}
 
 
+def compulsory_bytes(prob):
+    """Bytes a forward launch must move: Q, K, V read once, O and LSE written."""
+    H_kv = prob.H_kv or prob.H
+    qo = 2 * prob.B * prob.H * prob.N * prob.D * 2
+    kv = 2 * prob.B * H_kv * prob.N * prob.D * 2
+    return float(qo + kv + prob.B * prob.H * prob.N * 4)
+
+
 def sample_unit(prob):
     return "(head, CQS) query sets" if is_image_layer(prob) else "query blocks"
 
@@ -675,6 +683,16 @@ def main():
                 "frac": achieved / peak, "traffic": traffic, "kernel": "k_bsa_forward",
                 "peak_source": f"{peak_src} bf16 burst", "ms_per_launch": fwd_avg_ms,
                 "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak))}
+    # A workload whose FLOPs per compulsory byte (Q, K, V read once, O and LSE
+    # written once) fall below the measured ridge is bounded by HBM instead.
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    alg_bytes = compulsory_bytes(prob)
+    if flops / alg_bytes < peak * 1e12 / (hbm * 1e9):
+        gbs = alg_bytes / (fwd_avg_ms * 1e-3) / 1e9
+        roofline.update({"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                         "peak_source": f"{peak_src} HBM copy", "algorithmic_bytes": alg_bytes,
+                         "tensor_tflops": achieved})
+        roofline.pop("frac_of_sustained")
 
     if rank != 0:
         return
