@@ -252,6 +252,41 @@ struct CrmIter {
     }
 };
 
+// Geometry mode: the query tile qb of head bh, and key/value tile kb of
+// key/value head bh_kv, each as one TMA box (Scatter group tile, pair of
+// image patches, window band, or 128 consecutive text tokens).
+__device__ __forceinline__ void geo_load_q(const Params& P, uint32_t dst, uint32_t bar, int64_t bh, int32_t qb) {
+    if (P.geo.scatter) {
+        // 128 queries of one Scatter group at stride R
+        tma_load_5d(dst, &P.map_qg, 0, qb / P.geo.G, 128 * (qb % P.geo.G), 0, (int32_t)bh, bar);
+    } else if (qb >= P.geo.nT) {
+        // two vertically adjacent 8 x 8 patches: 16 image rows x 8 columns
+        const int32_t pq = qb - P.geo.nT;
+        tma_load_5d(dst, &P.map_qi, 0, 8 * (pq % P.geo.pw), 16 * (pq / P.geo.pw), 0, (int32_t)bh, bar);
+    } else {
+        tma_load_3d(dst, &P.map_q, 0, (int32_t)(bh * P.N) + qb * 128, 0, bar);
+    }
+}
+__device__ __forceinline__ void geo_load_kv(const Params& P, uint32_t dst, uint32_t bar, bool is_v, int64_t bh_kv,
+                                            int32_t kb) {
+    if (kb >= P.geo.nT) {
+        const int32_t pk = kb - P.geo.nT;
+        if (pk < 4 * P.geo.P) {
+            // a window band: 8 image rows x 16 columns
+            int32_t c0;
+            const int32_t y0 = g0::band_top(P.geo, pk / 4, pk % 4, c0);
+            tma_load_5d(dst, is_v ? &P.map_vi : &P.map_ki, 0, c0, y0, 0, (int32_t)bh_kv, bar);
+        } else {
+            // 128 tokens of one Scatter group
+            const int32_t v = pk - 4 * P.geo.P;
+            tma_load_5d(dst, is_v ? &P.map_vg : &P.map_kg, 0, v / P.geo.G, 128 * (v % P.geo.G), 0, (int32_t)bh_kv,
+                        bar);
+        }
+    } else {
+        tma_load_3d(dst, is_v ? &P.map_v : &P.map_k, 0, (int32_t)(bh_kv * P.N) + kb * 128, 0, bar);
+    }
+}
+
 template <int D, int kPoly, bool kCrm, bool kGather, bool kMask, bool kGeom, bool kQuad>
 __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const __grid_constant__ Params P) {
     static_assert(!(kCrm && kMask), "the token mask reads block indices from the lists");
@@ -357,18 +392,8 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
             int32_t issued = 0;
             if (g == 0 && P.q_map == nullptr && lane == 0) {  // gathered Q: the softmax warps
                 mbar_arrive_expect_tx(smem_u32(&bars->q_full), C::kTile);
-                if (kGeom && P.geo.scatter) {
-                    // 128 queries of one Scatter group at stride R
-                    tma_load_5d(s_q, &P.map_qg, 0, qb / P.geo.G, 128 * (qb % P.geo.G), 0, (int32_t)bh,
-                                smem_u32(&bars->q_full));
-                } else if (kGeom && qb >= P.geo.nT) {
-                    // two vertically adjacent 8 x 8 patches: 16 image rows x 8 columns
-                    const int32_t pq = qb - P.geo.nT;
-                    tma_load_5d(s_q, &P.map_qi, 0, 8 * (pq % P.geo.pw), 16 * (pq / P.geo.pw), 0, (int32_t)bh,
-                                smem_u32(&bars->q_full));
-                } else {
-                    tma_load_3d(s_q, &P.map_q, 0, (int32_t)(bh * N) + qb * 128, 0, smem_u32(&bars->q_full));
-                }
+                if constexpr (kGeom) geo_load_q(P, s_q, smem_u32(&bars->q_full), bh, qb);
+                else tma_load_3d(s_q, &P.map_q, 0, (int32_t)(bh * N) + qb * 128, 0, smem_u32(&bars->q_full));
             }
             // Load order = MMA consumption order: K_0, K_1, K_2, then V_i, K_{i+3}.
             // The list is read 32 entries at a time with one coalesced load and
@@ -479,22 +504,8 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
                     for (int j = 0; j < 4; ++j) tok[j] = tok_next[j];
                 } else if (lane == 0) {  // tile load
                     mbar_arrive_expect_tx(fb, C::kTile);
-                    if (kGeom && kb >= P.geo.nT) {
-                        const int32_t pk = kb - P.geo.nT;
-                        if (pk < 4 * P.geo.P) {
-                            // a window band: 8 image rows x 16 columns
-                            int32_t c0;
-                            const int32_t y0 = g0::band_top(P.geo, pk / 4, pk % 4, c0);
-                            tma_load_5d(dst, is_v ? &P.map_vi : &P.map_ki, 0, c0, y0, 0, (int32_t)bh_kv, fb);
-                        } else {
-                            // 128 tokens of one Scatter group
-                            const int32_t v = pk - 4 * P.geo.P;
-                            tma_load_5d(dst, is_v ? &P.map_vg : &P.map_kg, 0, v / P.geo.G, 128 * (v % P.geo.G), 0,
-                                        (int32_t)bh_kv, fb);
-                        }
-                    } else {
-                        tma_load_3d(dst, is_v ? &P.map_v : &P.map_k, 0, (int32_t)(bh_kv * N) + kb * 128, 0, fb);
-                    }
+                    if constexpr (kGeom) geo_load_kv(P, dst, fb, is_v, bh_kv, kb);
+                    else tma_load_3d(dst, is_v ? &P.map_v : &P.map_k, 0, (int32_t)(bh_kv * N) + kb * 128, 0, fb);
                 }
                 issued = t + 1;
             }
@@ -832,6 +843,450 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
+// ---------------------------------------------------------------- per-item blocks
+// The geometry layers (Scatter, Gather 0) have short rows: 1 and 7-8 block
+// pairs.  One thread block per row pays a launch, a prologue, the first
+// tiles' DRAM round trip and an epilogue with the tensor core idle.  Here one
+// block per SM walks several rows ("items") in wave order: the producer runs
+// into the next item's Q (two Q buffers) and tiles while the current item
+// computes, the MMA lane starts the next item's QK as soon as its tiles land,
+// and the softmax warps hand O over (o_free) before they normalise and store
+// it.  Ring and score-buffer positions continue across items.
+struct ItemBarriers {
+    uint64_t full[16];
+    uint64_t empty[16];
+    uint64_t q_full[2];
+    uint64_t q_empty[2];
+    uint64_t p_full[kSBuf];
+    uint64_t o_free;
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int32_t abort;
+};
+
+struct Item {
+    int64_t bh, bh_kv, row;
+    int32_t qb, n;
+};
+
+// Item f is execution slot f % nQB of head f / nQB.  false: a bad row order
+// entry (every role skips the item alike).  `report`: raise the status for
+// bad entries (one role does).
+__device__ __forceinline__ bool decode_item(const Params& P, int64_t f, Item& it, bool report = false) {
+    const int32_t nQB = P.nQB;
+    it.bh = f / nQB;
+    const int32_t slot = (int32_t)(f - it.bh * nQB);
+    int32_t qb = slot;
+    if (P.row_perm != nullptr) {
+        qb = P.row_perm[it.bh * nQB + slot];
+        if (qb < 0 || qb >= nQB) {
+            if (report) raise_status(P.status, BSA_ERR_BOUNDS);
+            return false;
+        }
+    }
+    it.qb = qb;
+    it.bh_kv = (it.bh / P.H) * (P.H / P.group) + (it.bh % P.H) / P.group;
+    it.row = it.bh * nQB + qb;
+    int32_t n = P.kv_cnt[it.row];
+    if (report && (n < 0 || n > P.max_kv)) raise_status(P.status, n < 0 ? BSA_ERR_BOUNDS : BSA_ERR_OVERFLOW);
+    n = n < 0 ? 0 : (n > P.max_kv ? P.max_kv : n);
+    it.n = n;
+    return true;
+}
+
+__device__ __forceinline__ bool items_aborted(const ItemBarriers* b) {
+    return *reinterpret_cast<const volatile int32_t*>(&b->abort) != 0;
+}
+__device__ __forceinline__ void items_set_abort(ItemBarriers* b, int32_t* status) {
+    *reinterpret_cast<volatile int32_t*>(&b->abort) = 1;
+    raise_status(status, BSA_ERR_TIMEOUT);
+}
+
+template <int D>
+struct ItemCfg {
+    static constexpr int kStages = Cfg<D>::kStages - 1;  // room for the second Q tile
+    static constexpr int kData = Cfg<D>::kTile * (2 + kStages);
+};
+
+template <int D, int kPoly, bool kQuad>
+__global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_constant__ Params P, int64_t n_items) {
+    using C = Cfg<D>;
+    using IC = ItemCfg<D>;
+    constexpr int S = IC::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s_q = smem_u32(smem);  // two Q buffers, then the K/V ring
+    const uint32_t s_ring = s_q + 2 * C::kTile;
+    ItemBarriers* bars = reinterpret_cast<ItemBarriers*>(smem + IC::kData);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int32_t N = P.N, max_kv = P.max_kv, nKB = P.n_kv / 128;
+    // wave w takes item w * G + b, or w * G + G - 1 - b on odd waves (zig-zag)
+    const int64_t G = gridDim.x;
+    auto item_of = [&](int64_t w) -> int64_t {
+        return w * G + ((w & 1) ? (G - 1 - (int64_t)blockIdx.x) : (int64_t)blockIdx.x);
+    };
+
+    if (*reinterpret_cast<const volatile int32_t*>(P.status) == BSA_ERR_TIMEOUT) return;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&bars->full[s]), 1);
+            mbar_init(smem_u32(&bars->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bars->q_full[b]), 1);
+            mbar_init(smem_u32(&bars->q_empty[b]), 1);
+        }
+        for (int s = 0; s < kSBuf; ++s) mbar_init(smem_u32(&bars->p_full[s]), 128);
+        mbar_init(smem_u32(&bars->o_free), 128);
+        mbar_init(smem_u32(&bars->mma_done), 1);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tensormap(&P.map_k);
+        prefetch_tensormap(&P.map_v);
+        prefetch_tensormap(&P.map_ki);
+        prefetch_tensormap(&P.map_vi);
+        if (P.geo.nt > 0 || P.geo.scatter) {
+            prefetch_tensormap(&P.map_kg);
+            prefetch_tensormap(&P.map_vg);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ producer
+        uint32_t t_glob = 0, qi = 0;
+        uint32_t issued = 0, q_issued = 0;  // copies started (ring positions, Q loads)
+        bool ok = true;
+        for (int64_t w = 0; ok; ++w) {
+            const int64_t f = item_of(w);
+            if (f >= n_items) break;
+            Item it;
+            if (!decode_item(P, f, it, lane == 0)) continue;
+            const int32_t n = it.n;
+            if (n == 0) continue;
+            const int32_t* list = P.kv_idx + it.row * max_kv;
+            const uint32_t qbuf = qi & 1u;
+            if (lane == 0) {
+                // the buffer's previous item must be done with it
+                if (qi >= 2 && !mbar_wait(smem_u32(&bars->q_empty[qbuf]), ((qi >> 1) - 1u) & 1u, kWaitNs, P.status,
+                                          BSA_ERR_TIMEOUT))
+                    ok = false;
+                if (ok) {
+                    mbar_arrive_expect_tx(smem_u32(&bars->q_full[qbuf]), C::kTile);
+                    geo_load_q(P, s_q + qbuf * C::kTile, smem_u32(&bars->q_full[qbuf]), it.bh, it.qb);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+            if (!ok) break;
+            q_issued = qi + 1;
+            // tiles in MMA consumption order: K_0 .. K_2, then V_i, K_{i+3}, then the last V
+            int32_t chunk_base = -64, kb_lane = 0;
+            auto block_kb = [&](int32_t e) -> int32_t {
+                if (e - chunk_base >= 32 || e < chunk_base) {
+                    chunk_base = e & ~31;
+                    kb_lane = chunk_base + lane < n ? list[chunk_base + lane] : 0;
+                    if (kb_lane < 0 || kb_lane >= nKB) {
+                        raise_status(P.status, BSA_ERR_BOUNDS);
+                        kb_lane = 0;
+                    }
+                }
+                return __shfl_sync(0xffffffffu, kb_lane, e - chunk_base);
+            };
+            const int32_t lead = n < kSBuf ? n : kSBuf;
+            const int32_t inter = 2 * (n - lead);
+            for (int32_t t = 0; t < 2 * n; ++t) {
+                const bool is_v = t >= lead && (t - lead >= inter || ((t - lead) & 1) == 0);
+                int32_t e;
+                if (t < lead) e = t;
+                else if (t - lead < inter) e = ((t - lead) >> 1) + (is_v ? 0 : kSBuf);
+                else e = (n - lead) + (t - lead - inter);
+                const int32_t kb = block_kb(e);
+                const uint32_t pos = t_glob + (uint32_t)t;
+                const uint32_t slot = pos % S;
+                int wt = 1;
+                if (lane == 0)
+                    wt = mbar_wait(smem_u32(&bars->empty[slot]), ((pos / S) & 1u) ^ 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                wt = __shfl_sync(0xffffffffu, wt, 0);
+                if (!wt || items_aborted(bars)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t fb = smem_u32(&bars->full[slot]);
+                    mbar_arrive_expect_tx(fb, C::kTile);
+                    geo_load_kv(P, s_ring + slot * C::kTile, fb, is_v, it.bh_kv, kb);
+                }
+                issued = pos + 1;
+            }
+            if (!ok) break;
+            t_glob += 2u * (uint32_t)n;
+            ++qi;
+        }
+        if (!ok && lane == 0) items_set_abort(bars, P.status);
+        // Drain: every issued copy must land before the block exits (older
+        // copies were consumed before their buffers were reused).
+        if (lane == 0) {
+            for (uint32_t q = q_issued > 2 ? q_issued - 2 : 0; q < q_issued; ++q)
+                if (!mbar_wait(smem_u32(&bars->q_full[q & 1u]), (q >> 1) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT))
+                    raise_status(P.status, BSA_ERR_TIMEOUT);
+            const uint32_t first = issued > (uint32_t)S ? issued - S : 0;
+            for (uint32_t i = first; i < issued; ++i)
+                if (!mbar_wait(smem_u32(&bars->full[i % S]), (i / S) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT))
+                    raise_status(P.status, BSA_ERR_TIMEOUT);
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint64_t dk = smem_desc_sw128(s_ring, 16, 1024);
+            const uint64_t dv = smem_desc_sw128(s_ring, C::kBoxBytes, 1024);
+            uint32_t pos = 0, g_glob = 0, qi = 0;  // ring position, score buffer count, items
+            bool ok = true;
+            for (int64_t w = 0; ok; ++w) {
+                const int64_t f = item_of(w);
+                if (f >= n_items) break;
+                Item it;
+                if (!decode_item(P, f, it) || it.n == 0) continue;
+                const int32_t n = it.n;
+                const uint32_t qbuf = qi & 1u;
+                ok = mbar_wait(smem_u32(&bars->q_full[qbuf]), (qi >> 1) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t dq = smem_desc_sw128(s_q + qbuf * C::kTile, 16, 1024);
+                auto issue_qk = [&](int32_t j) -> bool {
+                    const uint32_t slot = pos % S;
+                    if (!mbar_wait(smem_u32(&bars->full[slot]), (pos / S) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT))
+                        return false;
+                    tc_fence_after();
+                    const uint64_t ks = dk + (uint64_t)((slot * C::kTile) >> 4);
+                    const uint32_t d_col = ((g_glob + (uint32_t)j) % kSBuf) * 128u;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+                        mma_ss(tmem + d_col, dq + off, ks + off, C::kIdescQK, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&bars->empty[slot]));  // also signals S_j to the softmax
+                    ++pos;
+                    return true;
+                };
+                for (int32_t j = 0; ok && j < n && j < kSBuf; ++j) ok = issue_qk(j);
+                for (int32_t i = 0; ok && i < n; ++i) {
+                    const uint32_t gb = g_glob + (uint32_t)i;
+                    ok = mbar_wait(smem_u32(&bars->p_full[gb % kSBuf]), (gb / kSBuf) & 1u, kWaitNs, P.status,
+                                   BSA_ERR_TIMEOUT);
+                    // the first PV of an item overwrites O: the previous item's
+                    // epilogue must have read it out
+                    if (ok && i == 0 && qi > 0)
+                        ok = mbar_wait(smem_u32(&bars->o_free), (qi - 1u) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                    if (!ok) break;
+                    const uint32_t slot = pos % S;
+                    ok = mbar_wait(smem_u32(&bars->full[slot]), (pos / S) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t vs = dv + (uint64_t)((slot * C::kTile) >> 4);
+                    const uint32_t p_col = (gb % kSBuf) * 128u;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ts(tmem + kColO, tmem + p_col + kk * 8, vs + (uint64_t)(kk * 2048 >> 4), C::kIdescPV,
+                               (i > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(smem_u32(&bars->empty[slot]));  // also signals PV_i to the softmax
+                    ++pos;
+                    // score buffer gb % 3 is free again once PV_i (issued above) has read P
+                    if (i + kSBuf < n) ok = issue_qk(i + kSBuf);
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&bars->q_empty[qbuf]));  // this item's Q buffer, once its MMAs ran
+                g_glob += (uint32_t)n;
+                ++qi;
+            }
+            if (!ok) items_set_abort(bars, P.status);
+            // Drain: nothing of ours may still be running when TMEM is freed.
+            mma_commit(smem_u32(&bars->mma_done));
+            if (!mbar_wait(smem_u32(&bars->mma_done), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT))
+                raise_status(P.status, BSA_ERR_TIMEOUT);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int qd = warp & 3;                 // TMEM lane quadrant of this warp
+        const int r = qd * 32 + lane;            // row within the query tile
+        const uint32_t t_lane = tmem + ((uint32_t)(qd * 32) << 16);
+        const float sl2 = P.scale_log2;
+        uint32_t t_glob = 0, g_glob = 0;
+        bool ok = true;
+        for (int64_t w = 0; ok; ++w) {
+            const int64_t f = item_of(w);
+            if (f >= n_items) break;
+            Item it;
+            if (!decode_item(P, f, it)) continue;
+            const int32_t n = it.n;
+            const int32_t tok = g0::query_token(P.geo, it.qb * 128 + r);
+            __nv_bfloat16* orow = P.o + (it.bh * N + tok) * D;
+            if (n == 0) {
+                const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(orow + c) = z;
+                P.lse[it.bh * N + tok] = -INFINITY;
+                continue;
+            }
+            const float* lw_row = P.log_w ? P.log_w + it.row * max_kv : nullptr;
+            const uint8_t* qm_row = (kQuad && P.quad_mask != nullptr) ? P.quad_mask + it.row * max_kv : nullptr;
+            float m = -INFINITY, l = 0.0f;
+            float lw_next = lw_row ? lw_row[0] : 0.0f;
+            uint32_t qm_chunk = 0xFu;
+            if constexpr (kQuad) qm_chunk = (qm_row != nullptr && lane < n) ? qm_row[lane] : 0xFu;
+            for (int32_t j = 0; j < n; ++j) {
+                const float lw2 = lw_next * kLog2e;
+                lw_next = (lw_row && j + 1 < n) ? lw_row[j + 1] : 0.0f;
+                if (kQuad && j > 0 && (j & 31) == 0)
+                    qm_chunk = (qm_row != nullptr && j + lane < n) ? qm_row[j + lane] : 0xFu;
+                const uint32_t gb = g_glob + (uint32_t)j;
+                const uint32_t sbuf = (gb % kSBuf) * 128u;
+                bool hidden = false;  // warp-uniform: no row of this warp sees block j
+                if constexpr (kQuad) hidden = ((__shfl_sync(0xffffffffu, qm_chunk, j & 31) >> qd) & 1u) == 0u;
+                const uint32_t pk = t_glob + (uint32_t)ring_pos_k(j);
+                bool wt = mbar_wait(smem_u32(&bars->empty[pk % S]), (pk / S) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                if (__any_sync(0xffffffffu, !wt || items_aborted(bars))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (kQuad && hidden) {
+                    // P_j = 0 for these rows; m, l and O are unchanged
+                    uint32_t z[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) z[c] = 0u;
+                    tmem_st32(t_lane + sbuf + 0, z);
+                    tmem_st32(t_lane + sbuf + 32, z);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&bars->p_full[gb % kSBuf]));
+                    continue;
+                }
+                uint32_t s[128];
+                tmem_ld32(t_lane + sbuf + 0, &s[0]);
+                tmem_ld32(t_lane + sbuf + 32, &s[32]);
+                tmem_ld32(t_lane + sbuf + 64, &s[64]);
+                tmem_ld32(t_lane + sbuf + 96, &s[96]);
+                tmem_wait_ld();
+                float mx0 = __uint_as_float(s[0]), mx1 = __uint_as_float(s[1]);
+                float mx2 = __uint_as_float(s[2]), mx3 = __uint_as_float(s[3]);
+#pragma unroll
+                for (int c = 4; c < 128; c += 4) {
+                    mx0 = fmaxf(mx0, __uint_as_float(s[c + 0]));
+                    mx1 = fmaxf(mx1, __uint_as_float(s[c + 1]));
+                    mx2 = fmaxf(mx2, __uint_as_float(s[c + 2]));
+                    mx3 = fmaxf(mx3, __uint_as_float(s[c + 3]));
+                }
+                const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2 + lw2;
+                const bool rescale = j > 0 && __any_sync(0xffffffffu, mt > m + kRescaleThreshold);
+                float alpha = 1.0f;
+                if (j == 0) {
+                    m = mt;
+                } else if (rescale) {
+                    const float m_new = fmaxf(m, mt);
+                    alpha = (kQuad && m == -INFINITY) ? 0.0f : ex2(m - m_new);
+                    l *= alpha;
+                    m = m_new;
+                }
+                const float bias = lw2 - ((kQuad && m == -INFINITY) ? 0.0f : m);
+                float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+                for (int c = 0; c < 128; c += 4) {
+                    const float x0 = fmaf(__uint_as_float(s[c + 0]), sl2, bias);
+                    const float x1 = fmaf(__uint_as_float(s[c + 1]), sl2, bias);
+                    const float x2 = fmaf(__uint_as_float(s[c + 2]), sl2, bias);
+                    const float x3 = fmaf(__uint_as_float(s[c + 3]), sl2, bias);
+                    const float p0 = ((c + 0) % 8) < kPoly ? exp2_fma(x0) : ex2(x0);
+                    const float p1 = ((c + 1) % 8) < kPoly ? exp2_fma(x1) : ex2(x1);
+                    const float p2 = ((c + 2) % 8) < kPoly ? exp2_fma(x2) : ex2(x2);
+                    const float p3 = ((c + 3) % 8) < kPoly ? exp2_fma(x3) : ex2(x3);
+                    l0 += p0;
+                    l1 += p1;
+                    l2 += p2;
+                    l3 += p3;
+                    s[c / 2] = pack_bf16(p0, p1);
+                    s[c / 2 + 1] = pack_bf16(p2, p3);
+                }
+                l += (l0 + l1) + (l2 + l3);
+                tmem_st32(t_lane + sbuf + 0, &s[0]);
+                tmem_st32(t_lane + sbuf + 32, &s[32]);
+                if (rescale) {
+                    // O must hold P_0..P_{j-1} V: wait for PV_{j-1}
+                    const uint32_t pv = t_glob + (uint32_t)ring_pos_v(j - 1, n);
+                    wt = mbar_wait(smem_u32(&bars->empty[pv % S]), (pv / S) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                    if (__any_sync(0xffffffffu, !wt)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(t_lane + kColO + c, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(t_lane + kColO + c, o);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars->p_full[gb % kSBuf]));
+            }
+            if (!ok) break;
+            // Epilogue: once PV_{n-1} has run, read O out of tensor memory, hand
+            // the accumulator to the next item (o_free), then normalise and
+            // store while the next item's products proceed.
+            {
+                const uint32_t pv = t_glob + (uint32_t)ring_pos_v(n - 1, n);
+                const bool wt = mbar_wait(smem_u32(&bars->empty[pv % S]), (pv / S) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                if (__any_sync(0xffffffffu, !wt)) {
+                    ok = false;
+                    break;
+                }
+            }
+            tc_fence_after();
+            uint32_t o[D];
+#pragma unroll
+            for (int c = 0; c < D; c += 32) tmem_ld32(t_lane + kColO + c, &o[c]);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars->o_free));
+            const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;  // l = 0: every key dropped
+#pragma unroll
+            for (int c = 0; c < D; c += 8) {
+                uint4 v4;
+                v4.x = pack_bf16(__uint_as_float(o[c + 0]) * inv_l, __uint_as_float(o[c + 1]) * inv_l);
+                v4.y = pack_bf16(__uint_as_float(o[c + 2]) * inv_l, __uint_as_float(o[c + 3]) * inv_l);
+                v4.z = pack_bf16(__uint_as_float(o[c + 4]) * inv_l, __uint_as_float(o[c + 5]) * inv_l);
+                v4.w = pack_bf16(__uint_as_float(o[c + 6]) * inv_l, __uint_as_float(o[c + 7]) * inv_l);
+                *reinterpret_cast<uint4*>(orow + c) = v4;
+            }
+            P.lse[it.bh * N + tok] = l > 0.0f ? (m + log2f(l)) * kLn2 : -INFINITY;
+            t_glob += 2u * (uint32_t)n;
+            g_glob += (uint32_t)n;
+        }
+        if (!ok && lane == 0) items_set_abort(bars, P.status);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
 // [rows, D] as (64 columns, rows, D/64 halves) with a 64 x 128 x D/64 box.
 bool encode_tile_map(CUtensorMap* map, const void* base, uint64_t rows, int D) {
     auto enc = get_encode();
@@ -888,6 +1343,36 @@ cudaError_t prepare_kernel() {
 
 // Share of exponentials (out of every 8) computed by exp2_fma instead of
 // the MUFU unit.  BSA_EXP2_POLY=<0|2> overrides it (tuning).
+// Per-item blocks for the geometry layers (the default); BSA_ITEMS=0 runs
+// one block per row instead (tuning, comparisons).
+int items_setting() {
+    static int v = -1;
+    if (v < 0) {
+        const char* s = getenv("BSA_ITEMS");
+        v = (s && s[0] == '0' && s[1] == 0) ? 0 : 1;
+    }
+    return v;
+}
+
+template <int D, bool kQuad>
+bsa_status launch_items(const Params& P, int64_t n_items, cudaStream_t stream) {
+    const size_t smem = 1024 + ItemCfg<D>::kData + sizeof(ItemBarriers);
+    static int done[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
+    if (dev >= 64 || !done[dev]) {
+        if (cudaFuncSetAttribute(k_bsa_forward_items<D, kDefaultPoly, kQuad>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return BSA_ERR_CUDA;
+        if (dev < 64) done[dev] = 1;
+    }
+    const int32_t resident = forward_resident_ctas(D);
+    if (resident <= 0) return BSA_ERR_CUDA;
+    const unsigned grid = (unsigned)(n_items < resident ? n_items : resident);
+    k_bsa_forward_items<D, kDefaultPoly, kQuad><<<grid, 192, smem, stream>>>(P, n_items);
+    return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
 int poly_setting() {
     static int v = -1;
     if (v < 0) {
@@ -959,6 +1444,7 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
             ok = encode_image_map(&P.map_kg, a.k, kh, a.N, D, g, true, 0, 0) &&
                  encode_image_map(&P.map_vg, a.v, kh, a.N, D, g, true, 0, 0);
         if (!ok) return BSA_ERR_CUDA;
+        if (items_setting()) return launch_items<D, true>(P, (int64_t)gx * gy, stream);
         return launch_dp<D, kDefaultPoly, false, false, true, true, true>(P, gx, gy, stream);
     }
     if (a.scatter_R > 0) {
@@ -974,6 +1460,7 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
              encode_image_map(&P.map_kg, a.k, kh, a.N, D, g, true, 0, 0) &&
              encode_image_map(&P.map_vg, a.v, kh, a.N, D, g, true, 0, 0);
         if (!ok) return BSA_ERR_CUDA;
+        if (items_setting()) return launch_items<D, false>(P, (int64_t)gx * gy, stream);
         return launch_dp<D, kDefaultPoly, false, false, false, true, false>(P, gx, gy, stream);
     }
     const bool crm = a.crm != nullptr, gather = a.kv_map != nullptr;
