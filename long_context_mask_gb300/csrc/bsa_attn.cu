@@ -908,8 +908,9 @@ struct ItemCfg {
     static constexpr int kData = Cfg<D>::kTile * (2 + kStages);
 };
 
-template <int D, int kPoly, bool kQuad>
+template <int D, int kPoly, bool kMask, bool kGeom, bool kQuad>
 __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_constant__ Params P, int64_t n_items) {
+    static_assert(!kQuad || kMask, "quadrant masks live in the masked variant");
     using C = Cfg<D>;
     using IC = ItemCfg<D>;
     constexpr int S = IC::kStages;
@@ -920,7 +921,7 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
     ItemBarriers* bars = reinterpret_cast<ItemBarriers*>(smem + IC::kData);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int32_t N = P.N, max_kv = P.max_kv, nKB = P.n_kv / 128;
+    const int32_t N = P.N, max_kv = P.max_kv, nKB = kGeom ? P.n_kv / 128 : P.nQB;
     // wave w takes item w * G + b, or w * G + G - 1 - b on odd waves (zig-zag)
     const int64_t G = gridDim.x;
     auto item_of = [&](int64_t w) -> int64_t {
@@ -951,11 +952,13 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
     if (warp == kProducerWarp && lane == 0) {
         prefetch_tensormap(&P.map_k);
         prefetch_tensormap(&P.map_v);
-        prefetch_tensormap(&P.map_ki);
-        prefetch_tensormap(&P.map_vi);
-        if (P.geo.nt > 0 || P.geo.scatter) {
-            prefetch_tensormap(&P.map_kg);
-            prefetch_tensormap(&P.map_vg);
+        if constexpr (kGeom) {
+            prefetch_tensormap(&P.map_ki);
+            prefetch_tensormap(&P.map_vi);
+            if (P.geo.nt > 0 || P.geo.scatter) {
+                prefetch_tensormap(&P.map_kg);
+                prefetch_tensormap(&P.map_vg);
+            }
         }
     }
     tc_fence_before();
@@ -984,7 +987,9 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
                     ok = false;
                 if (ok) {
                     mbar_arrive_expect_tx(smem_u32(&bars->q_full[qbuf]), C::kTile);
-                    geo_load_q(P, s_q + qbuf * C::kTile, smem_u32(&bars->q_full[qbuf]), it.bh, it.qb);
+                    if constexpr (kGeom) geo_load_q(P, s_q + qbuf * C::kTile, smem_u32(&bars->q_full[qbuf]), it.bh, it.qb);
+                    else tma_load_3d(s_q + qbuf * C::kTile, &P.map_q, 0, (int32_t)(it.bh * N) + it.qb * 128, 0,
+                                     smem_u32(&bars->q_full[qbuf]));
                 }
             }
             ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
@@ -1025,7 +1030,9 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
                 if (lane == 0) {
                     const uint32_t fb = smem_u32(&bars->full[slot]);
                     mbar_arrive_expect_tx(fb, C::kTile);
-                    geo_load_kv(P, s_ring + slot * C::kTile, fb, is_v, it.bh_kv, kb);
+                    if constexpr (kGeom) geo_load_kv(P, s_ring + slot * C::kTile, fb, is_v, it.bh_kv, kb);
+                    else tma_load_3d(s_ring + slot * C::kTile, is_v ? &P.map_v : &P.map_k, 0,
+                                     (int32_t)(it.bh_kv * N) + kb * 128, 0, fb);
                 }
                 issued = pos + 1;
             }
@@ -1131,7 +1138,7 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
             Item it;
             if (!decode_item(P, f, it)) continue;
             const int32_t n = it.n;
-            const int32_t tok = g0::query_token(P.geo, it.qb * 128 + r);
+            const int32_t tok = kGeom ? g0::query_token(P.geo, it.qb * 128 + r) : it.qb * 128 + r;
             __nv_bfloat16* orow = P.o + (it.bh * N + tok) * D;
             if (n == 0) {
                 const uint4 z = make_uint4(0, 0, 0, 0);
@@ -1142,6 +1149,7 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
             }
             const float* lw_row = P.log_w ? P.log_w + it.row * max_kv : nullptr;
             const uint8_t* qm_row = (kQuad && P.quad_mask != nullptr) ? P.quad_mask + it.row * max_kv : nullptr;
+            const int32_t* list = P.kv_idx + it.row * max_kv;
             float m = -INFINITY, l = 0.0f;
             float lw_next = lw_row ? lw_row[0] : 0.0f;
             uint32_t qm_chunk = 0xFu;
@@ -1155,6 +1163,32 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
                 const uint32_t sbuf = (gb % kSBuf) * 128u;
                 bool hidden = false;  // warp-uniform: no row of this warp sees block j
                 if constexpr (kQuad) hidden = ((__shfl_sync(0xffffffffu, qm_chunk, j & 31) >> qd) & 1u) == 0u;
+                // Token mask of block j (contiguous keys 128 kb ..): visibility
+                // words from at most two runs, built before S_j arrives
+                bool need_mask = false;
+                uint32_t vis_w[4] = {~0u, ~0u, ~0u, ~0u};
+                if (kMask && !kGeom) {
+                    int32_t kb = list[j];
+                    kb = (kb < 0 || kb >= nKB) ? 0 : kb;  // flagged by the producer
+                    const int32_t kbase = kb * 128, kmax = kbase + 127;
+                    need_mask = kmax >= P.n_valid || (P.causal && kmax > tok) ||
+                                (P.window > 0 && kbase <= tok - P.window && kmax >= P.sinks);
+                    if (__any_sync(0xffffffffu, need_mask)) {
+                        const int32_t hi_g = P.causal ? min(P.n_valid, tok + 1) : P.n_valid;
+                        int32_t a1 = -kbase, a2 = 0, b2 = 0;
+                        if (P.window > 0) {
+                            a1 = tok - P.window + 1 - kbase;
+                            a2 = -kbase;
+                            b2 = min(P.sinks, hi_g) - kbase;
+                        }
+                        const int32_t b1 = hi_g - kbase;
+#pragma unroll
+                        for (int x = 0; x < 4; ++x)
+                            vis_w[x] = run_bits(a1 - 32 * x, b1 - 32 * x) | run_bits(a2 - 32 * x, b2 - 32 * x);
+                    } else {
+                        need_mask = false;
+                    }
+                }
                 const uint32_t pk = t_glob + (uint32_t)ring_pos_k(j);
                 bool wt = mbar_wait(smem_u32(&bars->empty[pk % S]), (pk / S) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
                 if (__any_sync(0xffffffffu, !wt || items_aborted(bars))) {
@@ -1180,6 +1214,13 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
                 tmem_ld32(t_lane + sbuf + 64, &s[64]);
                 tmem_ld32(t_lane + sbuf + 96, &s[96]);
                 tmem_wait_ld();
+                if constexpr (kMask && !kGeom) {
+                    if (__any_sync(0xffffffffu, need_mask)) {
+                        const uint32_t ninf = __float_as_uint(-INFINITY);
+#pragma unroll
+                        for (int c = 0; c < 128; ++c) s[c] = ((vis_w[c >> 5] >> (c & 31)) & 1u) ? s[c] : ninf;
+                    }
+                }
                 float mx0 = __uint_as_float(s[0]), mx1 = __uint_as_float(s[1]);
                 float mx2 = __uint_as_float(s[2]), mx3 = __uint_as_float(s[3]);
 #pragma unroll
@@ -1196,11 +1237,13 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
                     m = mt;
                 } else if (rescale) {
                     const float m_new = fmaxf(m, mt);
-                    alpha = (kQuad && m == -INFINITY) ? 0.0f : ex2(m - m_new);
+                    // a row with every key so far dropped has l = 0 and O = 0
+                    alpha = (kMask && m == -INFINITY) ? 0.0f : ex2(m - m_new);
                     l *= alpha;
                     m = m_new;
                 }
-                const float bias = lw2 - ((kQuad && m == -INFINITY) ? 0.0f : m);
+                // a row with every key so far dropped keeps m = -inf (avoid -inf - -inf)
+                const float bias = lw2 - ((kMask && m == -INFINITY) ? 0.0f : m);
                 float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
                 for (int c = 0; c < 128; c += 4) {
@@ -1354,14 +1397,33 @@ int items_setting() {
     return v;
 }
 
-template <int D, bool kQuad>
+// Per-item blocks on the tile path pay off for short rows only (a wave of
+// long rows keeps every SM busy on its own, and the per-item kernel's ring
+// is one slot shorter).  A sliding window bounds a row by construction: with
+// only blocks that hold a visible key listed, a row has at most
+// (window + 254) / 128 window blocks plus the sink blocks.  BSA_ITEMS_TILE=<0|1>
+// forces the choice (tuning, comparisons).
+constexpr int32_t kShortRowBlocks = 16;
+bool items_tile_choice(const ForwardArgs& a) {
+    static int v = -2;
+    if (v == -2) {
+        const char* s = getenv("BSA_ITEMS_TILE");
+        v = (s && (s[0] == '0' || s[0] == '1') && s[1] == 0) ? s[0] - '0' : -1;
+    }
+    if (v >= 0) return v == 1;
+    if (!a.masked || a.window <= 0) return false;
+    const int64_t bound = ((int64_t)a.window + 254) / 128 + ((int64_t)a.sinks + 127) / 128;
+    return bound <= kShortRowBlocks;
+}
+
+template <int D, bool kMask, bool kGeom, bool kQuad>
 bsa_status launch_items(const Params& P, int64_t n_items, cudaStream_t stream) {
     const size_t smem = 1024 + ItemCfg<D>::kData + sizeof(ItemBarriers);
     static int done[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
     if (dev >= 64 || !done[dev]) {
-        if (cudaFuncSetAttribute(k_bsa_forward_items<D, kDefaultPoly, kQuad>,
+        if (cudaFuncSetAttribute(k_bsa_forward_items<D, kDefaultPoly, kMask, kGeom, kQuad>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return BSA_ERR_CUDA;
         if (dev < 64) done[dev] = 1;
@@ -1369,7 +1431,7 @@ bsa_status launch_items(const Params& P, int64_t n_items, cudaStream_t stream) {
     const int32_t resident = forward_resident_ctas(D);
     if (resident <= 0) return BSA_ERR_CUDA;
     const unsigned grid = (unsigned)(n_items < resident ? n_items : resident);
-    k_bsa_forward_items<D, kDefaultPoly, kQuad><<<grid, 192, smem, stream>>>(P, n_items);
+    k_bsa_forward_items<D, kDefaultPoly, kMask, kGeom, kQuad><<<grid, 192, smem, stream>>>(P, n_items);
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
@@ -1444,7 +1506,7 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
             ok = encode_image_map(&P.map_kg, a.k, kh, a.N, D, g, true, 0, 0) &&
                  encode_image_map(&P.map_vg, a.v, kh, a.N, D, g, true, 0, 0);
         if (!ok) return BSA_ERR_CUDA;
-        if (items_setting()) return launch_items<D, true>(P, (int64_t)gx * gy, stream);
+        if (items_setting()) return launch_items<D, true, true, true>(P, (int64_t)gx * gy, stream);
         return launch_dp<D, kDefaultPoly, false, false, true, true, true>(P, gx, gy, stream);
     }
     if (a.scatter_R > 0) {
@@ -1460,7 +1522,7 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
              encode_image_map(&P.map_kg, a.k, kh, a.N, D, g, true, 0, 0) &&
              encode_image_map(&P.map_vg, a.v, kh, a.N, D, g, true, 0, 0);
         if (!ok) return BSA_ERR_CUDA;
-        if (items_setting()) return launch_items<D, false>(P, (int64_t)gx * gy, stream);
+        if (items_setting()) return launch_items<D, false, true, false>(P, (int64_t)gx * gy, stream);
         return launch_dp<D, kDefaultPoly, false, false, false, true, false>(P, gx, gy, stream);
     }
     const bool crm = a.crm != nullptr, gather = a.kv_map != nullptr;
@@ -1469,9 +1531,13 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
         if (gather && P.quad_mask != nullptr)
             return launch_dp<D, kDefaultPoly, false, true, true, false, true>(P, gx, gy, stream);
         if (P.quad_mask != nullptr) return BSA_ERR_UNSUPPORTED;  // packed tiles need kv_map
+        if (!gather && P.q_map == nullptr && items_tile_choice(a))
+            return launch_items<D, true, false, false>(P, (int64_t)gx * gy, stream);
         return gather ? launch_dp<D, kDefaultPoly, false, true, true>(P, gx, gy, stream)
                       : launch_dp<D, kDefaultPoly, false, false, true>(P, gx, gy, stream);
     }
+    if (!gather && !crm && P.q_map == nullptr && items_tile_choice(a))
+        return launch_items<D, false, false, false>(P, (int64_t)gx * gy, stream);
     if (gather)
         return crm ? launch_dp<D, kDefaultPoly, true, true>(P, gx, gy, stream)
                    : launch_dp<D, kDefaultPoly, false, true>(P, gx, gy, stream);
