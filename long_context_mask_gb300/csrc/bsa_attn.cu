@@ -902,22 +902,26 @@ __device__ __forceinline__ void items_set_abort(ItemBarriers* b, int32_t* status
     raise_status(status, BSA_ERR_TIMEOUT);
 }
 
-template <int D>
+// kQB Q buffers: two let the next row's Q load while the current row's
+// products still read its Q, at the cost of one ring slot; with one, the next
+// Q loads once the current row's last QK has run (the PVs do not read Q).
+template <int D, int kQB>
 struct ItemCfg {
-    static constexpr int kStages = Cfg<D>::kStages - 1;  // room for the second Q tile
-    static constexpr int kData = Cfg<D>::kTile * (2 + kStages);
+    static constexpr int kStages = Cfg<D>::kStages + 1 - kQB;
+    static constexpr int kData = Cfg<D>::kTile * (kQB + kStages);
 };
 
-template <int D, int kPoly, bool kMask, bool kGeom, bool kQuad>
+template <int D, int kPoly, bool kMask, bool kGeom, bool kQuad, int kQB>
 __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_constant__ Params P, int64_t n_items) {
     static_assert(!kQuad || kMask, "quadrant masks live in the masked variant");
+    static_assert(kQB == 1 || kQB == 2, "one or two Q buffers");
     using C = Cfg<D>;
-    using IC = ItemCfg<D>;
+    using IC = ItemCfg<D, kQB>;
     constexpr int S = IC::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s_q = smem_u32(smem);  // two Q buffers, then the K/V ring
-    const uint32_t s_ring = s_q + 2 * C::kTile;
+    const uint32_t s_ring = s_q + kQB * C::kTile;
     ItemBarriers* bars = reinterpret_cast<ItemBarriers*>(smem + IC::kData);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -979,11 +983,11 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
             const int32_t n = it.n;
             if (n == 0) continue;
             const int32_t* list = P.kv_idx + it.row * max_kv;
-            const uint32_t qbuf = qi & 1u;
+            const uint32_t qbuf = qi % kQB;
             if (lane == 0) {
                 // the buffer's previous item must be done with it
-                if (qi >= 2 && !mbar_wait(smem_u32(&bars->q_empty[qbuf]), ((qi >> 1) - 1u) & 1u, kWaitNs, P.status,
-                                          BSA_ERR_TIMEOUT))
+                if (qi >= (uint32_t)kQB && !mbar_wait(smem_u32(&bars->q_empty[qbuf]), (qi / kQB - 1u) & 1u, kWaitNs,
+                                                      P.status, BSA_ERR_TIMEOUT))
                     ok = false;
                 if (ok) {
                     mbar_arrive_expect_tx(smem_u32(&bars->q_full[qbuf]), C::kTile);
@@ -995,18 +999,28 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
             ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
             if (!ok) break;
             q_issued = qi + 1;
-            // tiles in MMA consumption order: K_0 .. K_2, then V_i, K_{i+3}, then the last V
-            int32_t chunk_base = -64, kb_lane = 0;
-            auto block_kb = [&](int32_t e) -> int32_t {
-                if (e - chunk_base >= 32 || e < chunk_base) {
-                    chunk_base = e & ~31;
-                    kb_lane = chunk_base + lane < n ? list[chunk_base + lane] : 0;
-                    if (kb_lane < 0 || kb_lane >= nKB) {
-                        raise_status(P.status, BSA_ERR_BOUNDS);
-                        kb_lane = 0;
-                    }
+            // tiles in MMA consumption order: K_0 .. K_2, then V_i, K_{i+3}, then the last V.
+            // The K and V streams each walk the list in increasing order through
+            // their own 32-entry window, with the next window already loaded
+            // (lane e holds entry base + e): every entry is read once, about 32
+            // tiles before it is needed.
+            auto fetch = [&](int32_t e) -> int32_t {
+                int32_t kb = e < n ? list[e] : 0;
+                if (kb < 0 || kb >= nKB) {
+                    raise_status(P.status, BSA_ERR_BOUNDS);
+                    kb = 0;  // keeps the pipeline in step; this row's result is unspecified
                 }
-                return __shfl_sync(0xffffffffu, kb_lane, e - chunk_base);
+                return kb;
+            };
+            int32_t k_base = 0, k_cur = fetch(lane), k_nxt = fetch(32 + lane);
+            int32_t v_base = 0, v_cur = k_cur, v_nxt = k_nxt;
+            auto stream_kb = [&](int32_t e, int32_t& base, int32_t& cur, int32_t& nxt) -> int32_t {
+                while (e >= base + 32) {
+                    base += 32;
+                    cur = nxt;
+                    nxt = fetch(base + 32 + lane);
+                }
+                return __shfl_sync(0xffffffffu, cur, e - base);
             };
             const int32_t lead = n < kSBuf ? n : kSBuf;
             const int32_t inter = 2 * (n - lead);
@@ -1016,7 +1030,7 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
                 if (t < lead) e = t;
                 else if (t - lead < inter) e = ((t - lead) >> 1) + (is_v ? 0 : kSBuf);
                 else e = (n - lead) + (t - lead - inter);
-                const int32_t kb = block_kb(e);
+                const int32_t kb = is_v ? stream_kb(e, v_base, v_cur, v_nxt) : stream_kb(e, k_base, k_cur, k_nxt);
                 const uint32_t pos = t_glob + (uint32_t)t;
                 const uint32_t slot = pos % S;
                 int wt = 1;
@@ -1044,8 +1058,8 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
         // Drain: every issued copy must land before the block exits (older
         // copies were consumed before their buffers were reused).
         if (lane == 0) {
-            for (uint32_t q = q_issued > 2 ? q_issued - 2 : 0; q < q_issued; ++q)
-                if (!mbar_wait(smem_u32(&bars->q_full[q & 1u]), (q >> 1) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT))
+            for (uint32_t q = q_issued > (uint32_t)kQB ? q_issued - kQB : 0; q < q_issued; ++q)
+                if (!mbar_wait(smem_u32(&bars->q_full[q % kQB]), (q / kQB) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT))
                     raise_status(P.status, BSA_ERR_TIMEOUT);
             const uint32_t first = issued > (uint32_t)S ? issued - S : 0;
             for (uint32_t i = first; i < issued; ++i)
@@ -1066,8 +1080,8 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
                 Item it;
                 if (!decode_item(P, f, it) || it.n == 0) continue;
                 const int32_t n = it.n;
-                const uint32_t qbuf = qi & 1u;
-                ok = mbar_wait(smem_u32(&bars->q_full[qbuf]), (qi >> 1) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                const uint32_t qbuf = qi % kQB;
+                ok = mbar_wait(smem_u32(&bars->q_full[qbuf]), (qi / kQB) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t dq = smem_desc_sw128(s_q + qbuf * C::kTile, 16, 1024);
@@ -1084,6 +1098,8 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
                         mma_ss(tmem + d_col, dq + off, ks + off, C::kIdescQK, kk > 0 ? 1u : 0u);
                     }
                     mma_commit(smem_u32(&bars->empty[slot]));  // also signals S_j to the softmax
+                    // one Q buffer: free once the row's last QK has run
+                    if (kQB == 1 && j == n - 1) mma_commit(smem_u32(&bars->q_empty[0]));
                     ++pos;
                     return true;
                 };
@@ -1113,7 +1129,7 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
                     if (i + kSBuf < n) ok = issue_qk(i + kSBuf);
                 }
                 if (!ok) break;
-                mma_commit(smem_u32(&bars->q_empty[qbuf]));  // this item's Q buffer, once its MMAs ran
+                if (kQB == 2) mma_commit(smem_u32(&bars->q_empty[qbuf]));  // this item's Q buffer, once its MMAs ran
                 g_glob += (uint32_t)n;
                 ++qi;
             }
@@ -1301,21 +1317,43 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
                 }
             }
             tc_fence_after();
-            uint32_t o[D];
-#pragma unroll
-            for (int c = 0; c < D; c += 32) tmem_ld32(t_lane + kColO + c, &o[c]);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bars->o_free));
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;  // l = 0: every key dropped
+            if constexpr (kQB == 2) {
+                // short rows: read all of O, hand the accumulator over, then store
+                uint32_t o[D];
 #pragma unroll
-            for (int c = 0; c < D; c += 8) {
-                uint4 v4;
-                v4.x = pack_bf16(__uint_as_float(o[c + 0]) * inv_l, __uint_as_float(o[c + 1]) * inv_l);
-                v4.y = pack_bf16(__uint_as_float(o[c + 2]) * inv_l, __uint_as_float(o[c + 3]) * inv_l);
-                v4.z = pack_bf16(__uint_as_float(o[c + 4]) * inv_l, __uint_as_float(o[c + 5]) * inv_l);
-                v4.w = pack_bf16(__uint_as_float(o[c + 6]) * inv_l, __uint_as_float(o[c + 7]) * inv_l);
-                *reinterpret_cast<uint4*>(orow + c) = v4;
+                for (int c = 0; c < D; c += 32) tmem_ld32(t_lane + kColO + c, &o[c]);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars->o_free));
+#pragma unroll
+                for (int c = 0; c < D; c += 8) {
+                    uint4 v4;
+                    v4.x = pack_bf16(__uint_as_float(o[c + 0]) * inv_l, __uint_as_float(o[c + 1]) * inv_l);
+                    v4.y = pack_bf16(__uint_as_float(o[c + 2]) * inv_l, __uint_as_float(o[c + 3]) * inv_l);
+                    v4.z = pack_bf16(__uint_as_float(o[c + 4]) * inv_l, __uint_as_float(o[c + 5]) * inv_l);
+                    v4.w = pack_bf16(__uint_as_float(o[c + 6]) * inv_l, __uint_as_float(o[c + 7]) * inv_l);
+                    *reinterpret_cast<uint4*>(orow + c) = v4;
+                }
+            } else {
+                // 32 columns at a time (fewer live registers), then the hand-over
+#pragma unroll
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(t_lane + kColO + c, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        uint4 v4;
+                        v4.x = pack_bf16(__uint_as_float(o[i + 0]) * inv_l, __uint_as_float(o[i + 1]) * inv_l);
+                        v4.y = pack_bf16(__uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
+                        v4.z = pack_bf16(__uint_as_float(o[i + 4]) * inv_l, __uint_as_float(o[i + 5]) * inv_l);
+                        v4.w = pack_bf16(__uint_as_float(o[i + 6]) * inv_l, __uint_as_float(o[i + 7]) * inv_l);
+                        *reinterpret_cast<uint4*>(orow + c + i) = v4;
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars->o_free));
             }
             P.lse[it.bh * N + tok] = l > 0.0f ? (m + log2f(l)) * kLn2 : -INFINITY;
             t_glob += 2u * (uint32_t)n;
@@ -1416,14 +1454,14 @@ bool items_tile_choice(const ForwardArgs& a) {
     return bound <= kShortRowBlocks;
 }
 
-template <int D, bool kMask, bool kGeom, bool kQuad>
+template <int D, bool kMask, bool kGeom, bool kQuad, int kQB>
 bsa_status launch_items(const Params& P, int64_t n_items, cudaStream_t stream) {
-    const size_t smem = 1024 + ItemCfg<D>::kData + sizeof(ItemBarriers);
+    const size_t smem = 1024 + ItemCfg<D, kQB>::kData + sizeof(ItemBarriers);
     static int done[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return BSA_ERR_CUDA;
     if (dev >= 64 || !done[dev]) {
-        if (cudaFuncSetAttribute(k_bsa_forward_items<D, kDefaultPoly, kMask, kGeom, kQuad>,
+        if (cudaFuncSetAttribute(k_bsa_forward_items<D, kDefaultPoly, kMask, kGeom, kQuad, kQB>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return BSA_ERR_CUDA;
         if (dev < 64) done[dev] = 1;
@@ -1431,7 +1469,7 @@ bsa_status launch_items(const Params& P, int64_t n_items, cudaStream_t stream) {
     const int32_t resident = forward_resident_ctas(D);
     if (resident <= 0) return BSA_ERR_CUDA;
     const unsigned grid = (unsigned)(n_items < resident ? n_items : resident);
-    k_bsa_forward_items<D, kDefaultPoly, kMask, kGeom, kQuad><<<grid, 192, smem, stream>>>(P, n_items);
+    k_bsa_forward_items<D, kDefaultPoly, kMask, kGeom, kQuad, kQB><<<grid, 192, smem, stream>>>(P, n_items);
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
@@ -1506,7 +1544,7 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
             ok = encode_image_map(&P.map_kg, a.k, kh, a.N, D, g, true, 0, 0) &&
                  encode_image_map(&P.map_vg, a.v, kh, a.N, D, g, true, 0, 0);
         if (!ok) return BSA_ERR_CUDA;
-        if (items_setting()) return launch_items<D, true, true, true>(P, (int64_t)gx * gy, stream);
+        if (items_setting()) return launch_items<D, true, true, true, 2>(P, (int64_t)gx * gy, stream);
         return launch_dp<D, kDefaultPoly, false, false, true, true, true>(P, gx, gy, stream);
     }
     if (a.scatter_R > 0) {
@@ -1522,7 +1560,7 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
              encode_image_map(&P.map_kg, a.k, kh, a.N, D, g, true, 0, 0) &&
              encode_image_map(&P.map_vg, a.v, kh, a.N, D, g, true, 0, 0);
         if (!ok) return BSA_ERR_CUDA;
-        if (items_setting()) return launch_items<D, false, true, false>(P, (int64_t)gx * gy, stream);
+        if (items_setting()) return launch_items<D, false, true, false, 2>(P, (int64_t)gx * gy, stream);
         return launch_dp<D, kDefaultPoly, false, false, false, true, false>(P, gx, gy, stream);
     }
     const bool crm = a.crm != nullptr, gather = a.kv_map != nullptr;
@@ -1532,12 +1570,12 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
             return launch_dp<D, kDefaultPoly, false, true, true, false, true>(P, gx, gy, stream);
         if (P.quad_mask != nullptr) return BSA_ERR_UNSUPPORTED;  // packed tiles need kv_map
         if (!gather && P.q_map == nullptr && items_tile_choice(a))
-            return launch_items<D, true, false, false>(P, (int64_t)gx * gy, stream);
+            return launch_items<D, true, false, false, 1>(P, (int64_t)gx * gy, stream);
         return gather ? launch_dp<D, kDefaultPoly, false, true, true>(P, gx, gy, stream)
                       : launch_dp<D, kDefaultPoly, false, false, true>(P, gx, gy, stream);
     }
     if (!gather && !crm && P.q_map == nullptr && items_tile_choice(a))
-        return launch_items<D, false, false, false>(P, (int64_t)gx * gy, stream);
+        return launch_items<D, false, false, false, 1>(P, (int64_t)gx * gy, stream);
     if (gather)
         return crm ? launch_dp<D, kDefaultPoly, true, true>(P, gx, gy, stream)
                    : launch_dp<D, kDefaultPoly, false, true>(P, gx, gy, stream);
