@@ -521,58 +521,71 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            // descriptors of the K-major Q tile and of ring slot 0; a slot / k-step
-            // offset is added to the start-address field (bits 0..13, 16-byte units)
-            const uint64_t dq = smem_desc_sw128(s_q, 16, 1024);
-            const uint64_t dk = smem_desc_sw128(s_ring, 16, 1024);
-            const uint64_t dv = smem_desc_sw128(s_ring, C::kBoxBytes, 1024);
-            bool ok = mbar_wait(smem_u32(&bars->q_full), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT);
-            if (P.q_map != nullptr) fence_proxy_async_smem();  // Q rows written by cp.async
+        // The whole warp walks the schedule, so that its control flow and the
+        // descriptor / tensor-memory address arithmetic stay warp-uniform; one
+        // elected lane issues each group of MMAs and its commit.
+        // descriptors of the K-major Q tile and of ring slot 0; a slot / k-step
+        // offset is added to the start-address field (bits 0..13, 16-byte units)
+        const uint64_t dq = smem_desc_sw128(s_q, 16, 1024);
+        const uint64_t dk = smem_desc_sw128(s_ring, 16, 1024);
+        const uint64_t dv = smem_desc_sw128(s_ring, C::kBoxBytes, 1024);
+        bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->q_full), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT));
+        if (P.q_map != nullptr) fence_proxy_async_smem();  // Q rows written by cp.async
+        tc_fence_after();
+        int32_t item = 0;  // ring position of the next tile (same order as the producer)
+        auto issue_qk = [&](int32_t j) -> bool {
+            const int32_t slot = item % C::kStages;
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[slot]), (uint32_t)(item / C::kStages) & 1u,
+                                                   kWaitNs, P.status, BSA_ERR_TIMEOUT)))
+                return false;
+            if constexpr (kGather) fence_proxy_async_smem();  // rows written by cp.async
             tc_fence_after();
-            int32_t item = 0;  // ring position of the next tile (same order as the producer)
-            auto issue_qk = [&](int32_t j) -> bool {
-                const int32_t slot = item % C::kStages;
-                if (!mbar_wait(smem_u32(&bars->full[slot]), (uint32_t)(item / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT)) return false;
-                if constexpr (kGather) fence_proxy_async_smem();  // rows written by cp.async
-                tc_fence_after();
-                const uint64_t ks = dk + (uint64_t)((slot * C::kTile) >> 4);
-                const uint32_t d_col = (uint32_t)(j % kSBuf) * 128u;
+            const uint64_t ks = dk + (uint64_t)((slot * C::kTile) >> 4);
+            const uint32_t d_col = (uint32_t)(j % kSBuf) * 128u;
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
                     mma_ss(tmem + d_col, dq + off, ks + off, C::kIdescQK, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(smem_u32(&bars->empty[slot]));  // also signals S_j to the softmax
-                ++item;
-                return true;
-            };
-            for (int32_t j = 0; ok && j < n && j < kSBuf; ++j) ok = issue_qk(j);
-            for (int32_t i = 0; ok && i < n; ++i) {
-                // O += P_i V_i once the softmax has written P_i (and rescaled O)
-                ok = mbar_wait(smem_u32(&bars->p_full[i % kSBuf]), (uint32_t)(i / kSBuf) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
-                if (!ok) break;
-                const int32_t slot = item % C::kStages;
-                ok = mbar_wait(smem_u32(&bars->full[slot]), (uint32_t)(item / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
-                if (!ok) break;
-                if constexpr (kGather) fence_proxy_async_smem();
-                tc_fence_after();
-                const uint64_t vs = dv + (uint64_t)((slot * C::kTile) >> 4);
-                const uint32_t p_col = (uint32_t)(i % kSBuf) * 128u;
+            }
+            __syncwarp();
+            ++item;
+            return true;
+        };
+        for (int32_t j = 0; ok && j < n && j < kSBuf; ++j) ok = issue_qk(j);
+        for (int32_t i = 0; ok && i < n; ++i) {
+            // O += P_i V_i once the softmax has written P_i (and rescaled O)
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->p_full[i % kSBuf]), (uint32_t)(i / kSBuf) & 1u,
+                                                   kWaitNs, P.status, BSA_ERR_TIMEOUT));
+            if (!ok) break;
+            const int32_t slot = item % C::kStages;
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->full[slot]), (uint32_t)(item / C::kStages) & 1u,
+                                                   kWaitNs, P.status, BSA_ERR_TIMEOUT));
+            if (!ok) break;
+            if constexpr (kGather) fence_proxy_async_smem();
+            tc_fence_after();
+            const uint64_t vs = dv + (uint64_t)((slot * C::kTile) >> 4);
+            const uint32_t p_col = (uint32_t)(i % kSBuf) * 128u;
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ts(tmem + kColO, tmem + p_col + kk * 8, vs + (uint64_t)(kk * 2048 >> 4),
                            C::kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(smem_u32(&bars->empty[slot]));  // also signals PV_i to the softmax
-                ++item;
-                // S buffer i % 3 is free again once PV_i (issued above) has read P_i
-                if (i + kSBuf < n) ok = issue_qk(i + kSBuf);
             }
-            if (!ok) set_abort(bars, P.status);
-            // Drain: nothing of ours may still be running when TMEM is freed.
-            mma_commit(smem_u32(&bars->mma_done));
-            if (!mbar_wait(smem_u32(&bars->mma_done), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT)) raise_status(P.status, BSA_ERR_TIMEOUT);
+            __syncwarp();
+            ++item;
+            // S buffer i % 3 is free again once PV_i (issued above) has read P_i
+            if (i + kSBuf < n) ok = issue_qk(i + kSBuf);
         }
+        if (!ok && lane == 0) set_abort(bars, P.status);
+        // Drain: nothing of ours may still be running when TMEM is freed.
+        if (elect_one()) mma_commit(smem_u32(&bars->mma_done));
+        __syncwarp();
+        if (!mbar_wait(smem_u32(&bars->mma_done), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT) && lane == 0)
+            raise_status(P.status, BSA_ERR_TIMEOUT);
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax + epilogue
