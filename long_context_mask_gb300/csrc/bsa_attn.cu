@@ -1082,29 +1082,33 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint64_t dk = smem_desc_sw128(s_ring, 16, 1024);
-            const uint64_t dv = smem_desc_sw128(s_ring, C::kBoxBytes, 1024);
-            uint32_t pos = 0, g_glob = 0, qi = 0;  // ring position, score buffer count, items
-            bool ok = true;
-            for (int64_t w = 0; ok; ++w) {
-                const int64_t f = item_of(w);
-                if (f >= n_items) break;
-                Item it;
-                if (!decode_item(P, f, it) || it.n == 0) continue;
-                const int32_t n = it.n;
-                const uint32_t qbuf = qi % kQB;
-                ok = mbar_wait(smem_u32(&bars->q_full[qbuf]), (qi / kQB) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
-                if (!ok) break;
+        // The whole warp walks the items (warp-uniform control flow and
+        // descriptor arithmetic); one elected lane issues each MMA group.
+        const uint64_t dk = smem_desc_sw128(s_ring, 16, 1024);
+        const uint64_t dv = smem_desc_sw128(s_ring, C::kBoxBytes, 1024);
+        uint32_t pos = 0, g_glob = 0, qi = 0;  // ring position, score buffer count, items
+        bool ok = true;
+        auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity, kWaitNs, P.status, BSA_ERR_TIMEOUT));
+        };
+        for (int64_t w = 0; ok; ++w) {
+            const int64_t f = item_of(w);
+            if (f >= n_items) break;
+            Item it;
+            if (!decode_item(P, f, it) || it.n == 0) continue;
+            const int32_t n = it.n;
+            const uint32_t qbuf = qi % kQB;
+            ok = wait_all(smem_u32(&bars->q_full[qbuf]), (qi / kQB) & 1u);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t dq = smem_desc_sw128(s_q + qbuf * C::kTile, 16, 1024);
+            auto issue_qk = [&](int32_t j) -> bool {
+                const uint32_t slot = pos % S;
+                if (!wait_all(smem_u32(&bars->full[slot]), (pos / S) & 1u)) return false;
                 tc_fence_after();
-                const uint64_t dq = smem_desc_sw128(s_q + qbuf * C::kTile, 16, 1024);
-                auto issue_qk = [&](int32_t j) -> bool {
-                    const uint32_t slot = pos % S;
-                    if (!mbar_wait(smem_u32(&bars->full[slot]), (pos / S) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT))
-                        return false;
-                    tc_fence_after();
-                    const uint64_t ks = dk + (uint64_t)((slot * C::kTile) >> 4);
-                    const uint32_t d_col = ((g_glob + (uint32_t)j) % kSBuf) * 128u;
+                const uint64_t ks = dk + (uint64_t)((slot * C::kTile) >> 4);
+                const uint32_t d_col = ((g_glob + (uint32_t)j) % kSBuf) * 128u;
+                if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
@@ -1113,45 +1117,51 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
                     mma_commit(smem_u32(&bars->empty[slot]));  // also signals S_j to the softmax
                     // one Q buffer: free once the row's last QK has run
                     if (kQB == 1 && j == n - 1) mma_commit(smem_u32(&bars->q_empty[0]));
-                    ++pos;
-                    return true;
-                };
-                for (int32_t j = 0; ok && j < n && j < kSBuf; ++j) ok = issue_qk(j);
-                for (int32_t i = 0; ok && i < n; ++i) {
-                    const uint32_t gb = g_glob + (uint32_t)i;
-                    ok = mbar_wait(smem_u32(&bars->p_full[gb % kSBuf]), (gb / kSBuf) & 1u, kWaitNs, P.status,
-                                   BSA_ERR_TIMEOUT);
-                    // the first PV of an item overwrites O: the previous item's
-                    // epilogue must have read it out
-                    if (ok && i == 0 && qi > 0)
-                        ok = mbar_wait(smem_u32(&bars->o_free), (qi - 1u) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
-                    if (!ok) break;
-                    const uint32_t slot = pos % S;
-                    ok = mbar_wait(smem_u32(&bars->full[slot]), (pos / S) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint64_t vs = dv + (uint64_t)((slot * C::kTile) >> 4);
-                    const uint32_t p_col = (gb % kSBuf) * 128u;
+                }
+                __syncwarp();
+                ++pos;
+                return true;
+            };
+            for (int32_t j = 0; ok && j < n && j < kSBuf; ++j) ok = issue_qk(j);
+            for (int32_t i = 0; ok && i < n; ++i) {
+                const uint32_t gb = g_glob + (uint32_t)i;
+                ok = wait_all(smem_u32(&bars->p_full[gb % kSBuf]), (gb / kSBuf) & 1u);
+                // the first PV of an item overwrites O: the previous item's
+                // epilogue must have read it out
+                if (ok && i == 0 && qi > 0) ok = wait_all(smem_u32(&bars->o_free), (qi - 1u) & 1u);
+                if (!ok) break;
+                const uint32_t slot = pos % S;
+                ok = wait_all(smem_u32(&bars->full[slot]), (pos / S) & 1u);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t vs = dv + (uint64_t)((slot * C::kTile) >> 4);
+                const uint32_t p_col = (gb % kSBuf) * 128u;
+                if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         mma_ts(tmem + kColO, tmem + p_col + kk * 8, vs + (uint64_t)(kk * 2048 >> 4), C::kIdescPV,
                                (i > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(smem_u32(&bars->empty[slot]));  // also signals PV_i to the softmax
-                    ++pos;
-                    // score buffer gb % 3 is free again once PV_i (issued above) has read P
-                    if (i + kSBuf < n) ok = issue_qk(i + kSBuf);
                 }
-                if (!ok) break;
-                if (kQB == 2) mma_commit(smem_u32(&bars->q_empty[qbuf]));  // this item's Q buffer, once its MMAs ran
-                g_glob += (uint32_t)n;
-                ++qi;
+                __syncwarp();
+                ++pos;
+                // score buffer gb % 3 is free again once PV_i (issued above) has read P
+                if (i + kSBuf < n) ok = issue_qk(i + kSBuf);
             }
-            if (!ok) items_set_abort(bars, P.status);
-            // Drain: nothing of ours may still be running when TMEM is freed.
-            mma_commit(smem_u32(&bars->mma_done));
-            if (!mbar_wait(smem_u32(&bars->mma_done), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT))
-                raise_status(P.status, BSA_ERR_TIMEOUT);
+            if (!ok) break;
+            if (kQB == 2) {
+                if (elect_one()) mma_commit(smem_u32(&bars->q_empty[qbuf]));  // once this item's MMAs ran
+                __syncwarp();
+            }
+            g_glob += (uint32_t)n;
+            ++qi;
         }
+        if (!ok && lane == 0) items_set_abort(bars, P.status);
+        // Drain: nothing of ours may still be running when TMEM is freed.
+        if (elect_one()) mma_commit(smem_u32(&bars->mma_done));
+        __syncwarp();
+        if (!mbar_wait(smem_u32(&bars->mma_done), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT) && lane == 0)
+            raise_status(P.status, BSA_ERR_TIMEOUT);
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax + epilogue
