@@ -482,9 +482,9 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
                 }
                 const int32_t slot = t % C::kStages;
                 const uint32_t phase = (uint32_t)(t / C::kStages) & 1u;
-                int w = 1;
-                if (lane == 0) w = mbar_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
-                w = __shfl_sync(0xffffffffu, w, 0);
+                // every lane waits (warp-uniform control flow); one elected lane issues tile loads
+                const bool w = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, kWaitNs,
+                                                                 P.status, BSA_ERR_TIMEOUT));
                 if (!w || aborted(bars)) {
                     if (lane == 0) set_abort(bars, P.status);
                     break;
@@ -502,10 +502,14 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
                     cp_async_arrive_noinc(fb);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) tok[j] = tok_next[j];
-                } else if (lane == 0) {  // tile load
-                    mbar_arrive_expect_tx(fb, C::kTile);
-                    if constexpr (kGeom) geo_load_kv(P, dst, fb, is_v, bh_kv, kb);
-                    else tma_load_3d(dst, is_v ? &P.map_v : &P.map_k, 0, (int32_t)(bh_kv * N) + kb * 128, 0, fb);
+                } else {
+                    // tile load by one elected lane
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(fb, C::kTile);
+                        if constexpr (kGeom) geo_load_kv(P, dst, fb, is_v, bh_kv, kb);
+                        else tma_load_3d(dst, is_v ? &P.map_v : &P.map_k, 0, (int32_t)(bh_kv * N) + kb * 128, 0, fb);
+                    }
+                    __syncwarp();
                 }
                 issued = t + 1;
             }
@@ -1046,21 +1050,21 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
                 const int32_t kb = is_v ? stream_kb(e, v_base, v_cur, v_nxt) : stream_kb(e, k_base, k_cur, k_nxt);
                 const uint32_t pos = t_glob + (uint32_t)t;
                 const uint32_t slot = pos % S;
-                int wt = 1;
-                if (lane == 0)
-                    wt = mbar_wait(smem_u32(&bars->empty[slot]), ((pos / S) & 1u) ^ 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
-                wt = __shfl_sync(0xffffffffu, wt, 0);
+                // every lane waits (warp-uniform control flow); one elected lane issues
+                const bool wt = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->empty[slot]), ((pos / S) & 1u) ^ 1u,
+                                                                  kWaitNs, P.status, BSA_ERR_TIMEOUT));
                 if (!wt || items_aborted(bars)) {
                     ok = false;
                     break;
                 }
-                if (lane == 0) {
+                if (elect_one()) {
                     const uint32_t fb = smem_u32(&bars->full[slot]);
                     mbar_arrive_expect_tx(fb, C::kTile);
                     if constexpr (kGeom) geo_load_kv(P, s_ring + slot * C::kTile, fb, is_v, it.bh_kv, kb);
                     else tma_load_3d(s_ring + slot * C::kTile, is_v ? &P.map_v : &P.map_k, 0,
                                      (int32_t)(it.bh_kv * N) + kb * 128, 0, fb);
                 }
+                __syncwarp();
                 issued = pos + 1;
             }
             if (!ok) break;
