@@ -10,27 +10,34 @@
 // blockIdx.x is the execution slot within the head (query block
 // row_perm[head][slot]) and blockIdx.y the head, so blocks are issued
 // head-major in slot order: the sequential-head, wave-ordered schedule of
-// WaveAlign section V.
+// WaveAlign section V.  Short rows (the Scatter and Gather 0 layers, sliding
+// windows) run in k_bsa_forward_items instead: one block per SM walks the
+// items in the same order (see the comment above that kernel).
 //
 // Warp roles (8 warps):
 //   warp 0      producer: Q once (one TMA tile copy; with q_map the softmax
 //               warps gather it), then K_j and V_j of every listed block
 //               into a ring of kStages shared-memory slots, one TMA tile
 //               copy each.  The list is read 32 entries at a time by the
-//               whole warp.
+//               whole warp; every lane waits for a free slot and one lane
+//               elected with elect.sync issues the copy, so the warp's
+//               control flow stays uniform.
 //   warps 6, 7  with kv_map given, warp 0 and these two gather the K/V
 //               tiles in turn: each copies the 128 token rows of its tiles
 //               with 16-byte cp.async into the swizzled layout, one warp
 //               alone being too slow for row-granular copies (INTRA's
 //               gather, on the load/store path instead of the tensor-copy
 //               unit).
-//   warp 1      allocates tensor memory; one lane issues tcgen05.mma in the
-//               order QK(0), QK(1), QK(2), then for i = 0..n-1: PV(i),
-//               QK(i+3): S_j = Q K_j^T into TMEM score buffer j % 3 (QK runs
-//               up to three blocks ahead of the softmax), O += P_i V_i with P
-//               read from TMEM.  This lane touches no global memory; it waits
-//               only for P_i and for data, and keeps the tensor core's
-//               instruction queue fed.
+//   warp 1      allocates tensor memory and issues tcgen05.mma in the order
+//               QK(0), QK(1), QK(2), then for i = 0..n-1: PV(i), QK(i+3):
+//               S_j = Q K_j^T into TMEM score buffer j % 3 (QK runs up to
+//               three blocks ahead of the softmax), O += P_i V_i with P read
+//               from TMEM.  The whole warp walks this schedule (the waits,
+//               the descriptor and TMEM address arithmetic) and one elected
+//               lane issues each group of MMAs and its commit: with lane 0
+//               alone inside a divergent branch the same schedule ran about
+//               5 % slower.  The warp touches no global memory; it waits
+//               only for P_i and for data.
 //   warps 2..5  softmax: one thread per query row (TMEM lane); with q_map
 //               each warp first copies its 32 query rows into the Q tile
 //               (cp.async, 16 bytes per lane); reads S_j,
