@@ -1,0 +1,55 @@
+"""Host-side accounting of bench.py (no GPU): the attended pairs of the Gather
+0 layer against the oracle's query and key sets, compulsory bytes with
+grouped heads, densities, and the reference arm's JSON line for the image
+layer."""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+import bench
+import oracle
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_image_pairs_match_oracle_sets():
+    for h, w, nt, g in [(32, 32, 128, 2), (16, 24, 0, 1), (64, 32, 256, 8)]:
+        prob = synth.image_gather0(H=1, img_h=h, img_w=w, n_text=nt, groups=g, D=64)
+        pairs = sum(len(qt) * len(kt) for qt, kt in oracle.gather0_sets(h, w, nt, g))
+        assert bench.image_visible_pairs(prob) == pairs
+        assert bench.image_useful_flops(prob) == 4.0 * 64 * pairs
+        assert np.isclose(bench.workload_density(prob, None), pairs / float(prob.N) ** 2)
+
+
+def test_flux_shape_pairs():
+    prob = synth.image_gather0()
+    # every image query: 512 text keys + its 16 x 16 window; every text query:
+    # 512 text keys + its Scatter group's 16384 / 8 image tokens
+    assert bench.image_visible_pairs(prob) == 16384 * (512 + 256) + 512 * (512 + 2048)
+
+
+def test_compulsory_bytes_grouped_heads():
+    prob = synth.llm_window(H=4, H_kv=2, N=1024, D=128)
+    q_and_o = 2 * 1 * 4 * 1024 * 128 * 2
+    k_and_v = 2 * 1 * 2 * 1024 * 128 * 2
+    lse = 1 * 4 * 1024 * 4
+    assert bench.compulsory_bytes(prob) == q_and_o + k_and_v + lse
+
+
+def test_reference_arm_image_layer_line():
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "9",
+           "--steps", "1", "--warmup", "0"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["dtype"] == "f64" and d["value"] > 0
+    assert d["config"]["config_id"] == 9 and d["config"]["image"] == "128x128"
+    assert "attended query-key pairs" in d["config"]["flops"]
+    assert "(head, CQS)" in d["cpu_baseline"]["sample"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0
