@@ -312,6 +312,11 @@ bsa_status bsa_forward(const void* q, const void* k, const void* v, int32_t B, i
  *    some visible key.
  *  - Without a mask (causal = 0, window = 0, n_valid = 0 or N) the result is
  *    bit-identical to bsa_forward on K/V heads repeated H/H_kv times.
+ *  - Scheduling: when window > 0 bounds every row to 16 listed blocks or
+ *    fewer ((window + 254) / 128 + ceil(sinks / 128) <= 16) and no map is
+ *    given, one thread block per SM walks the rows in order (short rows
+ *    otherwise leave the tensor cores idle between blocks); else one thread
+ *    block per row.  Results are bit-identical either way.
  *
  *  H_kv      1 .. H, dividing H.
  *  causal    0 or 1.   n_valid 0 .. N.   window >= 0.   sinks >= 0.
@@ -422,7 +427,8 @@ bsa_status bsa_gather0_layout(int32_t img_h, int32_t img_w, int32_t n_text, int3
  * and "CQS-Aware Token-Sparse FlashAttention Kernel" (index mappings
  * computed at run time, outputs scattered back).
  *
- * Same result as bsa_forward_packed (bit for bit) on the maps of
+ * One thread block per SM walks the query tiles (rows of 7-8 tiles).  Same
+ * result as bsa_forward_packed (bit for bit) on the maps of
  * bsa_gather0_layout, without reading them: a query tile of two patches is
  * a 16-row x 8-column box of the image, a window band an 8-row x 16-column
  * box, a Scatter-group tile 128 tokens at stride groups, a text tile 128
@@ -449,6 +455,9 @@ bsa_status bsa_forward_gather0(const void* q, const void* k, const void* v, int3
  * tokens as (t, r) = t*R + r in T neighbourhoods of R; group S_r = {(t, r)})
  * and "CQS-Aware Token-Sparse FlashAttention Kernel" (mappings computed at
  * run time, outputs scattered back).
+ *
+ * One thread block per SM walks the rows (each row is short: the launch,
+ * prologue and epilogue of a block per row would dominate).
  *
  * The result is bsa_forward_masked without a token mask on the maps
  *     q_map[bh][p] = kv_map[bh][p] = (p mod T)*R + p / T,   T = N / R,
