@@ -216,3 +216,30 @@ def test_geometry_mode_flux_shape():
     all_sets = oracle.gather0_sets(img_h, img_w, n_text, groups)
     rows = np.concatenate([all_sets[s][0] for s in sets])
     _check(o2, l2, O_ref, L_ref, heads, rows)
+
+
+def _sweep_shapes():
+    import test_gather0_shapes
+    return test_gather0_shapes.SHAPES
+
+
+@pytest.mark.parametrize("img_h,img_w,n_text,groups", _sweep_shapes())
+def test_layout_key_sets_sweep(img_h, img_w, n_text, groups):
+    """The GPU layout over 30 seeded image shapes: every query sees exactly
+    the oracle's key set (one head; heads are identical copies)."""
+    q_map, kv_map, idx, cnt, qm = (t.cpu().numpy() for t in _layout(img_h, img_w, n_text, groups, 1))
+    N = n_text + img_h * img_w
+    expected = {}
+    for qt, kt in oracle.gather0_sets(img_h, img_w, n_text, groups):
+        ks = np.sort(kt)
+        for t in qt:
+            expected[int(t)] = ks
+    assert np.array_equal(np.sort(q_map[0]), np.arange(N))
+    for qb in range(N // 128):
+        n = int(cnt[qb])
+        for quad in range(4):
+            tiles = [int(t) for t, m in zip(idx[qb, :n], qm[qb, :n]) if (m >> quad) & 1]
+            keys = np.sort(np.concatenate([kv_map[0, 128 * t: 128 * t + 128] for t in tiles]))
+            toks = q_map[0, qb * 128 + 32 * quad: qb * 128 + 32 * quad + 32]
+            for tok in toks:
+                assert np.array_equal(keys, expected[int(tok)])
