@@ -5,7 +5,11 @@ One step = one pass of the whole path over one synthetic workload resident
 in HBM: index-list construction (threshold map, mask or top-k scores, plus
 sampling where the workload has it) -> query-row reordering -> block-sparse
 attention forward.  The metric is effective TFLOP/s: 4 * 128 * 128 * D FLOPs
-per computed (query block, KV block) pair, divided by the step time.
+per computed (query block, KV block) pair, divided by the step time; for the
+Gather 0 image layer (config 9) 4 * D FLOPs per attended query-key pair.  The
+roofline object reports the forward kernel against the measured bf16 peak,
+or against the measured HBM copy bandwidth when the workload's FLOPs per
+compulsory byte fall below the ridge (the one-pair Scatter layer).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2]
                     [--order reordered|identity] [--impl ours|reference]
