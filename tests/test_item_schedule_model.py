@@ -42,13 +42,20 @@ def tile_is_v(t, n):
 
 
 class Model:
-    def __init__(self, rows, S, kqb, rng):
+    def __init__(self, rows, S, kqb, rng, producers=1):
         self.rows, self.S, self.kqb, self.rng = rows, S, kqb, rng
         self.count = {}          # barrier -> completions so far
         self.waiting = {}        # process name -> (barrier, target completion index)
         self.copies = []         # pending copy-engine completions (barrier names)
         self.pipe = []           # tensor pipe: in-order list of barrier names to complete
-        self.procs = {"producer": self.producer(), "mma": self.mma(), "softmax": self.softmax()}
+        if producers == 1:
+            self.procs = {"producer": self.producer()}
+        else:
+            # the single-row kernel's gathered K/V: producer warps g take
+            # tiles t with t % producers == g (one row, Q loaded once)
+            assert len(rows) == 1
+            self.procs = {f"producer{g}": self.gather_producer(g, producers) for g in range(producers)}
+        self.procs.update({"mma": self.mma(), "softmax": self.softmax()})
 
     # a wait for completion number k passes when count > k; the model yields
     # the wait to the scheduler until then
@@ -78,6 +85,16 @@ class Model:
                 self.copies.append(("full", slot))
                 pos += 1
             qi += 1
+
+    def gather_producer(self, g, producers):
+        n = self.rows[0]
+        if g == 0 and n > 0:
+            self.copies.append(("q_full", 0))
+        for pos in range(g, 2 * n, producers):
+            slot = pos % self.S
+            if pos >= self.S:
+                yield self.wait(("empty", slot), pos // self.S - 1)
+            self.copies.append(("full", slot))  # the tile's 32 lane arrivals, once all copies landed
 
     def mma(self):
         pos = 0
@@ -193,3 +210,13 @@ def test_model_catches_a_short_ring():
         except AssertionError:
             failures += 1
     assert failures > 0
+
+
+@pytest.mark.parametrize("S", [6, 12])
+@pytest.mark.parametrize("seed", range(12))
+def test_row_protocol_with_three_gathering_warps(S, seed):
+    """The single-row kernel with gathered K/V: three producer warps copy
+    the tiles in turn, each waiting for its own ring slot."""
+    rng = random.Random(1000 + seed * 13 + S)
+    n = rng.choice([1, 2, 3, 4, 7, 16, 33, 69])
+    Model([n], S, 1, rng, producers=3).run()
