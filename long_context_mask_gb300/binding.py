@@ -133,6 +133,51 @@ def _dtype(t, name, *dtypes):
         raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
 
 
+# The library takes plain pointers, so it cannot see how large a buffer is:
+# the checks below reject, before any launch, a buffer smaller than what the
+# kernels read or write, an index array of another width, and tensors on
+# different devices.  A larger buffer is accepted (only its leading part is
+# used).
+
+def _rows(t, name, rows, dtype, cols=None):
+    """A 2-D array of `dtype` with at least `rows` rows (and exactly `cols`
+    columns when given, i.e. sharing another array's row stride)."""
+    if t is None:
+        return
+    _dtype(t, name, dtype)
+    if t.dim() != 2 or t.shape[0] < rows or (cols is not None and t.shape[1] != cols):
+        want = "any" if cols is None else cols
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected [>= {rows}, {want}]")
+
+
+def _flat(t, name, n, dtype):
+    """An array of `dtype` with at least `n` entries."""
+    if t is None:
+        return
+    _dtype(t, name, dtype)
+    if t.numel() < n:
+        raise ValueError(f"{name}: {t.numel()} entries, expected >= {n}")
+
+
+def _same_device(ref, *ts):
+    for t in ts:
+        if t is not None and t.device != ref.device:
+            raise ValueError(f"tensors on {t.device} and {ref.device}: all must be on one device")
+
+
+def _lists(B, H, N, kv_idx, kv_cnt, log_w=None, row_perm=None, lse=None):
+    """The per-row block lists of a forward over B*H heads of N tokens."""
+    import torch
+    if kv_idx is None or kv_cnt is None:
+        raise ValueError("kv_idx and kv_cnt are required")
+    rows = B * H * (N // BLOCK)
+    _rows(kv_idx, "kv_idx", rows, torch.int32)
+    _flat(kv_cnt, "kv_cnt", rows, torch.int32)
+    _rows(log_w, "log_w", rows, torch.float32, cols=kv_idx.shape[1])
+    _flat(row_perm, "row_perm", rows, torch.int32)
+    _flat(lse, "lse", B * H * N, torch.float32)
+
+
 def build_index(mode: int, src, kv_idx, kv_cnt, *, p: float = 0.0, k_per_row=None,
                 k_const: int = 0, stream=None):
     """Fill kv_idx [rows, max_kv] / kv_cnt [rows] from src [rows, nKB] (see bsa.h)."""
@@ -142,6 +187,10 @@ def build_index(mode: int, src, kv_idx, kv_cnt, *, p: float = 0.0, k_per_row=Non
     _dtype(kv_cnt, "kv_cnt", torch.int32)
     _dtype(k_per_row, "k_per_row", torch.int32)
     rows, nkb = src.shape
+    _rows(kv_idx, "kv_idx", rows, torch.int32)
+    _flat(kv_cnt, "kv_cnt", rows, torch.int32)
+    _flat(k_per_row, "k_per_row", rows, torch.int32)
+    _same_device(src, kv_idx, kv_cnt, k_per_row)
     code = load_library().bsa_build_index(mode, _ptr(src), rows, nkb, float(p), _ptr(k_per_row),
                                           int(k_const), _ptr(kv_idx), _ptr(kv_cnt),
                                           kv_idx.shape[1], _stream(stream))
@@ -159,6 +208,12 @@ def block_scores(q, k, scores, *, q_map=None, kv_map=None, scale: float = 0.0,
     _dtype(k, "k", torch.bfloat16)
     _dtype(scores, "scores", torch.float32)
     B, H, N, D = q.shape
+    if k.shape != q.shape:
+        raise ValueError("q and k must share the shape [B, H, N, D]")
+    _flat(scores, "scores", B * H * (N // BLOCK) * (N // BLOCK), torch.float32)
+    _flat(q_map, "q_map", B * H * N, torch.int32)
+    _flat(kv_map, "kv_map", B * H * N, torch.int32)
+    _same_device(q, k, scores, q_map, kv_map, workspace)
     lib = load_library()
     need = int(lib.bsa_block_scores_workspace_size(B, H, N, D))
     if workspace is None:
@@ -177,6 +232,8 @@ def build_crm(mode: int, src, words, *, p: float = 0.0, stream=None):
     _dtype(src, "src", torch.uint8 if mode == IDX_MASK_U8 else torch.float32)
     _dtype(words, "words", torch.int32)
     rows, nkb = src.shape
+    _rows(words, "words", rows, torch.int32)
+    _same_device(src, words)
     _check("bsa_build_crm", load_library().bsa_build_crm(mode, _ptr(src), rows, nkb, float(p),
                                                          _ptr(words), words.shape[1],
                                                          _stream(stream)))
@@ -190,6 +247,14 @@ def forward_crm(q, k, v, crm, o, lse, *, q_map=None, kv_map=None, row_perm=None,
         _dtype(t, n, torch.bfloat16)
     _dtype(crm, "crm", torch.int32)
     B, H, N, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape or o.shape != q.shape:
+        raise ValueError("q, k, v, o must share the shape [B, H, N, D]")
+    _rows(crm, "crm", B * H * (N // BLOCK), torch.int32)
+    _flat(q_map, "q_map", B * H * N, torch.int32)
+    _flat(kv_map, "kv_map", B * H * N, torch.int32)
+    _flat(row_perm, "row_perm", B * H * (N // BLOCK), torch.int32)
+    _flat(lse, "lse", B * H * N, torch.float32)
+    _same_device(q, k, v, crm, o, lse, q_map, kv_map, row_perm)
     code = load_library().bsa_forward_crm(_ptr(q), _ptr(k), _ptr(v), B, H, N, D, _ptr(crm),
                                           crm.shape[1], _ptr(q_map), _ptr(kv_map), _ptr(row_perm),
                                           float(scale), _ptr(o), _ptr(lse), _stream(stream))
@@ -202,7 +267,10 @@ def upscale_threshold(T_base, T_target, *, stream=None):
     _dtype(T_base, "T_base", torch.float32)
     _dtype(T_target, "T_target", torch.float32)
     heads, ub, vb = T_base.shape
-    _, ut, vt = T_target.shape
+    h_out, ut, vt = T_target.shape
+    if h_out != heads:
+        raise ValueError("T_base and T_target must hold the same number of heads")
+    _same_device(T_base, T_target)
     _check("bsa_upscale_threshold", load_library().bsa_upscale_threshold(
         _ptr(T_base), heads, ub, vb, ut, vt, _ptr(T_target), _stream(stream)))
 
@@ -219,6 +287,7 @@ def gather_rows(src, map, dst=None, *, stream=None):
     _dtype(dst, "dst", torch.bfloat16)
     if map.numel() != heads * N or dst.shape != src.shape:
         raise ValueError("gather_rows: map must hold heads * N entries and dst match src")
+    _same_device(src, map, dst)
     _check("bsa_gather_rows", load_library().bsa_gather_rows(_ptr(src), _ptr(map), heads, N, D,
                                                              _ptr(dst), _stream(stream)))
     return dst
@@ -231,9 +300,21 @@ def reorder_rows(kv_cnt, wave: int, row_perm, *, order_in=None, stream=None):
     _dtype(row_perm, "row_perm", torch.int32)
     _dtype(order_in, "order_in", torch.int32)
     heads, nqb = kv_cnt.shape
+    _flat(row_perm, "row_perm", heads * nqb, torch.int32)
+    _flat(order_in, "order_in", heads * nqb, torch.int32)
+    _same_device(kv_cnt, row_perm, order_in)
     code = load_library().bsa_reorder_rows(_ptr(kv_cnt), _ptr(order_in), heads, nqb, int(wave),
                                            _ptr(row_perm), _stream(stream))
     _check("bsa_reorder_rows", code)
+
+
+def _spectral_args(heads, nqb, kv_idx, kv_cnt, x0, x_out, angle):
+    import torch
+    _rows(kv_idx, "kv_idx", heads * nqb, torch.int32)
+    _flat(kv_cnt, "kv_cnt", heads * nqb, torch.int32)
+    _flat(x0, "x0", heads * nqb * 2, torch.float32)
+    _flat(x_out, "x_out", heads * nqb * 2, torch.float32)
+    _flat(angle, "angle", heads * nqb, torch.float32)
 
 
 def spectral_order_workspace_size(heads: int, nqb: int, nkb: int) -> int:
@@ -252,6 +333,8 @@ def spectral_order(kv_idx, kv_cnt, n_kb: int, x0, order, *, workspace=None, x_ou
     _dtype(x0, "x0", torch.float32)
     _dtype(order, "order", torch.int32)
     heads, nqb = order.shape
+    _spectral_args(heads, nqb, kv_idx, kv_cnt, x0, x_out, angle)
+    _same_device(order, kv_idx, kv_cnt, x0, x_out, angle, workspace)
     need = spectral_order_workspace_size(heads, nqb, n_kb)
     if workspace is None:
         workspace = torch.empty(max(need, 8), dtype=torch.uint8, device=order.device)
@@ -274,6 +357,8 @@ def spectral_order_noalloc(kv_idx, kv_cnt, n_kb: int, x0, order, *, x_out=None, 
     _dtype(x0, "x0", torch.float32)
     _dtype(order, "order", torch.int32)
     heads, nqb = order.shape
+    _spectral_args(heads, nqb, kv_idx, kv_cnt, x0, x_out, angle)
+    _same_device(order, kv_idx, kv_cnt, x0, x_out, angle)
     code = load_library().bsa_spectral_order_noalloc(_ptr(kv_idx), _ptr(kv_cnt), kv_idx.shape[1],
                                                      heads, nqb, int(n_kb), int(iters), _ptr(x0),
                                                      _ptr(x_out), _ptr(angle), _ptr(order),
@@ -297,8 +382,19 @@ def sample_blocks(scores, exact_idx, exact_cnt, m: int, u, kv_idx, kv_cnt, log_w
     _dtype(u, "u", torch.float64)
     if scores is None:
         rows = exact_cnt.shape[0]
+        if nkb is None:
+            raise ValueError("sample_blocks: pass nkb with the uniform sampler (scores None)")
     else:
         rows, nkb = scores.shape
+    _rows(exact_idx, "exact_idx", rows, torch.int32)
+    _flat(exact_cnt, "exact_cnt", rows, torch.int32)
+    _flat(u, "u", rows, torch.float64)
+    if kv_idx is None or kv_cnt is None or log_w is None:
+        raise ValueError("kv_idx, kv_cnt and log_w are required")
+    _rows(kv_idx, "kv_idx", rows, torch.int32)
+    _flat(kv_cnt, "kv_cnt", rows, torch.int32)
+    _rows(log_w, "log_w", rows, torch.float32, cols=kv_idx.shape[1])
+    _same_device(exact_idx, scores, exact_cnt, u, kv_idx, kv_cnt, log_w)
     code = load_library().bsa_sample_blocks(_ptr(scores), rows, nkb, _ptr(exact_idx),
                                             _ptr(exact_cnt), exact_idx.shape[1], int(m), _ptr(u),
                                             _ptr(kv_idx), _ptr(kv_cnt), _ptr(log_w),
@@ -317,6 +413,10 @@ def forward(q, k, v, kv_idx, kv_cnt, o, lse, *, log_w=None, q_map=None, kv_map=N
     B, H, N, D = q.shape
     if k.shape != q.shape or v.shape != q.shape or o.shape != q.shape:
         raise ValueError("q, k, v, o must share the shape [B, H, N, D]")
+    _lists(B, H, N, kv_idx, kv_cnt, log_w, row_perm, lse)
+    _flat(q_map, "q_map", B * H * N, torch.int32)
+    _flat(kv_map, "kv_map", B * H * N, torch.int32)
+    _same_device(q, k, v, o, lse, kv_idx, kv_cnt, log_w, q_map, kv_map, row_perm)
     code = load_library().bsa_forward(_ptr(q), _ptr(k), _ptr(v), B, H, N, D, _ptr(kv_idx),
                                       _ptr(kv_cnt), kv_idx.shape[1], _ptr(log_w), _ptr(q_map),
                                       _ptr(kv_map), _ptr(row_perm), float(scale), _ptr(o),
@@ -337,6 +437,10 @@ def forward_masked(q, k, v, kv_idx, kv_cnt, o, lse, *, causal: bool = False, n_v
     H_kv = k.shape[1]
     if k.shape != (B, H_kv, N, D) or v.shape != k.shape or o.shape != q.shape:
         raise ValueError("q, o [B, H, N, D]; k, v [B, H_kv, N, D]")
+    _lists(B, H, N, kv_idx, kv_cnt, log_w, row_perm, lse)
+    _flat(q_map, "q_map", B * H * N, torch.int32)
+    _flat(kv_map, "kv_map", B * H_kv * N, torch.int32)
+    _same_device(q, k, v, o, lse, kv_idx, kv_cnt, log_w, q_map, kv_map, row_perm)
     code = load_library().bsa_forward_masked(
         _ptr(q), _ptr(k), _ptr(v), B, H, H_kv, N, D, _ptr(kv_idx), _ptr(kv_cnt), kv_idx.shape[1],
         _ptr(log_w), _ptr(q_map), _ptr(kv_map), _ptr(row_perm), int(bool(causal)), int(n_valid),
@@ -365,6 +469,10 @@ def forward_packed(q, k, v, kv_idx, kv_cnt, kv_map, o, lse, *, quad_mask=None, c
     N_kv = kv_map.shape[-1]
     if quad_mask is not None and tuple(quad_mask.shape) != tuple(kv_idx.shape):
         raise ValueError("quad_mask must have kv_idx's shape")
+    _lists(B, H, N, kv_idx, kv_cnt, log_w, row_perm, lse)
+    _flat(q_map, "q_map", B * H * N, torch.int32)
+    _flat(kv_map, "kv_map", B * H_kv * N_kv, torch.int32)
+    _same_device(q, k, v, o, lse, kv_idx, kv_cnt, log_w, q_map, kv_map, quad_mask, row_perm)
     code = load_library().bsa_forward_packed(
         _ptr(q), _ptr(k), _ptr(v), B, H, H_kv, N, D, _ptr(kv_idx), _ptr(kv_cnt), kv_idx.shape[1],
         _ptr(log_w), _ptr(q_map), _ptr(kv_map), int(N_kv), _ptr(quad_mask), _ptr(row_perm),
@@ -415,6 +523,9 @@ def forward_gather0(q, k, v, img_h: int, img_w: int, n_text: int, groups: int, k
         raise ValueError("q, o [B, H, N, D]; k, v [B, H_kv, N, D]")
     if N != n_text + img_h * img_w:
         raise ValueError("N must be n_text + img_h * img_w")
+    _lists(B, H, N, kv_idx, kv_cnt, None, row_perm, lse)
+    _rows(quad_mask, "quad_mask", B * H * (N // BLOCK), torch.uint8, cols=kv_idx.shape[1])
+    _same_device(q, k, v, o, lse, kv_idx, kv_cnt, quad_mask, row_perm)
     code = load_library().bsa_forward_gather0(
         _ptr(q), _ptr(k), _ptr(v), B, H, H_kv, D, img_h, img_w, n_text, groups, _ptr(kv_idx),
         _ptr(kv_cnt), _ptr(quad_mask), kv_idx.shape[1], _ptr(row_perm), float(scale), _ptr(o),
@@ -435,6 +546,8 @@ def forward_scatter(q, k, v, R: int, kv_idx, kv_cnt, o, lse, *, log_w=None, row_
     H_kv = k.shape[1]
     if k.shape != (B, H_kv, N, D) or v.shape != k.shape or o.shape != q.shape:
         raise ValueError("q, o [B, H, N, D]; k, v [B, H_kv, N, D]")
+    _lists(B, H, N, kv_idx, kv_cnt, log_w, row_perm, lse)
+    _same_device(q, k, v, o, lse, kv_idx, kv_cnt, log_w, row_perm)
     code = load_library().bsa_forward_scatter(
         _ptr(q), _ptr(k), _ptr(v), B, H, H_kv, N, D, int(R), _ptr(kv_idx), _ptr(kv_cnt),
         kv_idx.shape[1], _ptr(log_w), _ptr(row_perm), float(scale), _ptr(o), _ptr(lse), _stream(stream))
