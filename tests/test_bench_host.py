@@ -53,3 +53,36 @@ def test_reference_arm_image_layer_line():
     assert "attended query-key pairs" in d["config"]["flops"]
     assert "(head, CQS)" in d["cpu_baseline"]["sample"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_recorded_traffic_follows_the_kernel_source(monkeypatch):
+    """ncu counters are reported only for the kernel they were taken on and
+    only on the workload they were taken on."""
+    import argparse
+    args = argparse.Namespace(config=2, heads=None, dense=False, crm=False, scores_on_gpu=False,
+                              order="reordered", kv_gather="auto")
+    with open(os.path.join(ROOT, "profiles", "forward_traffic.json")) as f:
+        rec = json.load(f)["config2"]
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: rec["kernel_hash"])
+    assert bench.recorded_traffic(args) == rec["dram_bytes_per_launch"]
+    assert rec["dram_bytes_per_launch"] == rec["dram_bytes_read"] + rec["dram_bytes_write"]
+    for change in (dict(heads=2), dict(dense=True), dict(order="identity"), dict(kv_gather="kernel"),
+                   dict(config=5)):
+        assert bench.recorded_traffic(argparse.Namespace(**{**vars(args), **change})) is None
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    assert bench.recorded_traffic(args) is None
+
+
+def test_kernel_hash_ignores_comments_only(tmp_path, monkeypatch):
+    """A comment edit keeps the hash; a code edit changes it."""
+    src_dir = tmp_path / "long_context_mask_gb300" / "csrc"
+    src_dir.mkdir(parents=True)
+    names = ("bsa_attn.cu", "bsa_ptx.cuh", "bsa_math.cuh", "bsa_gather0.cuh")
+    for n in names:
+        (src_dir / n).write_text("int f(int x) {\n  return x + 1;  // one\n}\n/* block */\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_hash()
+    (src_dir / names[0]).write_text("int f(int x) {\n  /* a note */ return x + 1;  // another\n}\n")
+    assert bench.kernel_source_hash() == h0
+    (src_dir / names[0]).write_text("int f(int x) {\n  return x + 2;\n}\n")
+    assert bench.kernel_source_hash() != h0
