@@ -86,3 +86,23 @@ def test_kernel_hash_ignores_comments_only(tmp_path, monkeypatch):
     assert bench.kernel_source_hash() == h0
     (src_dir / names[0]).write_text("int f(int x) {\n  return x + 2;\n}\n")
     assert bench.kernel_source_hash() != h0
+
+
+def test_clock_summary_parses_samples():
+    """The clocks record: median SM clock over the busy samples, the maximum,
+    and every throttle reason seen active (nvidia-smi csv, no header/units)."""
+    s = bench.ClockSampler("0")
+    s.lines = [
+        "345, 2070, 120.5, 0x0000000000000001, Not Active, Not Active, Not Active, Not Active",   # idle
+        "1965, 2070, 1210.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "1980, 2070, 1190.2, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "1950, 2070, 1250.7, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "[N/A], 2070, [N/A], [N/A], [N/A], [N/A], [N/A], [N/A]",                                # unreadable
+        "garbage",
+    ]
+    d = s.summary()
+    assert d == {"sm_mhz": 1965.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 4}
+    s.lines.append("1500, 2070, 1300.0, 0x0000000000000048, Active, Not Active, Active, Not Active")
+    assert s.summary()["reasons"] == ["hw_slowdown", "sw_power_cap", "sw_thermal_slowdown"]
+    s.lines = []
+    assert s.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
