@@ -19,6 +19,10 @@
  *    (batch, head, query block) triples in that nesting order:
  *    row = (b * H + h) * nQB + qb.
  *  - Block edge is 128 tokens for queries and keys (nQB = nKB = N / 128).
+ *  - A pointer carries no length: every array must hold at least the
+ *    entries its layout below gives (the library reads and writes exactly
+ *    those), on the device that is current when the call is made.  The
+ *    Python binding checks both before it calls.
  */
 #ifndef BSA_H
 #define BSA_H
