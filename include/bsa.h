@@ -68,7 +68,7 @@ typedef enum {
  *
  *  mode      which predicate selects a block (see bsa_idx_mode).
  *  src       device, [rows, nKB] uint8 (MASK) or fp32 (THRESHOLD, TOPK).
- *  rows      number of (b, h, qb) rows, >= 0.
+ *  rows      number of (b, h, qb) rows, 0 .. 8 * (2^31 - 1).
  *  nKB       KV blocks per row, 1 .. 65536.
  *  p         THRESHOLD: keep src <= p, compared in fp32 (inclusive).
  *  k_per_row TOPK: device int32 [rows] or NULL to use k_const for every row.
@@ -238,7 +238,7 @@ bsa_status bsa_spectral_order_noalloc(const int32_t* kv_idx, const int32_t* kv_c
  *               entries, -log(pi_j) (fp32 log) for drawn ones (tail 0).
  *  max_kv       capacity; a longer merged list is truncated and raises
  *               BSA_ERR_OVERFLOW.
- *  Outputs must not alias inputs.  nKB <= 4096.
+ *  Outputs must not alias inputs.  nKB <= 4096; rows 0 .. 64 * (2^31 - 1).
  */
 bsa_status bsa_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
                              const int32_t* exact_idx, const int32_t* exact_cnt,
@@ -512,6 +512,7 @@ bsa_status bsa_gather_rows(const void* src, const int32_t* map, int64_t heads, i
  * block states).  Same selection as bsa_build_index (MASK / THRESHOLD);
  * bits at or beyond nKB are 0.
  *
+ *  rows       0 .. 8 * (2^31 - 1), as for bsa_build_index.
  *  words      device uint32 [rows, crm_words] out; crm_words >= ceil(nKB/32)
  *             (words beyond ceil(nKB/32) are written as 0).
  */
@@ -547,6 +548,7 @@ bsa_status bsa_forward_crm(const void* q, const void* k, const void* v, int32_t 
  * minimum of T over those (one or two per axis, the upper index clamped).
  *
  *  T_base    device fp32 [heads, Ub, Vb];  T_target device fp32 [heads, Ut, Vt] out.
+ *  heads <= 65535, Ut <= 65535; Ub, Vb, Vt <= 65536 (all >= 1).
  */
 bsa_status bsa_upscale_threshold(const float* T_base, int64_t heads, int32_t Ub, int32_t Vb,
                                  int32_t Ut, int32_t Vt, float* T_target, void* stream);

@@ -60,7 +60,7 @@ bsa_status bsa_build_index(bsa_idx_mode mode, const void* src, int64_t rows, int
     if (mode != BSA_IDX_MASK_U8 && mode != BSA_IDX_THRESHOLD_F32 && mode != BSA_IDX_TOPK_F32)
         return BSA_ERR_INVALID_ARG;
     if (rows < 0 || nKB < 1 || nKB > 65536 || max_kv < 1 || max_kv > nKB) return BSA_ERR_INVALID_ARG;
-    if (rows > ((int64_t)1 << 40)) return BSA_ERR_INVALID_ARG;
+    if (rows > bsa::kListRowsPerBlock * bsa::kMaxGridX) return BSA_ERR_INVALID_ARG;
     if (rows == 0) return BSA_OK;
     if (!src || !kv_idx || !kv_cnt) return BSA_ERR_INVALID_ARG;
     if (!aligned(kv_idx, 4) || !aligned(kv_cnt, 4)) return BSA_ERR_INVALID_ARG;
@@ -162,7 +162,8 @@ bsa_status bsa_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
                              const int32_t* exact_idx, const int32_t* exact_cnt,
                              int32_t exact_stride, int32_t m, const double* u, int32_t* kv_idx,
                              int32_t* kv_cnt, float* log_w, int32_t max_kv, void* stream) {
-    if (rows < 0 || nKB < 1 || nKB > 4096 || exact_stride < 1 || m < 0 || max_kv < 1)
+    if (rows < 0 || rows > bsa::kSampleRowsPerBlock * bsa::kMaxGridX || nKB < 1 || nKB > 4096 ||
+        exact_stride < 1 || m < 0 || max_kv < 1)
         return BSA_ERR_INVALID_ARG;
     if (rows == 0) return BSA_OK;
     if (!exact_idx || !exact_cnt || !u || !kv_idx || !kv_cnt || !log_w)
@@ -366,7 +367,7 @@ bsa_status bsa_forward_crm(const void* q, const void* k, const void* v, int32_t 
 bsa_status bsa_build_crm(bsa_idx_mode mode, const void* src, int64_t rows, int32_t nKB, float p,
                          uint32_t* words, int32_t crm_words, void* stream) {
     if (mode != BSA_IDX_MASK_U8 && mode != BSA_IDX_THRESHOLD_F32) return BSA_ERR_INVALID_ARG;
-    if (rows < 0 || rows > ((int64_t)1 << 40) || nKB < 1 || nKB > 65536 ||
+    if (rows < 0 || rows > bsa::kListRowsPerBlock * bsa::kMaxGridX || nKB < 1 || nKB > 65536 ||
         crm_words < (nKB + 31) / 32 || crm_words > (1 << 20))
         return BSA_ERR_INVALID_ARG;
     if (rows == 0) return BSA_OK;
@@ -379,8 +380,8 @@ bsa_status bsa_build_crm(bsa_idx_mode mode, const void* src, int64_t rows, int32
 
 bsa_status bsa_upscale_threshold(const float* T_base, int64_t heads, int32_t Ub, int32_t Vb,
                                  int32_t Ut, int32_t Vt, float* T_target, void* stream) {
-    if (heads < 0 || heads > 65535 || Ub < 1 || Vb < 1 || Ut < 1 || Vt < 1 || Ub > 65536 ||
-        Vb > 65536 || Ut > 65536 || Vt > 65536)
+    if (heads < 0 || heads > bsa::kMaxGridYZ || Ub < 1 || Vb < 1 || Ut < 1 || Vt < 1 || Ub > 65536 ||
+        Vb > 65536 || Ut > bsa::kMaxGridYZ || Vt > 65536)
         return BSA_ERR_INVALID_ARG;
     if (heads == 0) return BSA_OK;
     if (!T_base || !T_target || !aligned(T_base, 4) || !aligned(T_target, 4)) return BSA_ERR_INVALID_ARG;

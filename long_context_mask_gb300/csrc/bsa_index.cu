@@ -244,6 +244,7 @@ constexpr int kWords = kMaxSampleKB / 32;
 // oracle bit for bit.  The exact / promoted set of each row is a bitset in
 // shared memory (word w of thread t at w * 64 + t: conflict-free).
 constexpr int kSampleThreads = 64;
+static_assert(kSampleThreads == kSampleRowsPerBlock, "the host bounds rows by this launch shape");
 
 __global__ void __launch_bounds__(kSampleThreads) k_sample_blocks(
     const float* __restrict__ scores, int64_t rows, int32_t nKB, const int32_t* __restrict__ exact_idx,
@@ -400,7 +401,7 @@ cudaError_t launch_index_predicate(bsa_idx_mode mode, const void* src, int64_t r
                                    float p, int32_t* kv_idx, int32_t* kv_cnt, int32_t max_kv,
                                    int32_t* status, cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
-    const int warps = 8;
+    const int warps = kListRowsPerBlock;
     const dim3 grid((unsigned)((rows + warps - 1) / warps));
     if (mode == BSA_IDX_MASK_U8)
         k_index_predicate<BSA_IDX_MASK_U8><<<grid, warps * 32, 0, stream>>>(src, rows, nKB, p, kv_idx,
@@ -414,11 +415,11 @@ cudaError_t launch_index_predicate(bsa_idx_mode mode, const void* src, int64_t r
 cudaError_t launch_crm_rows(bsa_idx_mode mode, const void* src, int64_t rows, int32_t nKB, float p,
                             uint32_t* words, int32_t n_words, cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
-    const dim3 grid((unsigned)((rows + 7) / 8));
+    const dim3 grid((unsigned)((rows + kListRowsPerBlock - 1) / kListRowsPerBlock));
     if (mode == BSA_IDX_MASK_U8)
-        k_crm_rows<BSA_IDX_MASK_U8><<<grid, 256, 0, stream>>>(src, rows, nKB, p, words, n_words);
+        k_crm_rows<BSA_IDX_MASK_U8><<<grid, kListRowsPerBlock * 32, 0, stream>>>(src, rows, nKB, p, words, n_words);
     else
-        k_crm_rows<BSA_IDX_THRESHOLD_F32><<<grid, 256, 0, stream>>>(src, rows, nKB, p, words, n_words);
+        k_crm_rows<BSA_IDX_THRESHOLD_F32><<<grid, kListRowsPerBlock * 32, 0, stream>>>(src, rows, nKB, p, words, n_words);
     return cudaGetLastError();
 }
 
@@ -435,7 +436,7 @@ cudaError_t launch_index_topk(const float* scores, int64_t rows, int32_t nKB,
                               int32_t* kv_cnt, int32_t max_kv, int32_t* status,
                               cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
-    const int warps = 8;
+    const int warps = kListRowsPerBlock;
     const dim3 grid((unsigned)((rows + warps - 1) / warps));
     if (nKB <= 32 * 32)
         k_index_topk<32><<<grid, warps * 32, 0, stream>>>(scores, rows, nKB, k_per_row, k_const, kv_idx,

@@ -11,6 +11,15 @@ namespace bsa {
 
 constexpr int kBlock = 128;  // query / key block edge
 
+// Launch shapes of the list kernels, which bound the rows one call may pass:
+// the index, top-k and CRM launches give each warp of an 8-warp block one
+// row, the sampler one thread of a 64-thread block, and grid.x is at most
+// 2^31 - 1 (grid.y and grid.z at most 65535).
+constexpr int kListRowsPerBlock = 8;
+constexpr int kSampleRowsPerBlock = 64;
+constexpr int64_t kMaxGridX = 2147483647;
+constexpr int64_t kMaxGridYZ = 65535;
+
 // Status word helpers (defined in bsa_api.cu).
 int32_t* status_word_ptr();  // device address of the current device's status word
 

@@ -215,3 +215,18 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="libbsa.so not found"):
         binding.load_library()
+
+
+def test_row_counts_beyond_one_launch_are_rejected(lib):
+    """Row counts a single launch cannot cover (grid.x <= 2^31 - 1 blocks of
+    8 rows for the list kernels, of 64 rows for the sampler; grid.y <= 65535
+    target rows for the upscale) are refused on the host instead of being
+    truncated; the calls return before any pointer is touched."""
+    grid_x = (1 << 31) - 1
+    assert lib.bsa_build_index(0, FAKE, 8 * grid_x + 1, 8, 0.5, None, 1, FAKE, FAKE, 8, None) == 1
+    assert lib.bsa_build_index(2, FAKE, 8 * grid_x + 1, 8, 0.5, None, 1, FAKE, FAKE, 8, None) == 1
+    assert lib.bsa_build_crm(0, FAKE, 8 * grid_x + 1, 8, 0.5, FAKE, 1, None) == 1
+    assert lib.bsa_sample_blocks(FAKE, 64 * grid_x + 1, 16, FAKE, FAKE, 1, 2, FAKE, FAKE, FAKE, FAKE, 4,
+                                 None) == 1
+    assert lib.bsa_upscale_threshold(FAKE, 1, 4, 4, 65536, 4, FAKE, None) == 1
+    assert lib.bsa_upscale_threshold(FAKE, 65536, 4, 4, 4, 4, FAKE, None) == 1
