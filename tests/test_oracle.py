@@ -320,6 +320,49 @@ def test_sample_size_inclusion_probabilities_and_promotion():
                 assert lw[r, e] == pytest.approx(-math.log(pi[list(resid).index(j)]), rel=1e-6)
 
 
+def _pps_cases():
+    cases, cur = [], None
+    for line in open(os.path.join(GOLD, "sampler_systematic_pps_example.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, _, rest = line.partition(" ")
+        if key == "case":
+            cur = {"name": rest}
+            cases.append(cur)
+        else:
+            cur[key] = rest.split()
+    return cases
+
+
+@pytest.mark.parametrize("case", _pps_cases(), ids=lambda c: c["name"])
+def test_sampler_hand_worked_draws(case):
+    """Single rows worked by hand: which blocks the points u + i select, the
+    capped block kept at weight 1, the whole residual kept when the budget
+    covers it, and the uniform sampler."""
+    from fractions import Fraction
+    if "uniform" in case:
+        scores, nkb = None, int(case["uniform"][0])
+    else:
+        scores = np.array([[float(x) for x in case["scores"]]], np.float32)
+        nkb = scores.shape[1]
+    exact = [int(x) for x in case.get("exact", [])]
+    ex = np.array([exact or [0]], np.int32)
+    ec = np.array([len(exact)], np.int32)
+    u = np.array([float(case["u"][0])])
+    idx, cnt, lw, ov = oracle.sample_blocks(scores, ex, ec, int(case["m"][0]), u, nkb, nkb=nkb)
+    blocks = [int(x) for x in case["blocks"]]
+    assert ov == 0 and cnt[0] == len(blocks)
+    assert list(idx[0, :cnt[0]]) == blocks
+    assert np.all(idx[0, cnt[0]:] == -1)
+    for e, f in enumerate(case["pi"]):
+        pi = Fraction(f)
+        if pi == 1:
+            assert lw[0, e] == 0.0
+        else:
+            assert lw[0, e] == pytest.approx(-math.log(float(pi)), rel=1e-6)
+
+
 def test_horvitz_thompson_estimate_is_unbiased():
     g = np.random.default_rng(9)
     nkb, m = 30, 5
