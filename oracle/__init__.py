@@ -39,8 +39,12 @@ _lib = None
 def _load():
     global _lib
     if _lib is None:
-        build()
-        lib = ctypes.CDLL(_LIB)
+        # ORACLE_LIB_OVERRIDE: a library built from a deliberately altered copy
+        # of bsa_oracle.c, used by the tests that check the pins catch it
+        override = os.environ.get("ORACLE_LIB_OVERRIDE")
+        if not override:
+            build()
+        lib = ctypes.CDLL(override or _LIB)
         P = ctypes.c_void_p
         i32, i64, f32, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_double
         lib.oracle_index_mask_u8.argtypes = [P, i64, i32, P, P, i32]

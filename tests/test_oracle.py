@@ -540,6 +540,26 @@ def test_spectral_order_is_equivariant_under_row_relabelling():
     np.testing.assert_allclose(angp[0], ang[0][perm], atol=1e-10)
 
 
+def test_spectral_angle_and_ties_to_the_lower_row():
+    """Identical mask rows get identical embeddings and angles; the order
+    lists such rows by ascending query block.  The angle is the polar angle
+    of the row's two coordinates, atan2(second, first)."""
+    rng = np.random.default_rng(13)
+    nqb, nkb = 40, 30
+    mask, _ = _planted_mask(rng, 1, nqb, nkb, clusters=2)
+    m = mask[0].copy()
+    for dst, src in ((7, 3), (25, 3), (31, 12), (2, 12)):
+        m[dst] = m[src]
+    idx, cnt = _lists_from_mask(m)
+    x0 = rng.standard_normal((1, nqb, 2))
+    X, ang, order = oracle.spectral_order(idx, cnt, nkb, x0, iters=12)
+    np.testing.assert_allclose(ang[0], np.arctan2(X[0][:, 1], X[0][:, 0]), rtol=0, atol=1e-12)
+    assert ang[0][3] == ang[0][7] == ang[0][25] and ang[0][2] == ang[0][12] == ang[0][31]
+    pos = {int(r): s for s, r in enumerate(order[0])}
+    assert pos[3] < pos[7] < pos[25] and pos[2] < pos[12] < pos[31]
+    assert [pos[r] for r in (3, 7, 25)] == list(range(pos[3], pos[3] + 3))
+
+
 # --------------------------------------------------------------------------
 # Block scores from block means (MC-Sparse mean-pooled score; InstaGen
 # centroid score exp(q_g . k_c / sqrt d)).
@@ -574,11 +594,13 @@ def test_block_scores_ignore_order_inside_a_block_and_follow_maps():
                        for _ in range(H)]).astype(np.int32)
     np.testing.assert_allclose(oracle.block_scores(q, k, q_map=within, kv_map=within),
                                oracle.block_scores(q, k), rtol=0, atol=1e-12)
-    # a map equals scoring the physically gathered tensors
+    # maps equal scoring the physically gathered tensors: query groups follow
+    # q_map and key clusters kv_map, two independent maps
     perm = np.stack([rng.permutation(N) for _ in range(H)]).astype(np.int32)
+    perm_k = np.stack([rng.permutation(N) for _ in range(H)]).astype(np.int32)
     qg = torch.stack([q[0, h][torch.from_numpy(perm[h]).long()] for h in range(H)])[None]
-    kg = torch.stack([k[0, h][torch.from_numpy(perm[h]).long()] for h in range(H)])[None]
-    np.testing.assert_allclose(oracle.block_scores(q, k, q_map=perm, kv_map=perm),
+    kg = torch.stack([k[0, h][torch.from_numpy(perm_k[h]).long()] for h in range(H)])[None]
+    np.testing.assert_allclose(oracle.block_scores(q, k, q_map=perm, kv_map=perm_k),
                                oracle.block_scores(qg, kg), rtol=0, atol=1e-12)
 
 
