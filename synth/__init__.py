@@ -26,8 +26,9 @@ structure the pages describe):
                  (InstaGen section 3.2.1).
 * ``dynamic``    long-video shape: H24 N118784 D128; Q/K carry per-cluster /
                  per-block offsets so that query blocks fall into 8 shuffled
-                 low-rank access clusters; block scores are mean-pooled QK^T;
-                 per-row k ~ U{ceil(0.10 nB) .. floor(0.20 nB)}.
+                 low-rank access clusters; block scores are the planted
+                 cluster-block affinity plus seeded noise (drawn, not pooled
+                 from the tokens); per-row k ~ U{ceil(0.10 nB) .. floor(0.20 nB)}.
 * ``long_video`` the same at N401408 (401 latent frames), H2: one head's K/V
                  exceeds the L2 (WaveAlign's longest Wan2.1 workload).
 * ``llm``, ``llm_window``  LLaMA-3.1-8B prefill shapes (32 query heads over 8
@@ -190,12 +191,18 @@ def dynamic(seed: int = 5, B: int = 1, H: int = 24, N: int = 118784, D: int = 12
     k = kf.to(torch.bfloat16).reshape(B, H, N, D)
     del kf
     v = normal_bf16(g, (B, H, N, D))
-    # mean-pooled block scores (block-sparse attention baseline scoring), fp64 -> fp32
-    qm = q.reshape(BH, nb, BLOCK, D).to(torch.float64).mean(2)
-    km = k.reshape(BH, nb, BLOCK, D).to(torch.float64).mean(2)
-    scores = (torch.bmm(qm, km.transpose(1, 2)) / math.sqrt(D)).to(torch.float32)
     k_lo, k_hi = math.ceil(lo * nb), math.floor(hi * nb)
     kpr = torch.randint(k_lo, k_hi + 1, (BH * nb,), generator=g, dtype=torch.int32).numpy()
+    # Block scores, an input of the top-k selection: the planted affinity
+    # a_c(qb) . b_kb / sqrt(D) of the query block's cluster offset with the key
+    # block's offset, plus N(0, 1/64) noise, about the spread that the token
+    # noise of a 128-row block adds to its mean (fp64, rounded to fp32).
+    # Scoring blocks from the tokens themselves is the library's block-score
+    # step and the oracle's, not the generator's.
+    a_q = a.double()[torch.arange(BH)[:, None], torch.from_numpy(cl)]
+    affinity = torch.bmm(a_q, b.double().transpose(1, 2)) / math.sqrt(D)
+    noise = torch.randn((BH, nb, nb), generator=g, dtype=torch.float64) / 8
+    scores = (affinity + noise).to(torch.float32)
     prob = Problem("dynamic", B, H, N, D, q, k, v, scores=scores.reshape(BH * nb, nb).numpy(),
                    k_per_row=kpr)
     prob.extra["clusters"] = cl
