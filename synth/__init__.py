@@ -279,7 +279,7 @@ CONFIG_NAMES = {
     2: "threshold-map mask B1 H12 N32768 D128, T~U(0,1) + frame band, p=0.15",
     3: "Scatter/Gather maps B1 H24 N16384 D128, T=R=128, one block per query block",
     4: "permuted exact top-16 + 8 PPS-sampled blocks B1 H40 N75776 D128",
-    5: "dynamic top-k (10-20%) of mean-pooled scores, 8 shuffled clusters, B1 H24 N118784 D128",
+    5: "dynamic top-k (10-20%) of cluster-structured block scores, 8 shuffled clusters, B1 H24 N118784 D128",
     6: "dynamic top-k (10-20%), 8 shuffled clusters, long video B1 H2 N401408 D128",
     7: "causal block-level layer (every second 256-token block) B1 H32 H_kv8 N16384 D128",
     8: "causal sliding window 575 + 64 sinks B1 H32 H_kv8 N16384 D128",

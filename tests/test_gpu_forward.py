@@ -170,7 +170,7 @@ def test_sampled_config_full_size():
 
 
 def test_dynamic_config_full_size_reordered_equals_identity():
-    prob = synth.dynamic(seed=5)  # H24 N118784, per-row top-k of mean-pooled scores
+    prob = synth.dynamic(seed=5)  # H24 N118784, per-row top-k of cluster-structured scores
     idx, cnt, _ = gpu_index(prob)
     heads = prob.B * prob.H
     rp = torch.empty((heads, prob.nqb), dtype=torch.int32, device=DEV)
