@@ -7,7 +7,6 @@ stream.  No arithmetic of the method happens here.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -604,4 +603,4 @@ __all__ = ["BLOCK", "BsaError", "IDX_MASK_U8", "IDX_THRESHOLD_F32", "IDX_TOPK_F3
            "gather0_layout",
            "spectral_order", "spectral_order_workspace_size", "spectral_order_noalloc",
            "NOALLOC_SCRATCH_BYTES", "reorder_guard",
-           "selftest_exp2", "selftest_wait_timeout", "math"]
+           "selftest_exp2", "selftest_wait_timeout"]
