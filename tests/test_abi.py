@@ -230,3 +230,24 @@ def test_row_counts_beyond_one_launch_are_rejected(lib):
                                  None) == 1
     assert lib.bsa_upscale_threshold(FAKE, 1, 4, 4, 65536, 4, FAKE, None) == 1
     assert lib.bsa_upscale_threshold(FAKE, 65536, 4, 4, 4, 4, FAKE, None) == 1
+
+
+def test_plain_c_client_builds_links_and_runs(lib, tmp_path):
+    """The headers compile as C99 and a C program links libbsa.so and calls
+    it (only calls that need no GPU)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    exe = str(tmp_path / "client")
+    libdir = os.path.dirname(bsa.lib_path())
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-I", os.path.join(ROOT, "include"), os.path.join(ROOT, "tests", "c_abi_client.c"),
+                    "-L", libdir, "-lbsa", "-Wl,-rpath," + libdir, "-o", exe], check=True)
+    out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
+    assert out[0] == "BSA_ERR_BOUNDS"
+    assert out[1] == "0"
+    N, N_kv, max_kv = (int(x) for x in out[2].split())
+    assert (N, N_kv) == (512 + 128 * 128, 512 + 5 * 128 * 128) and max_kv > 0
+    assert out[3] == "2"  # BSA_ERR_UNSUPPORTED
+    assert out[4] == "0"
