@@ -158,10 +158,20 @@ def _flat(t, name, n, dtype):
         raise ValueError(f"{name}: {t.numel()} entries, expected >= {n}")
 
 
+def _current_device(dev):
+    """The library launches on, and keeps its status word for, the current
+    CUDA device: tensors elsewhere would be read by another device's kernels."""
+    import torch
+    if dev.type == "cuda" and dev.index is not None and dev.index != torch.cuda.current_device():
+        raise ValueError(f"tensors on {dev} but the current device is cuda:{torch.cuda.current_device()}: "
+                         "call torch.cuda.set_device first")
+
+
 def _same_device(ref, *ts):
     for t in ts:
         if t is not None and t.device != ref.device:
             raise ValueError(f"tensors on {t.device} and {ref.device}: all must be on one device")
+    _current_device(ref.device)
 
 
 def _lists(B, H, N, kv_idx, kv_cnt, log_w=None, row_perm=None, lse=None):
@@ -494,7 +504,8 @@ def gather0_layout(img_h: int, img_w: int, n_text: int, groups: int, heads: int,
     kv_idx / quad_mask [heads*N/128, max_kv] and kv_cnt, built on the GPU."""
     import torch
     N, N_kv, max_kv = gather0_sizes(img_h, img_w, n_text, groups)
-    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    _current_device(dev)
     rows = heads * (N // BLOCK)
     q_map = torch.empty((heads, N), dtype=torch.int32, device=dev)
     kv_map = torch.empty((heads, N_kv), dtype=torch.int32, device=dev)

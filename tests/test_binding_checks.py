@@ -2,7 +2,8 @@
 
 The C-ABI takes plain pointers and cannot see how large a buffer is, so the
 binding rejects, before any launch, buffers smaller than what the kernels
-touch, index arrays of another dtype and tensors on different devices.
+touch, index arrays of another dtype, and tensors on different devices or
+not on the current device.
 With CPU tensors every accepted call stops at the binding's "expected a CUDA
 tensor" step, so the tests tell an accepted call (that message) from a
 rejected one (any other error).  The accepted shapes are the ones the GPU
@@ -249,3 +250,17 @@ def test_block_scores_and_upscale():
     rejected(bsa.block_scores, q, bf16(B, 2, N, D), f32(ROWS, NQB), workspace=ws, match="shape")
     accepted(bsa.upscale_threshold, f32(2, 3, 4), f32(2, 6, 8))
     rejected(bsa.upscale_threshold, f32(2, 3, 4), f32(3, 6, 8), match="heads")
+
+
+def test_tensors_must_be_on_the_current_device(monkeypatch):
+    """The kernels run on the current device: tensors of another device are
+    refused (checked with device objects; no GPU needed)."""
+    from long_context_mask_gb300 import binding
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 1)
+    with pytest.raises(ValueError, match="current device"):
+        binding._current_device(torch.device("cuda", 0))
+    binding._current_device(torch.device("cuda", 1))
+    binding._current_device(torch.device("cuda"))     # no index: allocated on the current device
+    binding._current_device(torch.device("cpu"))      # stops later, at the CUDA pointer step
+    with pytest.raises(ValueError, match="current device"):
+        bsa.gather0_layout(32, 32, 128, 2, 1, device="cuda:0")
