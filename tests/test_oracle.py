@@ -60,6 +60,26 @@ def test_all_ones_mask_is_dense_softmax_attention(D):
         np.testing.assert_allclose(lse, ref_l, rtol=0, atol=1e-12)
 
 
+def test_caller_scale_is_the_logit_factor():
+    """A caller-given scale c replaces 1/sqrt(D): dense softmax(c Q K^T) V in
+    matrix form; the default equals c = 1/sqrt(D) exactly."""
+    B, H, N, D = 1, 1, 256, 32
+    q, k, v = (_bf16((B, H, N, D), s) for s in (4, 5, 6))
+    idx, cnt = _all_blocks(2, 2)
+    Q, K, V = _f64(q[0, 0]), _f64(k[0, 0]), _f64(v[0, 0])
+    for c in (0.05, 0.5):
+        O, L, tok = oracle.attention(q, k, v, idx, cnt, scale=c)
+        o, lse = _by_token(O, L, tok, N)
+        logits = c * (Q @ K.T)
+        mx = logits.max(1, keepdims=True)
+        z = np.exp(logits - mx).sum(1, keepdims=True)
+        np.testing.assert_allclose(o, (np.exp(logits - mx) / z) @ V, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse, (mx + np.log(z))[:, 0], rtol=0, atol=1e-12)
+    O0, L0, _ = oracle.attention(q, k, v, idx, cnt)
+    O1, L1, _ = oracle.attention(q, k, v, idx, cnt, scale=1.0 / math.sqrt(D))
+    assert np.array_equal(O0, O1) and np.array_equal(L0, L1)
+
+
 def test_block_of_identical_keys_gives_its_value_exactly():
     """All 128 keys of the only listed block equal k and all values equal v:
     O = v and LSE = q.k*scale + ln 128 (closed form; fp64 rounding of the
