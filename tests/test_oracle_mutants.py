@@ -41,6 +41,8 @@ MUTANTS = [
     ("attention scale 1/D", "if (scale <= 0.0) scale = 1.0 / sqrt((double)D);\n    if (n_valid <= 0)",
      "if (scale <= 0.0) scale = 1.0 / (double)D;\n    if (n_valid <= 0)",
      [O + "test_all_ones_mask_is_dense_softmax_attention"]),
+    ("caller scale ignored", "if (scale <= 0.0) scale = 1.0 / sqrt((double)D);\n    if (n_valid <= 0)",
+     "scale = 1.0 / sqrt((double)D);\n    if (n_valid <= 0)", [O + "test_caller_scale_is_the_logit_factor"]),
     ("attention log-weight dropped", "visible ? dot * scale + lw : -INFINITY", "visible ? dot * scale : -INFINITY",
      [O + "test_log_weight_is_a_multiplicative_key_weight"]),
     ("attention log-weight subtracted", "visible ? dot * scale + lw : -INFINITY",
