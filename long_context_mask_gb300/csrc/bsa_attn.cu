@@ -91,7 +91,12 @@ constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kDefaultPoly = 0;            // exponentials per 8 on the FMA pipe
-constexpr float kRescaleThreshold = 8.0f;  // rescale O only when the max grows by > 2^8
+constexpr float kRescaleThreshold = 8.0f;  // blocks that compute their maximum rescale O when it grows by > 2^8
+// A block's exponentials are taken against the running maximum without
+// computing the block's own maximum; only a block whose exponentials sum
+// above 2^64 (or to inf / NaN) is redone with its maximum.  That bound keeps
+// P (bf16), the row sum and O (fp32) far from overflow.
+constexpr float kSumBound = 18446744073709551616.0f;  // 2^64
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kExtraProducerWarp = 6;  // warps 6, 7 also copy gathered K/V rows
@@ -170,6 +175,118 @@ __device__ __forceinline__ uint32_t run_bits(int32_t lo, int32_t hi) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Two fp32 values in one 64-bit register pair, and the packed f32x2
+// arithmetic of sm_100+ (each lane rounds exactly as fmaf / +).
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t r, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Largest of a row's 128 raw scores.
+__device__ __forceinline__ float max128(const uint32_t (&s)[128]) {
+    float a = -INFINITY, b = -INFINITY, c = -INFINITY, d = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 128; i += 8) {
+        a = fmax3(a, __uint_as_float(s[i + 0]), __uint_as_float(s[i + 1]));
+        b = fmax3(b, __uint_as_float(s[i + 2]), __uint_as_float(s[i + 3]));
+        c = fmax3(c, __uint_as_float(s[i + 4]), __uint_as_float(s[i + 5]));
+        d = fmax3(d, __uint_as_float(s[i + 6]), __uint_as_float(s[i + 7]));
+    }
+    return fmaxf(fmaxf(a, b), fmaxf(c, d));
+}
+
+// P = 2^(s * sl2 + bias) for a row's 128 scores, packed as bf16 pairs into
+// s[0..63]; returns their fp32 sum.  The affine step and the sum run two
+// columns per instruction; columns c with c % 8 < kPoly take the FMA-pipe
+// exponential instead of ex2.approx.
+template <int kPoly>
+__device__ __forceinline__ float exp128(uint32_t (&s)[128], float sl2, float bias) {
+    const uint64_t a2 = f2pack(sl2, sl2), b2 = f2pack(bias, bias);
+    uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
+#pragma unroll
+    for (int c = 0; c < 128; c += 8) {
+        float x[8];
+#pragma unroll
+        for (int i = 0; i < 8; i += 2)
+            f2unpack(fma2(f2pack(__uint_as_float(s[c + i]), __uint_as_float(s[c + i + 1])), a2, b2), x[i], x[i + 1]);
+        float p[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) p[i] = (i < kPoly) ? exp2_fma(x[i]) : ex2(x[i]);
+        acc0 = add2(acc0, f2pack(p[0], p[1]));
+        acc1 = add2(acc1, f2pack(p[2], p[3]));
+        acc2 = add2(acc2, f2pack(p[4], p[5]));
+        acc3 = add2(acc3, f2pack(p[6], p[7]));
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) s[c / 2 + i / 2] = pack_bf16(p[i], p[i + 1]);
+    }
+    float lo, hi;
+    f2unpack(add2(add2(acc0, acc1), add2(acc2, acc3)), lo, hi);
+    return lo + hi;
+}
+
+// One block of the online softmax for this thread's row.  On entry s holds
+// the row's 128 raw scores of block j (dropped keys -inf); on exit s[0..63]
+// holds P_j as bf16 pairs.  m is the running maximum (log2 domain, scale and
+// log-weight applied), l the running sum.  The first block of a row, and a
+// block while the row has seen no key (m = -inf, masked rows), compute the
+// block maximum and rescale when it grows by more than 2^8; other blocks take
+// their exponentials against m directly and fall back to the maximum only if
+// their sum leaves (0, 2^64] as a whole (reload() then refills s with the raw
+// scores).  Returns true when O must be multiplied by alpha before P_j V_j is
+// added; the decision is warp-uniform (the rescale's tensor-memory accesses
+// are warp-wide).
+template <int kPoly, bool kMask, typename Reload>
+__device__ __forceinline__ bool softmax_block(uint32_t (&s)[128], int32_t j, float sl2, float lw2, float& m,
+                                              float& l, float& alpha, Reload&& reload) {
+    alpha = 1.0f;
+    if (j > 0 && !__any_sync(0xffffffffu, m == -INFINITY)) {
+        const float l_blk = exp128<kPoly>(s, sl2, lw2 - m);
+        if (!__any_sync(0xffffffffu, !(l_blk <= kSumBound))) {
+            l += l_blk;
+            return false;
+        }
+        reload();  // rare: some row's block outgrew the running maximum by ~2^57
+    }
+    const float mt = max128(s) * sl2 + lw2;
+    bool rescale = false;
+    if (j == 0) {
+        m = mt;
+    } else {
+        rescale = __any_sync(0xffffffffu, mt > m + kRescaleThreshold);
+        if (rescale) {
+            const float m_new = fmaxf(m, mt);
+            // a row with every key so far dropped has l = 0 and O = 0
+            alpha = (kMask && m == -INFINITY) ? 0.0f : ex2(m - m_new);
+            l *= alpha;
+            m = m_new;
+        }
+    }
+    // a row with every key so far dropped keeps m = -inf: its exponentials
+    // are all 0 (avoid -inf - -inf)
+    const float bias = lw2 - ((kMask && m == -INFINITY) ? 0.0f : m);
+    l += exp128<kPoly>(s, sl2, bias);
+    return rescale;
 }
 
 __device__ __forceinline__ bool aborted(const Barriers* b) {
@@ -722,62 +839,24 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
                 continue;
             }
             uint32_t s[128];
-            tmem_ld32(t_lane + sbuf + 0, &s[0]);
-            tmem_ld32(t_lane + sbuf + 32, &s[32]);
-            tmem_ld32(t_lane + sbuf + 64, &s[64]);
-            tmem_ld32(t_lane + sbuf + 96, &s[96]);
-            tmem_wait_ld();
-            if constexpr (kMask) {
-                if (__any_sync(0xffffffffu, need_mask)) {
-                    const uint32_t ninf = __float_as_uint(-INFINITY);
+            // S_j out of tensor memory, dropped keys set to -inf
+            auto load_s = [&]() {
+                tmem_ld32(t_lane + sbuf + 0, &s[0]);
+                tmem_ld32(t_lane + sbuf + 32, &s[32]);
+                tmem_ld32(t_lane + sbuf + 64, &s[64]);
+                tmem_ld32(t_lane + sbuf + 96, &s[96]);
+                tmem_wait_ld();
+                if constexpr (kMask) {
+                    if (__any_sync(0xffffffffu, need_mask)) {
+                        const uint32_t ninf = __float_as_uint(-INFINITY);
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) s[c] = ((vis_w[c >> 5] >> (c & 31)) & 1u) ? s[c] : ninf;
+                        for (int c = 0; c < 128; ++c) s[c] = ((vis_w[c >> 5] >> (c & 31)) & 1u) ? s[c] : ninf;
+                    }
                 }
-            }
-            float mx0 = __uint_as_float(s[0]), mx1 = __uint_as_float(s[1]);
-            float mx2 = __uint_as_float(s[2]), mx3 = __uint_as_float(s[3]);
-#pragma unroll
-            for (int c = 4; c < 128; c += 4) {
-                mx0 = fmaxf(mx0, __uint_as_float(s[c + 0]));
-                mx1 = fmaxf(mx1, __uint_as_float(s[c + 1]));
-                mx2 = fmaxf(mx2, __uint_as_float(s[c + 2]));
-                mx3 = fmaxf(mx3, __uint_as_float(s[c + 3]));
-            }
-            const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2 + lw2;
-            // warp-uniform: the tcgen05 loads/stores of the rescale are warp-wide
-            const bool rescale = j > 0 && __any_sync(0xffffffffu, mt > m + kRescaleThreshold);
-            float alpha = 1.0f;
-            if (j == 0) {
-                m = mt;
-            } else if (rescale) {
-                const float m_new = fmaxf(m, mt);
-                // a row with every key so far dropped has l = 0 and O = 0
-                alpha = (kMask && m == -INFINITY) ? 0.0f : ex2(m - m_new);
-                l *= alpha;
-                m = m_new;
-            }
-            // a row with every key so far dropped keeps m = -inf: its exponentials
-            // are all 0 (avoid -inf - -inf)
-            const float bias = lw2 - ((kMask && m == -INFINITY) ? 0.0f : m);
-            float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-#pragma unroll
-            for (int c = 0; c < 128; c += 4) {
-                const float x0 = fmaf(__uint_as_float(s[c + 0]), sl2, bias);
-                const float x1 = fmaf(__uint_as_float(s[c + 1]), sl2, bias);
-                const float x2 = fmaf(__uint_as_float(s[c + 2]), sl2, bias);
-                const float x3 = fmaf(__uint_as_float(s[c + 3]), sl2, bias);
-                const float p0 = ((c + 0) % 8) < kPoly ? exp2_fma(x0) : ex2(x0);
-                const float p1 = ((c + 1) % 8) < kPoly ? exp2_fma(x1) : ex2(x1);
-                const float p2 = ((c + 2) % 8) < kPoly ? exp2_fma(x2) : ex2(x2);
-                const float p3 = ((c + 3) % 8) < kPoly ? exp2_fma(x3) : ex2(x3);
-                l0 += p0;
-                l1 += p1;
-                l2 += p2;
-                l3 += p3;
-                s[c / 2] = pack_bf16(p0, p1);
-                s[c / 2 + 1] = pack_bf16(p2, p3);
-            }
-            l += (l0 + l1) + (l2 + l3);
+            };
+            load_s();
+            float alpha;
+            const bool rescale = softmax_block<kPoly, kMask>(s, j, sl2, lw2, m, l, alpha, load_s);
             tmem_st32(t_lane + sbuf + 0, &s[0]);
             tmem_st32(t_lane + sbuf + 32, &s[32]);
             if (rescale) {
@@ -1259,60 +1338,24 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
                     continue;
                 }
                 uint32_t s[128];
-                tmem_ld32(t_lane + sbuf + 0, &s[0]);
-                tmem_ld32(t_lane + sbuf + 32, &s[32]);
-                tmem_ld32(t_lane + sbuf + 64, &s[64]);
-                tmem_ld32(t_lane + sbuf + 96, &s[96]);
-                tmem_wait_ld();
-                if constexpr (kMask && !kGeom) {
-                    if (__any_sync(0xffffffffu, need_mask)) {
-                        const uint32_t ninf = __float_as_uint(-INFINITY);
+                // S_j out of tensor memory, dropped keys set to -inf
+                auto load_s = [&]() {
+                    tmem_ld32(t_lane + sbuf + 0, &s[0]);
+                    tmem_ld32(t_lane + sbuf + 32, &s[32]);
+                    tmem_ld32(t_lane + sbuf + 64, &s[64]);
+                    tmem_ld32(t_lane + sbuf + 96, &s[96]);
+                    tmem_wait_ld();
+                    if constexpr (kMask && !kGeom) {
+                        if (__any_sync(0xffffffffu, need_mask)) {
+                            const uint32_t ninf = __float_as_uint(-INFINITY);
 #pragma unroll
-                        for (int c = 0; c < 128; ++c) s[c] = ((vis_w[c >> 5] >> (c & 31)) & 1u) ? s[c] : ninf;
+                            for (int c = 0; c < 128; ++c) s[c] = ((vis_w[c >> 5] >> (c & 31)) & 1u) ? s[c] : ninf;
+                        }
                     }
-                }
-                float mx0 = __uint_as_float(s[0]), mx1 = __uint_as_float(s[1]);
-                float mx2 = __uint_as_float(s[2]), mx3 = __uint_as_float(s[3]);
-#pragma unroll
-                for (int c = 4; c < 128; c += 4) {
-                    mx0 = fmaxf(mx0, __uint_as_float(s[c + 0]));
-                    mx1 = fmaxf(mx1, __uint_as_float(s[c + 1]));
-                    mx2 = fmaxf(mx2, __uint_as_float(s[c + 2]));
-                    mx3 = fmaxf(mx3, __uint_as_float(s[c + 3]));
-                }
-                const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2 + lw2;
-                const bool rescale = j > 0 && __any_sync(0xffffffffu, mt > m + kRescaleThreshold);
-                float alpha = 1.0f;
-                if (j == 0) {
-                    m = mt;
-                } else if (rescale) {
-                    const float m_new = fmaxf(m, mt);
-                    // a row with every key so far dropped has l = 0 and O = 0
-                    alpha = (kMask && m == -INFINITY) ? 0.0f : ex2(m - m_new);
-                    l *= alpha;
-                    m = m_new;
-                }
-                // a row with every key so far dropped keeps m = -inf (avoid -inf - -inf)
-                const float bias = lw2 - ((kMask && m == -INFINITY) ? 0.0f : m);
-                float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-#pragma unroll
-                for (int c = 0; c < 128; c += 4) {
-                    const float x0 = fmaf(__uint_as_float(s[c + 0]), sl2, bias);
-                    const float x1 = fmaf(__uint_as_float(s[c + 1]), sl2, bias);
-                    const float x2 = fmaf(__uint_as_float(s[c + 2]), sl2, bias);
-                    const float x3 = fmaf(__uint_as_float(s[c + 3]), sl2, bias);
-                    const float p0 = ((c + 0) % 8) < kPoly ? exp2_fma(x0) : ex2(x0);
-                    const float p1 = ((c + 1) % 8) < kPoly ? exp2_fma(x1) : ex2(x1);
-                    const float p2 = ((c + 2) % 8) < kPoly ? exp2_fma(x2) : ex2(x2);
-                    const float p3 = ((c + 3) % 8) < kPoly ? exp2_fma(x3) : ex2(x3);
-                    l0 += p0;
-                    l1 += p1;
-                    l2 += p2;
-                    l3 += p3;
-                    s[c / 2] = pack_bf16(p0, p1);
-                    s[c / 2 + 1] = pack_bf16(p2, p3);
-                }
-                l += (l0 + l1) + (l2 + l3);
+                };
+                load_s();
+                float alpha;
+                const bool rescale = softmax_block<kPoly, kMask>(s, j, sl2, lw2, m, l, alpha, load_s);
                 tmem_st32(t_lane + sbuf + 0, &s[0]);
                 tmem_st32(t_lane + sbuf + 32, &s[32]);
                 if (rescale) {
