@@ -2,17 +2,21 @@
 """Benchmark: block-sparse attention forward on one GB300 (per rank).
 
 One step = one pass of the whole path over one synthetic workload resident
-in HBM: index-list construction (threshold map, mask or top-k scores, plus
-sampling where the workload has it) -> query-row reordering -> block-sparse
-attention forward.  The metric is effective TFLOP/s: 4 * 128 * 128 * D FLOPs
+in HBM: block scoring (mean-pooled Q/K blocks, for the dynamic workloads) ->
+index-list construction (threshold map, mask or top-k scores, plus sampling
+where the workload has it) -> query-row reordering (when the reorder guard
+says it pays) -> block-sparse attention forward.  The default workload is the
+dynamic one (B1 H24 N118784 D128, top-k of mean-pooled QK^T at 10-20 %
+density), the largest that the benchmark configurations give one GPU.  The metric is effective TFLOP/s: 4 * 128 * 128 * D FLOPs
 per computed (query block, KV block) pair, divided by the step time; for the
 Gather 0 image layer (config 9) 4 * D FLOPs per attended query-key pair.  The
 roofline object reports the forward kernel against the measured bf16 peak,
 or against the measured HBM copy bandwidth when the workload's FLOPs per
 compulsory byte fall below the ridge (the one-pair Scatter layer).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2]
-                    [--order reordered|identity] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 5]
+                    [--order auto|identity|reordered|spectral] [--scores auto|pooled|given]
+                    [--impl ours|reference]
 
 --impl reference times the fp64 CPU oracle on a bounded sample of the same
 workload (the reference arm of this comparison).  Under torchrun each rank
@@ -69,21 +73,22 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(args):
+def recorded_traffic(args, order: str):
     """DRAM bytes per forward launch from a committed ncu capture, if it was
-    taken on the current kernel source and on this exact workload (the default
-    options of that configuration), else None."""
+    taken on the current kernel source, on this exact workload (the default
+    options of that configuration) and in the row order this run uses; else
+    None."""
     p = os.path.join(ROOT, "profiles", "forward_traffic.json")
     if not os.path.exists(p):
         return None
-    default_run = (args.heads is None and not args.dense and not args.crm and not args.scores_on_gpu
-                   and args.order == "reordered" and args.kv_gather == "auto")
+    default_run = (args.heads is None and not args.dense and not args.crm and args.scores == "auto"
+                   and args.order == "auto" and args.kv_gather == "auto")
     if not default_run:
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(f"config{args.config}")
-    if not e or e.get("kernel_hash") != kernel_source_hash():
+    if not e or e.get("kernel_hash") != kernel_source_hash() or e.get("order") != order:
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -267,15 +272,18 @@ class Path:
             self.q, self.k, self.v, self.src, self.q_map, self.kv_map, self.k_per_row, self.u)
         return [t for t in ts if t is not None]
 
-    def attend(self):
+    def attend(self, row_perm="auto"):
+        """The forward launch; row_perm overrides the path's row order (None:
+        input order) for the order comparison."""
+        if isinstance(row_perm, str):
+            row_perm = None if self.order == "identity" else self.row_perm
         if self.scatter_boxes:
             idx, cnt = self.lists()
             self.bsa.forward_scatter(self.q, self.k, self.v, self.prob.scatter_R, idx, cnt, self.o, self.lse,
-                                     log_w=self.lw,
-                                     row_perm=None if self.order == "identity" else self.row_perm)
+                                     log_w=self.lw, row_perm=row_perm)
             return
         if self.image:
-            perm = None if self.order == "identity" else self.row_perm
+            perm = row_perm
             p = self.prob
             if self.image_boxes:
                 self.bsa.forward_gather0(self.q, self.k, self.v, p.img_h, p.img_w, p.n_text, p.groups,
@@ -295,13 +303,17 @@ class Path:
             k, v, kv_map = self.kg, self.vg, None
         if self.masked:
             self.bsa.forward_masked(self.q, k, v, idx, cnt, self.o, self.lse, log_w=self.lw,
-                                    q_map=self.q_map, kv_map=kv_map,
-                                    row_perm=None if self.order == "identity" else self.row_perm,
+                                    q_map=self.q_map, kv_map=kv_map, row_perm=row_perm,
                                     **token_mask(self.prob))
             return
         self.bsa.forward(self.q, k, v, idx, cnt, self.o, self.lse, log_w=self.lw,
-                         q_map=self.q_map, kv_map=kv_map,
-                         row_perm=None if self.order == "identity" else self.row_perm)
+                         q_map=self.q_map, kv_map=kv_map, row_perm=row_perm)
+
+    def wave_order(self, out):
+        """The NNZ wave sort of the current lists into `out` (for the order
+        comparison and the guard's cost measurement)."""
+        _, cnt = self.lists()
+        self.bsa.reorder_rows(cnt.reshape(self.heads, self.prob.nqb), self.wave, out)
 
     def prepare_kv(self):
         """Keys/values into gathered order in HBM (only when pre-gathering)."""
@@ -335,15 +347,30 @@ def make_problem(config: int, heads: int | None, dense: bool = False):
 
 
 # ---------------------------------------------------------------- CPU oracle timing
+def sample_heads(prob):
+    """Heads the oracle samples: every head of the small workloads; the first
+    and the last head of those whose heads take the oracle a minute or more
+    each (the per-head rate is the same for every head)."""
+    bh = prob.B * prob.H
+    per_head_flops = float(prob.nqb) * prob.nqb * 4 * 128 * 128 * prob.D * 0.3
+    return None if per_head_flops < 2e12 or bh <= 2 else (0, bh - 1)
+
+
 def time_oracle(prob, lists, budget_s: float, max_blocks: int | None = None, seed: int = 0):
-    """Oracle on a bounded sample of query blocks (spread over heads, seeded).
-    Returns (effective TFLOP/s, seconds, blocks, threads)."""
+    """Oracle on a bounded sample of query blocks (seeded, spread over the
+    heads of sample_heads()).  Returns (effective TFLOP/s, seconds, blocks,
+    threads)."""
     import oracle
     if is_image_layer(prob):
         return time_oracle_image(prob, budget_s, seed)
     idx, cnt, lw = lists
     g = np.random.default_rng(seed)
-    order = g.permutation(prob.rows)
+    heads = sample_heads(prob)
+    if heads is None:
+        order = g.permutation(prob.rows)
+    else:
+        rows = np.concatenate([np.arange(h * prob.nqb, (h + 1) * prob.nqb) for h in heads])
+        order = rows[g.permutation(len(rows))]
     done, fl, t_total = 0, 0.0, 0.0
     chunk = 8
     while done < len(order):
@@ -405,8 +432,17 @@ def uses_masked_forward(prob):
             or is_image_layer(prob))
 
 
-def host_lists(prob):
-    """Index lists for the oracle, from the oracle (reference arm / CPU leg only)."""
+def uses_pooled_scores(prob, scores_arg: str, config: int) -> bool:
+    """Block scores from the tokens inside the step: the dynamic workloads by
+    default (top-k of mean-pooled QK^T), any scored workload on request."""
+    if prob.scores is None:
+        return False
+    return scores_arg == "pooled" or (scores_arg == "auto" and config in (5, 6))
+
+
+def host_lists(prob, pooled: bool = False):
+    """Index lists for the oracle, from the oracle (reference arm / CPU leg
+    only); with pooled scores the oracle scores the blocks itself."""
     import oracle
     if is_image_layer(prob):
         return None  # the Gather 0 oracle works from the layer's definition
@@ -419,7 +455,11 @@ def host_lists(prob):
         idx, cnt, _ = oracle.index_threshold(prob.T, prob.p)
     else:
         k = prob.k_per_row if prob.k_per_row is not None else prob.k_const
-        idx, cnt, _ = oracle.index_topk(prob.scores, k)
+        scores = prob.scores
+        if pooled:
+            scores = oracle.block_scores(prob.q, prob.k, prob.q_map, prob.kv_map,
+                                         mode=1 if prob.m_sample else 0).astype(np.float32)
+        idx, cnt, _ = oracle.index_topk(scores, k)
     if prob.m_sample:
         idx, cnt, lw, _ = oracle.sample_blocks(prob.scores, idx, cnt, prob.m_sample, prob.u,
                                                idx.shape[1] + prob.m_sample)
@@ -433,15 +473,18 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9])
+    ap.add_argument("--config", type=int, default=5, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9])
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller profiling case)")
-    ap.add_argument("--order", default="reordered", choices=["reordered", "identity", "spectral"],
-                    help="row order: NNZ-guided wave sort, identity, or spectral (stage 1) + wave sort")
+    ap.add_argument("--order", default="auto", choices=["auto", "reordered", "identity", "spectral"],
+                    help="row order: as the reorder guard decides (auto), NNZ-guided wave sort, "
+                         "identity, or spectral (stage 1) + wave sort")
     ap.add_argument("--crm", action="store_true",
                     help="mask / threshold workloads: CRM bitmask rows instead of index lists "
                          "(identity row order)")
-    ap.add_argument("--scores-on-gpu", action="store_true",
-                    help="score blocks from Q/K inside the step (mean-pooled; centroid for --config 4)")
+    ap.add_argument("--scores", default="auto", choices=["auto", "pooled", "given"],
+                    help="top-k / sampling scores: from Q/K inside the step (pooled: mean-pooled "
+                         "QK^T, centroid scores for --config 4) or the generator's (given); auto: "
+                         "pooled for the dynamic workloads 5 and 6")
     ap.add_argument("--dense", action="store_true",
                     help="every query block attends to every KV block (the in-build dense ceiling)")
     ap.add_argument("--kv-gather", default="auto", choices=["auto", "kernel", "hbm"],
@@ -483,13 +526,14 @@ def max_over_ranks(x: float, world: int, dev) -> float:
     return float(t.item())
 
 
-def config_dict(prob, config, order, density, world):
+def config_dict(prob, config, density, world):
     name = synth.CONFIG_NAMES[config] + (" [dense: all blocks listed]" if prob.name.endswith("+dense") else "")
     return {"workload": name, "config_id": config, "B": prob.B, "H": prob.H,
-            "N": prob.N, "D": prob.D, "block": 128, "density": round(density, 4), "order": order,
+            "N": prob.N, "D": prob.D, "block": 128, "density": round(density, 4),
             "l2": "flushed between timed steps (256 MiB write)",
             "parallelism": "one independent workload per GPU" if world > 1 else "single GPU",
-            "scores": "from Q/K inside the step" if getattr(prob, "_scores_on_gpu", False) else "given",
+            "scores": (("centroid scores of Q/K blocks" if prob.m_sample else "mean-pooled Q/K blocks")
+                       + ", inside the step") if getattr(prob, "_scores_on_gpu", False) else "given",
             "kv_sets": "CRM bitmask rows" if getattr(prob, "_crm", False) else "index lists",
             "kv_rows": getattr(prob, "_kv_rows", "contiguous"),
             **({"H_kv": prob.H_kv or prob.H, "token_mask": token_mask(prob),
@@ -512,6 +556,15 @@ def compulsory_bytes(prob):
     return float(qo + kv + prob.B * prob.H * prob.N * 4)
 
 
+def sample_text(prob):
+    heads = sample_heads(prob)
+    if is_image_layer(prob):
+        return "seeded sample over all heads"
+    if heads is None:
+        return "seeded sample over all heads"
+    return f"seeded sample of heads {heads[0]} and {heads[1]}; the rate is per query block, the same for every head"
+
+
 def sample_unit(prob):
     return "(head, CQS) query sets" if is_image_layer(prob) else "query blocks"
 
@@ -528,7 +581,9 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     prob = make_problem(args.config, args.heads, args.dense)
-    lists = host_lists(prob)
+    pooled = uses_pooled_scores(prob, args.scores, args.config)
+    prob._scores_on_gpu = pooled
+    lists = host_lists(prob, pooled)
     density = workload_density(prob, None if lists is None else lists[1].sum())
     # each step: the oracle on a bounded sample (about 1 s of CPU work)
     budget = 1.0
@@ -546,13 +601,71 @@ def run_reference(args, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": config_dict(prob, args.config, args.order, density, 1),
+            "config": config_dict(prob, args.config, density, 1),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{blocks} {sample_unit(prob)} over {args.steps} steps "
-                                       f"(~{budget:.0f} s of oracle CPU time per step)"},
+                             "sample": f"{blocks} {sample_unit(prob)} ({sample_text(prob)}) over "
+                                       f"{args.steps} steps (~{budget:.0f} s of oracle CPU time per step)"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+ORDER_OF_GUARD = {"input": "identity", "wave": "reordered", "spectral": "spectral"}
+
+
+def event_ms(fn, reps: int, flush=None) -> float:
+    """Mean device time of fn() over reps launches (CUDA events on the current
+    stream, L2 flushed before each when a flush buffer is given)."""
+    stream = torch.cuda.current_stream()
+    total = 0.0
+    for _ in range(reps):
+        if flush is not None:
+            flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        total += a.elapsed_time(b)
+    return total / reps
+
+
+def choose_order(prob, dev, args, pooled: bool, peaks: dict, flush):
+    """The row order the reorder guard picks for this workload, and the guard's
+    inputs and estimates.  The inputs are measured on this GPU: the listed
+    block pairs, the forward's rate in the input order, and what the NNZ wave
+    sort and the spectral stage cost on these lists."""
+    import long_context_mask_gb300 as bsa
+    path = Path(prob, dev, "identity", pooled, args.crm, args.kv_gather)
+    path.step()
+    torch.cuda.synchronize()
+    _, cnt = path.lists()
+    listed = int(cnt.sum().item())
+    fwd_ms = event_ms(path.attend, 3, flush)
+    rate = listed * 4.0 * 128 * 128 * prob.D / (fwd_ms * 1e-3) / 1e12 if listed else 0.0
+    perm = torch.empty_like(path.row_perm)
+    wave_ms = event_ms(lambda: path.wave_order(perm), 3)
+    idx, cnt = path.lists()
+    nqb = prob.nqb
+    # key tiles a list entry may name: blocks of the sequence, or packed tiles of the image layer
+    nkb = path.kv_map.shape[-1] // 128 if path.image else nqb
+    spectral_ms = -1.0  # the guard's estimate where the spectral stage does not apply
+    if nqb >= 2:
+        x0 = torch.from_numpy(synth.spectral_start(7, path.heads, nqb)).float().to(dev)
+        spec = torch.empty((path.heads, nqb), dtype=torch.int32, device=dev)
+        ws = torch.empty(max(1, bsa.spectral_order_workspace_size(path.heads, nqb, nkb)),
+                         dtype=torch.uint8, device=dev)
+        spectral_ms = event_ms(lambda: bsa.spectral_order(idx, cnt, nkb, x0, spec, workspace=ws, iters=10), 3)
+        del x0, spec, ws
+    g = bsa.reorder_guard(heads=path.heads, kv_heads=prob.B * (prob.H_kv or prob.H), nqb=nqb, nkb=nkb,
+                          D=prob.D, listed_blocks=listed, tensor_tflops=rate,
+                          hbm_gbs=float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
+                          wave_ms=wave_ms, spectral_ms=spectral_ms)
+    del path, perm
+    torch.cuda.empty_cache()
+    g.update({"measured_forward_ms_input_order": fwd_ms, "measured_wave_ms": wave_ms,
+              "measured_spectral_ms": spectral_ms, "listed_blocks": listed})
+    return ORDER_OF_GUARD[g["order"]], g
 
 
 def main():
@@ -569,10 +682,19 @@ def main():
     __graft_entry__.build()
     import long_context_mask_gb300 as bsa
 
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     prob = make_problem(args.config, args.heads, args.dense)
-    prob._scores_on_gpu = args.scores_on_gpu and prob.scores is not None
+    pooled = uses_pooled_scores(prob, args.scores, args.config)
+    prob._scores_on_gpu = pooled
     prob._crm = args.crm and (prob.mask is not None or prob.T is not None)
-    path = Path(prob, dev, args.order, args.scores_on_gpu, args.crm, args.kv_gather)
+    guard = None
+    order = args.order
+    if prob._crm:
+        order = "identity"
+    elif order == "auto":
+        order, guard = choose_order(prob, dev, args, pooled, peaks, flush)
+    path = Path(prob, dev, order, pooled, args.crm, args.kv_gather)
     if path.image:
         prob._kv_rows = ("tiles fetched as TMA boxes of the image / Scatter-group views "
                          "(bsa_forward_gather0)" if path.image_boxes else
@@ -586,18 +708,15 @@ def main():
     torch.cuda.synchronize()
     if args.profile_once:
         st = bsa.device_status()
-        print(json.dumps({"profile_once": True, "status": st}))
+        print(json.dumps({"profile_once": True, "status": st, "order": path.order}))
         return
 
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
     for _ in range(max(args.warmup, 3)):
         path.step()
     torch.cuda.synchronize()
     flops = path.effective_flops()
     density = workload_density(prob, path.lists()[1].sum())
-    if path.crm:
-        args.order = "identity"
 
     uuid = str(torch.cuda.get_device_properties(dev).uuid)
     gpu_id = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
@@ -626,6 +745,15 @@ def main():
             fwd_ev[i][1].record(stream)
         torch.cuda.synchronize()
         fwd_ms = [a.elapsed_time(b) for a, b in fwd_ev]
+    # ---- the forward under the input order and under the NNZ wave sort (same lists)
+    orders_ms = None
+    if not path.crm:
+        perm = torch.empty_like(path.row_perm)
+        path.wave_order(perm)
+        reps = max(3, min(K, 10))
+        orders_ms = {"identity": event_ms(lambda: path.attend(None), reps, flush),
+                     "reordered": event_ms(lambda: path.attend(perm), reps, flush)}
+        del perm
     status = bsa.device_status()
     if status != 0:
         raise SystemExit(f"device status {status} after the timed region")
@@ -639,7 +767,7 @@ def main():
     # region.  Two device buffer sets and separate copy streams let step k+1's
     # inputs travel (and step k-1's outputs come back) while step k computes.
     pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-    paths = [path, Path(prob, dev, args.order, args.scores_on_gpu, args.crm, args.kv_gather)]
+    paths = [path, Path(prob, dev, path.order, pooled, args.crm, args.kv_gather)]
 
     d_ins = [pth.host_inputs() for pth in paths]
     h_in = [pin(t) for t in d_ins[0]]
@@ -684,11 +812,10 @@ def main():
     e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
     del paths
 
-    peaks, peak_src = load_peaks()
     fwd_avg_ms = sum(fwd_ms) / len(fwd_ms)
     achieved = flops / (fwd_avg_ms * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    traffic = recorded_traffic(args)
+    traffic = recorded_traffic(args, path.order)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic, "kernel": "k_bsa_forward",
                 "peak_source": f"{peak_src} bf16 burst", "ms_per_launch": fwd_avg_ms,
@@ -708,15 +835,18 @@ def main():
         return
     cpu = None
     if not args.no_cpu_baseline:
-        v, s, b, threads = time_oracle(prob, host_lists(prob), args.cpu_budget)
+        v, s, b, threads = time_oracle(prob, host_lists(prob, pooled), args.cpu_budget)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"{b} {sample_unit(prob)} (seeded sample of the workload), "
-                         f"{s:.1f} s fp64 on host cores"}
+               "sample": f"{b} {sample_unit(prob)} ({sample_text(prob)}), "
+                         f"{s:.1f} s fp64 on host cores",
+               "full_workload_s_extrapolated": flops / (v * 1e12) if v else None}
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
             "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
             "ms_per_step_median": statistics.median(step_ms) if world == 1 else None,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": config_dict(prob, args.config, args.order, density, world),
+            "data": "synthetic", "config": config_dict(prob, args.config, density, world),
+            "row_order": {"order": path.order, "chosen_by": "reorder guard" if guard else "--order",
+                          "guard": guard, "forward_ms": orders_ms},
             "pct_of_peak": 100.0 * value / world / peak,
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": bi,

@@ -100,7 +100,8 @@ bsa_status bsa_build_index(bsa_idx_mode mode, const void* src, int64_t rows, int
  *
  *  q, k      device bf16 [B, H, N, D]; N a multiple of 128, D 8 .. 256 (x8).
  *  q_map, kv_map  device int32 [B*H, N] or NULL (as in bsa_forward).
- *  scale     <= 0 selects 1/sqrt(D).
+ *  scale     <= 0 selects 1/sqrt(D); a NaN or infinite scale is rejected
+ *            (BSA_ERR_INVALID_ARG).
  *  mode      BSA_SCORE_MEAN_DOT or BSA_SCORE_CENTROID_EXP.
  *  workspace device scratch of at least bsa_block_scores_workspace_size()
  *            bytes (the fp32 block means), 16-byte aligned.
@@ -136,6 +137,81 @@ size_t bsa_block_scores_workspace_size(int32_t B, int32_t H, int32_t N, int32_t 
  */
 bsa_status bsa_reorder_rows(const int32_t* kv_cnt, const int32_t* order_in, int64_t heads,
                             int32_t nQB, int32_t wave, int32_t* row_perm, void* stream);
+
+/*
+ * bsa_reorder_guard - whether reordering query rows pays for one forward
+ * call, and with which stages (host-side arithmetic; launches nothing).
+ *
+ * Defined by: WaveAlign, "A. Design Rationale" and "E. Runtime
+ * Coordination" of its design section (an adaptive guard skips reordering
+ * when its estimated latency reduction does not exceed its overhead); "C.
+ * Why Access Is Irregular: Two Root Causes" (reuse is lost when a wave's K/V
+ * working set overflows L2); "D. L2 Cache Locality and HBM Traffic" of its
+ * evaluation (HBM reads fall by 68.89 %-83.67 % with the intra-wave NNZ sort
+ * alone and by 80.71 %-92.11 % with both stages); "F. Other Factors"
+ * (reordering skipped at short sequences and low densities).
+ *
+ * The pages give no formula; this guard estimates the forward's latency as
+ * max(compute, DRAM traffic) for three orders and picks the one whose
+ * saving beats its cost by the most:
+ *   F   = nKB * 128 * D * 4 bytes, one head's K and V;
+ *   C   = l2_bytes / 2, the L2 share K/V keep (the rest streams Q, O and
+ *         the next head's first blocks; heads run one after another);
+ *   mu  = max(0, 1 - C / F), the fraction of K/V tile reads that miss L2 in
+ *         the input order (a head's blocks compete for C at random);
+ *   DRAM(order) = Q + O + LSE + kv_heads * F + listed_blocks * 512 * D * mu_order
+ *         with mu_input = mu, mu_wave = mu * (1 - 0.6889),
+ *         mu_spectral = mu * (1 - 0.8071) (the smallest cuts the page reports);
+ *   t(order) = max(listed_blocks * 4 * 128^2 * D / tensor rate, DRAM / HBM rate).
+ * The wave sort is chosen when t(input) - t(wave) > its cost, the spectral
+ * stage (plus wave sort) when its saving over the wave sort also beats its
+ * extra cost.  When one head's K/V fits its L2 share (mu = 0) nothing can be
+ * saved and the input order is kept.
+ *
+ *  a->heads        B*H query heads, >= 1.   a->kv_heads  B*H_kv, 1 .. heads.
+ *  a->nQB, a->nKB  query / key blocks per head, >= 1.   a->D  head dimension, >= 1.
+ *  a->listed_blocks  listed (query block, key block) pairs of the call, >= 0.
+ *  a->l2_bytes     L2 capacity in bytes; 0: the current device's.
+ *  a->tensor_tflops  effective block-pair rate of the forward (TFLOP/s);
+ *                  0: 1500.   a->hbm_gbs  DRAM bandwidth (GB/s); 0: 6800.
+ *  a->wave_ms, a->spectral_ms  measured cost of bsa_reorder_rows and of
+ *                  bsa_spectral_order for this call; a negative value asks
+ *                  for the guard's estimate (bytes moved at the HBM rate plus
+ *                  10 us per launch; the spectral stage 10 iterations).
+ *  r               host out: the decision and the estimates behind it.
+ * Returns BSA_ERR_INVALID_ARG for null pointers or sizes out of range,
+ * BSA_ERR_CUDA if l2_bytes is 0 and no device answers.
+ */
+typedef struct {
+    int64_t heads;
+    int64_t kv_heads;
+    int32_t nQB;
+    int32_t nKB;
+    int32_t D;
+    int64_t listed_blocks;
+    double l2_bytes;
+    double tensor_tflops;
+    double hbm_gbs;
+    double wave_ms;
+    double spectral_ms;
+} bsa_guard_args;
+
+typedef enum {
+    BSA_ORDER_INPUT = 0,    /* keep the input order (reordering skipped)          */
+    BSA_ORDER_WAVE = 1,     /* NNZ-guided intra-wave sort (bsa_reorder_rows)      */
+    BSA_ORDER_SPECTRAL = 2  /* spectral order, then the wave sort                 */
+} bsa_row_order;
+
+typedef struct {
+    bsa_row_order order;
+    double kv_head_bytes;   /* F */
+    double kv_cache_bytes;  /* C */
+    double miss_fraction;   /* mu */
+    double t_input_ms, t_wave_ms, t_spectral_ms;  /* estimated forward times */
+    double wave_cost_ms, spectral_cost_ms;        /* costs used */
+} bsa_guard_result;
+
+bsa_status bsa_reorder_guard(const bsa_guard_args* a, bsa_guard_result* r);
 
 /*
  * bsa_spectral_order - spatial row order from the rank-2 embedding of each
@@ -283,7 +359,8 @@ bsa_status bsa_sample_blocks(const float* scores, int64_t rows, int32_t nKB,
  *            permutation of 0..N-1 (a q_map entry outside [0, N) skips that
  *            output row and raises BSA_ERR_BOUNDS).
  *  row_perm  device int32 [B*H, nQB] or NULL (see bsa_reorder_rows).
- *  scale     logit scale; <= 0 selects 1/sqrt(D).
+ *  scale     logit scale; <= 0 selects 1/sqrt(D); a NaN or infinite scale
+ *            is rejected (BSA_ERR_INVALID_ARG).
  *  o         device bf16 [B, H, N, D] out, 16-byte aligned.
  *  lse       device fp32 [B, H, N] out.
  */
@@ -552,6 +629,40 @@ bsa_status bsa_forward_crm(const void* q, const void* k, const void* v, int32_t 
  */
 bsa_status bsa_upscale_threshold(const float* T_base, int64_t heads, int32_t Ub, int32_t Vb,
                                  int32_t Ut, int32_t Vt, float* T_target, void* stream);
+
+/*
+ * bsa_set_forward_options - how this host thread's later forward calls
+ * launch (every bsa_forward* entry point).  The result does not depend on
+ * the schedule: every choice computes the same per-row arithmetic, bit for
+ * bit.  The exponential option changes the last bits of O and LSE.
+ *
+ *  schedule   BSA_SCHEDULE_AUTO (default): per-item thread blocks for the
+ *             Scatter and Gather 0 layers and for windowed token masks that
+ *             bound every row to 16 listed blocks, one thread block per row
+ *             otherwise;  BSA_SCHEDULE_PER_ROW: one thread block per query
+ *             block always;  BSA_SCHEDULE_PER_ITEM: one thread block per SM
+ *             walking the rows wherever the per-item kernel applies (the
+ *             Scatter and Gather 0 layers, and the tile path without maps).
+ *  exp2_fma   0 (default) or 2: exponentials out of every 8 that the plain
+ *             tile path (bsa_forward without maps, masks or CRM rows)
+ *             computes on the FMA pipe (Cody-Waite reduction and a degree-3
+ *             minimax polynomial, 7.5e-5 relative error) instead of
+ *             ex2.approx; other paths ignore it.
+ * o = NULL restores the defaults.  The options are per host thread (thread
+ * local storage in the library); other threads keep theirs.
+ */
+typedef enum {
+    BSA_SCHEDULE_AUTO = 0,
+    BSA_SCHEDULE_PER_ROW = 1,
+    BSA_SCHEDULE_PER_ITEM = 2
+} bsa_schedule;
+
+typedef struct {
+    bsa_schedule schedule;
+    int32_t exp2_fma;
+} bsa_forward_options;
+
+bsa_status bsa_set_forward_options(const bsa_forward_options* o);
 
 /*
  * bsa_device_status - read and clear the status word of the current device.

@@ -37,6 +37,7 @@ from .binding import (  # noqa: F401
     reorder_rows,
     resident_ctas,
     sample_blocks,
+    set_forward_options,
     selftest_exp2,
     selftest_wait_timeout,
     spectral_order,

@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "BSA_OK", 1: "BSA_ERR_INVALID_ARG", 2: "BSA_ERR_UNSUPPORTED",
 
 EXPORTS = ("bsa_build_index", "bsa_build_crm", "bsa_forward_crm", "bsa_upscale_threshold",
            "bsa_block_scores", "bsa_block_scores_workspace_size",
-           "bsa_reorder_rows", "bsa_spectral_order",
+           "bsa_reorder_rows", "bsa_reorder_guard", "bsa_set_forward_options", "bsa_spectral_order",
            "bsa_spectral_order_workspace_size", "bsa_spectral_order_noalloc", "bsa_sample_blocks",
            "bsa_forward", "bsa_forward_masked", "bsa_forward_packed", "bsa_gather_rows",
            "bsa_gather0_sizes", "bsa_gather0_layout", "bsa_forward_gather0",
@@ -91,6 +91,10 @@ def load_library():
     lib.bsa_forward_gather0.restype = i32
     lib.bsa_forward_scatter.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, P, P, i32, P, P, f32, P, P, P]
     lib.bsa_forward_scatter.restype = i32
+    lib.bsa_set_forward_options.argtypes = [P]
+    lib.bsa_set_forward_options.restype = i32
+    lib.bsa_reorder_guard.argtypes = [P, P]
+    lib.bsa_reorder_guard.restype = i32
     lib.bsa_device_status.argtypes = [P, ctypes.POINTER(i32)]
     lib.bsa_resident_ctas.argtypes = [i32]
     lib.bsa_status_string.argtypes = [i32]
@@ -375,11 +379,53 @@ def spectral_order_noalloc(kv_idx, kv_cnt, n_kb: int, x0, order, *, x_out=None, 
     _check("bsa_spectral_order_noalloc", code)
 
 
-def reorder_guard(N: int, D: int, l2_bytes: int) -> bool:
-    """Whether row reordering can pay on this GPU: only when one head's K/V
-    (2 * N * D bf16 values) exceeds the L2, since heads run one after another
-    and a working set that fits in L2 is already reused in any row order."""
-    return 2 * N * D * 2 > l2_bytes
+class GuardArgs(ctypes.Structure):
+    _fields_ = [("heads", ctypes.c_int64), ("kv_heads", ctypes.c_int64), ("nQB", ctypes.c_int32),
+                ("nKB", ctypes.c_int32), ("D", ctypes.c_int32), ("listed_blocks", ctypes.c_int64),
+                ("l2_bytes", ctypes.c_double), ("tensor_tflops", ctypes.c_double),
+                ("hbm_gbs", ctypes.c_double), ("wave_ms", ctypes.c_double),
+                ("spectral_ms", ctypes.c_double)]
+
+
+class GuardResult(ctypes.Structure):
+    _fields_ = [("order", ctypes.c_int32), ("kv_head_bytes", ctypes.c_double),
+                ("kv_cache_bytes", ctypes.c_double), ("miss_fraction", ctypes.c_double),
+                ("t_input_ms", ctypes.c_double), ("t_wave_ms", ctypes.c_double),
+                ("t_spectral_ms", ctypes.c_double), ("wave_cost_ms", ctypes.c_double),
+                ("spectral_cost_ms", ctypes.c_double)]
+
+
+class ForwardOptions(ctypes.Structure):
+    _fields_ = [("schedule", ctypes.c_int32), ("exp2_fma", ctypes.c_int32)]
+
+
+SCHEDULES = {"auto": 0, "per_row": 1, "per_item": 2}
+
+
+def set_forward_options(schedule: str = "auto", exp2_fma: int = 0):
+    """bsa_set_forward_options for this host thread: the launch schedule of
+    later forward calls ("auto", "per_row", "per_item") and how many
+    exponentials of every 8 the plain tile path takes on the FMA pipe (0, 2)."""
+    o = ForwardOptions(SCHEDULES[schedule], int(exp2_fma))
+    _check("bsa_set_forward_options", load_library().bsa_set_forward_options(ctypes.byref(o)))
+
+
+ORDER_NAMES = {0: "input", 1: "wave", 2: "spectral"}
+
+
+def reorder_guard(*, heads: int, nqb: int, nkb: int, D: int, listed_blocks: int, kv_heads=None,
+                  l2_bytes: float = 0.0, tensor_tflops: float = 0.0, hbm_gbs: float = 0.0,
+                  wave_ms: float = -1.0, spectral_ms: float = -1.0) -> dict:
+    """bsa_reorder_guard: which row order pays for this forward call ("input",
+    "wave" or "spectral") and the estimates behind the choice (see bsa.h)."""
+    a = GuardArgs(heads, heads if kv_heads is None else kv_heads, nqb, nkb, D, int(listed_blocks),
+                  float(l2_bytes), float(tensor_tflops), float(hbm_gbs), float(wave_ms),
+                  float(spectral_ms))
+    r = GuardResult()
+    _check("bsa_reorder_guard", load_library().bsa_reorder_guard(ctypes.byref(a), ctypes.byref(r)))
+    out = {f: getattr(r, f) for f, _ in GuardResult._fields_}
+    out["order"] = ORDER_NAMES[r.order]
+    return out
 
 
 def sample_blocks(scores, exact_idx, exact_cnt, m: int, u, kv_idx, kv_cnt, log_w, *, nkb=None,
@@ -613,5 +659,5 @@ __all__ = ["BLOCK", "BsaError", "IDX_MASK_U8", "IDX_THRESHOLD_F32", "IDX_TOPK_F3
            "upscale_threshold", "gather_rows", "forward_masked", "forward_packed", "forward_gather0", "forward_scatter", "gather0_sizes",
            "gather0_layout",
            "spectral_order", "spectral_order_workspace_size", "spectral_order_noalloc",
-           "NOALLOC_SCRATCH_BYTES", "reorder_guard",
+           "NOALLOC_SCRATCH_BYTES", "reorder_guard", "set_forward_options",
            "selftest_exp2", "selftest_wait_timeout"]

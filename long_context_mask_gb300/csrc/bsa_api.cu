@@ -21,6 +21,9 @@ std::mutex g_status_mu;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// A logit scale must be finite (<= 0 selects 1/sqrt(D)).
+bool scale_ok(float s) { return s == s && s - s == 0.0f; }
+
 }  // namespace
 
 int32_t* status_word_ptr() {
@@ -38,6 +41,7 @@ int32_t* status_word_ptr() {
 }  // namespace bsa
 
 using bsa::aligned;
+using bsa::scale_ok;
 
 extern "C" {
 
@@ -96,6 +100,55 @@ bsa_status bsa_reorder_rows(const int32_t* kv_cnt, const int32_t* order_in, int6
     return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
+bsa_status bsa_reorder_guard(const bsa_guard_args* a, bsa_guard_result* r) {
+    if (!a || !r) return BSA_ERR_INVALID_ARG;
+    if (a->heads < 1 || a->kv_heads < 1 || a->kv_heads > a->heads || a->nQB < 1 || a->nKB < 1 || a->D < 1 ||
+        a->listed_blocks < 0 || !(a->l2_bytes >= 0.0) || !(a->tensor_tflops >= 0.0) || !(a->hbm_gbs >= 0.0))
+        return BSA_ERR_INVALID_ARG;
+    double l2 = a->l2_bytes;
+    if (l2 == 0.0) {
+        int dev = 0, bytes = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess || bytes <= 0)
+            return BSA_ERR_CUDA;
+        l2 = (double)bytes;
+    }
+    const double flops_rate = (a->tensor_tflops > 0.0 ? a->tensor_tflops : 1500.0) * 1e12;  // FLOP/s
+    const double bw = (a->hbm_gbs > 0.0 ? a->hbm_gbs : 6800.0) * 1e9;                       // B/s
+    const double D = a->D, listed = (double)a->listed_blocks;
+    const double rows_q = (double)a->heads * a->nQB * 128.0;  // query tokens
+    const double F = (double)a->nKB * 128.0 * D * 4.0;       // one head's K and V
+    const double C = 0.5 * l2;
+    const double mu = F > C ? 1.0 - C / F : 0.0;
+    const double tile = 512.0 * D;                           // K and V tile of one pair
+    const double compulsory = rows_q * D * 2.0 * 2.0 + rows_q * 4.0 + (double)a->kv_heads * F;
+    const double t_compute = listed * 4.0 * 128.0 * 128.0 * D / flops_rate;
+    auto t_ms = [&](double miss) {
+        const double t_mem = (compulsory + listed * tile * miss) / bw;
+        return 1e3 * (t_compute > t_mem ? t_compute : t_mem);
+    };
+    const double rows = (double)a->heads * a->nQB;
+    // the wave sort reads the counts and writes the order; the spectral stage
+    // reads the lists twice per iteration (10 iterations), then sorts per head
+    const double wave_cost = a->wave_ms >= 0.0 ? a->wave_ms : 1e3 * (rows * 8.0 / bw) + 0.01;
+    const double spec_cost =
+        a->spectral_ms >= 0.0 ? a->spectral_ms : 1e3 * (10.0 * 2.0 * 4.0 * listed / bw) + 0.01 * 32.0;
+    r->kv_head_bytes = F;
+    r->kv_cache_bytes = C;
+    r->miss_fraction = mu;
+    r->t_input_ms = t_ms(mu);
+    r->t_wave_ms = t_ms(mu * (1.0 - 0.6889));
+    r->t_spectral_ms = t_ms(mu * (1.0 - 0.8071));
+    r->wave_cost_ms = wave_cost;
+    r->spectral_cost_ms = spec_cost;
+    const double net_wave = r->t_input_ms - r->t_wave_ms - wave_cost;
+    const double net_spec = r->t_input_ms - r->t_spectral_ms - wave_cost - spec_cost;
+    r->order = BSA_ORDER_INPUT;
+    if (net_wave > 0.0 || net_spec > 0.0)
+        r->order = net_spec > net_wave ? BSA_ORDER_SPECTRAL : BSA_ORDER_WAVE;
+    return BSA_OK;
+}
+
 static bool score_sizes_ok(int32_t B, int32_t H, int32_t N, int32_t D) {
     return B >= 1 && H >= 1 && (int64_t)B * H <= 65535 && N >= 128 && (N % 128) == 0 &&
            N <= (1 << 24) && (int64_t)B * H * N < ((int64_t)1 << 31) && D >= 8 && D <= 256 &&
@@ -111,7 +164,7 @@ bsa_status bsa_block_scores(const void* q, const void* k, int32_t B, int32_t H, 
                             int32_t D, const int32_t* q_map, const int32_t* kv_map, float scale,
                             bsa_score_mode mode, void* workspace, size_t workspace_bytes,
                             float* scores, void* stream) {
-    if (!score_sizes_ok(B, H, N, D)) return BSA_ERR_INVALID_ARG;
+    if (!score_sizes_ok(B, H, N, D) || !scale_ok(scale)) return BSA_ERR_INVALID_ARG;
     if (mode != BSA_SCORE_MEAN_DOT && mode != BSA_SCORE_CENTROID_EXP) return BSA_ERR_INVALID_ARG;
     if (!q || !k || !scores || !workspace) return BSA_ERR_INVALID_ARG;
     if (workspace_bytes < bsa::block_scores_workspace_bytes((int64_t)B * H, N, D))
@@ -187,8 +240,9 @@ bsa_status check_forward(const void* q, const void* k, const void* v, int32_t B,
                          int32_t H_kv, int32_t N, int32_t D, const int32_t* kv_idx,
                          const int32_t* kv_cnt, int32_t max_kv, const float* log_w,
                          const int32_t* q_map, const int32_t* kv_map, const int32_t* row_perm,
-                         const void* o, const float* lse, int32_t nKB = 0) {
+                         const void* o, const float* lse, float scale, int32_t nKB = 0) {
     if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+    if (!scale_ok(scale)) return BSA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 128 || (N % 128) != 0 || N > (1 << 24)) return BSA_ERR_INVALID_ARG;
     if (H_kv < 1 || H_kv > H || H % H_kv != 0) return BSA_ERR_INVALID_ARG;
     const int64_t total_rows = (int64_t)B * H * N;
@@ -213,7 +267,7 @@ bsa_status bsa_forward(const void* q, const void* k, const void* v, int32_t B, i
                        const float* log_w, const int32_t* q_map, const int32_t* kv_map,
                        const int32_t* row_perm, float scale, void* o, float* lse, void* stream) {
     const bsa_status c = check_forward(q, k, v, B, H, H, N, D, kv_idx, kv_cnt, max_kv, log_w, q_map,
-                                       kv_map, row_perm, o, lse);
+                                       kv_map, row_perm, o, lse, scale);
     if (c != BSA_OK) return c;
     int32_t* status = bsa::status_word_ptr();
     if (!status) return BSA_ERR_CUDA;
@@ -230,7 +284,7 @@ bsa_status bsa_forward_masked(const void* q, const void* k, const void* v, int32
                               int32_t window, int32_t sinks, float scale, void* o, float* lse,
                               void* stream) {
     const bsa_status c = check_forward(q, k, v, B, H, H_kv, N, D, kv_idx, kv_cnt, max_kv, log_w,
-                                       q_map, kv_map, row_perm, o, lse);
+                                       q_map, kv_map, row_perm, o, lse, scale);
     if (c != BSA_OK) return c;
     if ((causal != 0 && causal != 1) || n_valid < 0 || n_valid > N || window < 0 || sinks < 0)
         return BSA_ERR_INVALID_ARG;
@@ -258,7 +312,7 @@ bsa_status bsa_forward_packed(const void* q, const void* k, const void* v, int32
         return BSA_ERR_INVALID_ARG;
     if (B >= 1 && H_kv >= 1 && (int64_t)B * H_kv * N_kv >= ((int64_t)1 << 40)) return BSA_ERR_INVALID_ARG;
     const bsa_status c = check_forward(q, k, v, B, H, H_kv, N, D, kv_idx, kv_cnt, max_kv, log_w,
-                                       q_map, kv_map, row_perm, o, lse, N_kv / 128);
+                                       q_map, kv_map, row_perm, o, lse, scale, N_kv / 128);
     if (c != BSA_OK) return c;
     if ((causal != 0 && causal != 1) || n_valid < 0 || n_valid > N || window < 0 || sinks < 0)
         return BSA_ERR_INVALID_ARG;
@@ -311,7 +365,7 @@ bsa_status bsa_forward_gather0(const void* q, const void* k, const void* v, int3
     if (!bsa::gather0_geometry(img_h, img_w, n_text, groups, &g)) return BSA_ERR_INVALID_ARG;
     if (B >= 1 && H_kv >= 1 && (int64_t)B * H_kv * g.N_kv >= ((int64_t)1 << 40)) return BSA_ERR_INVALID_ARG;
     const bsa_status c = check_forward(q, k, v, B, H, H_kv, g.N, D, kv_idx, kv_cnt, max_kv, nullptr,
-                                       nullptr, nullptr, row_perm, o, lse, g.N_kv / 128);
+                                       nullptr, nullptr, row_perm, o, lse, scale, g.N_kv / 128);
     if (c != BSA_OK) return c;
     int32_t* status = bsa::status_word_ptr();
     if (!status) return BSA_ERR_CUDA;
@@ -331,7 +385,7 @@ bsa_status bsa_forward_scatter(const void* q, const void* k, const void* v, int3
                                const int32_t* row_perm, float scale, void* o, float* lse, void* stream) {
     if (R < 1 || N < 128 || (N % R) != 0 || ((N / R) % 128) != 0) return BSA_ERR_INVALID_ARG;
     const bsa_status c = check_forward(q, k, v, B, H, H_kv, N, D, kv_idx, kv_cnt, max_kv, log_w,
-                                       nullptr, nullptr, row_perm, o, lse);
+                                       nullptr, nullptr, row_perm, o, lse, scale);
     if (c != BSA_OK) return c;
     int32_t* status = bsa::status_word_ptr();
     if (!status) return BSA_ERR_CUDA;
@@ -347,6 +401,7 @@ bsa_status bsa_forward_crm(const void* q, const void* k, const void* v, int32_t 
                            const int32_t* q_map, const int32_t* kv_map, const int32_t* row_perm,
                            float scale, void* o, float* lse, void* stream) {
     if (D != 64 && D != 128) return BSA_ERR_UNSUPPORTED;
+    if (!scale_ok(scale)) return BSA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 128 || (N % 128) != 0 || N > (1 << 24)) return BSA_ERR_INVALID_ARG;
     const int64_t total_rows = (int64_t)B * H * N;
     if (total_rows >= ((int64_t)1 << 31) || (int64_t)B * H > 65535) return BSA_ERR_INVALID_ARG;
@@ -406,6 +461,19 @@ bsa_status bsa_gather_rows(const void* src, const int32_t* map, int64_t heads, i
     cudaError_t e = bsa::launch_gather_rows(src, map, heads, N, D, dst, status,
                                             static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
+}
+
+bsa_status bsa_set_forward_options(const bsa_forward_options* o) {
+    if (o == nullptr) {
+        bsa::forward_options() = bsa_forward_options{BSA_SCHEDULE_AUTO, 0};
+        return BSA_OK;
+    }
+    if ((o->schedule != BSA_SCHEDULE_AUTO && o->schedule != BSA_SCHEDULE_PER_ROW &&
+         o->schedule != BSA_SCHEDULE_PER_ITEM) ||
+        (o->exp2_fma != 0 && o->exp2_fma != 2))
+        return BSA_ERR_INVALID_ARG;
+    bsa::forward_options() = *o;
+    return BSA_OK;
 }
 
 bsa_status bsa_device_status(void* stream, int32_t* first_error) {

@@ -90,7 +90,7 @@ using namespace ptx;
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kDefaultPoly = 0;            // exponentials per 8 on the FMA pipe
+constexpr int kDefaultPoly = 0;  // exponentials per 8 on the FMA pipe (see bsa_set_forward_options)
 constexpr float kRescaleThreshold = 8.0f;  // blocks that compute their maximum rescale O when it grows by > 2^8
 // A block's exponentials are taken against the running maximum without
 // computing the block's own maximum; only a block whose exponentials sum
@@ -1499,37 +1499,23 @@ cudaError_t prepare_kernel() {
     return e;
 }
 
-// Share of exponentials (out of every 8) computed by exp2_fma instead of
-// the MUFU unit.  BSA_EXP2_POLY=<0|2> overrides it (tuning).
-// Per-item blocks for the geometry layers (the default); BSA_ITEMS=0 runs
-// one block per row instead (tuning, comparisons).
-int items_setting() {
-    static int v = -1;
-    if (v < 0) {
-        const char* s = getenv("BSA_ITEMS");
-        v = (s && s[0] == '0' && s[1] == 0) ? 0 : 1;
-    }
-    return v;
-}
-
 // Per-item blocks on the tile path pay off for short rows only (a wave of
 // long rows keeps every SM busy on its own, and the per-item kernel's ring
 // is one slot shorter).  A sliding window bounds a row by construction: with
 // only blocks that hold a visible key listed, a row has at most
-// (window + 254) / 128 window blocks plus the sink blocks.  BSA_ITEMS_TILE=<0|1>
-// forces the choice (tuning, comparisons).
+// (window + 254) / 128 window blocks plus the sink blocks.
 constexpr int32_t kShortRowBlocks = 16;
 bool items_tile_choice(const ForwardArgs& a) {
-    static int v = -2;
-    if (v == -2) {
-        const char* s = getenv("BSA_ITEMS_TILE");
-        v = (s && (s[0] == '0' || s[0] == '1') && s[1] == 0) ? s[0] - '0' : -1;
-    }
-    if (v >= 0) return v == 1;
+    const bsa_schedule sched = forward_options().schedule;
+    if (sched != BSA_SCHEDULE_AUTO) return sched == BSA_SCHEDULE_PER_ITEM;
     if (!a.masked || a.window <= 0) return false;
     const int64_t bound = ((int64_t)a.window + 254) / 128 + ((int64_t)a.sinks + 127) / 128;
     return bound <= kShortRowBlocks;
 }
+
+// The geometry layers (Scatter, Gather 0) run per-item blocks unless one
+// block per row is asked for.
+bool items_geometry() { return forward_options().schedule != BSA_SCHEDULE_PER_ROW; }
 
 template <int D, bool kMask, bool kGeom, bool kQuad, int kQB>
 bsa_status launch_items(const Params& P, int64_t n_items, cudaStream_t stream) {
@@ -1548,16 +1534,6 @@ bsa_status launch_items(const Params& P, int64_t n_items, cudaStream_t stream) {
     const unsigned grid = (unsigned)(n_items < resident ? n_items : resident);
     k_bsa_forward_items<D, kDefaultPoly, kMask, kGeom, kQuad, kQB><<<grid, 192, smem, stream>>>(P, n_items);
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
-}
-
-int poly_setting() {
-    static int v = -1;
-    if (v < 0) {
-        const char* s = getenv("BSA_EXP2_POLY");
-        v = kDefaultPoly;
-        if (s && (s[0] == '0' || s[0] == '2') && s[1] == 0) v = s[0] - '0';
-    }
-    return v;
 }
 
 template <int D, int kPoly, bool kCrm, bool kGather, bool kMask = false, bool kGeom = false, bool kQuad = false>
@@ -1621,7 +1597,7 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
             ok = encode_image_map(&P.map_kg, a.k, kh, a.N, D, g, true, 0, 0) &&
                  encode_image_map(&P.map_vg, a.v, kh, a.N, D, g, true, 0, 0);
         if (!ok) return BSA_ERR_CUDA;
-        if (items_setting()) return launch_items<D, true, true, true, 2>(P, (int64_t)gx * gy, stream);
+        if (items_geometry()) return launch_items<D, true, true, true, 2>(P, (int64_t)gx * gy, stream);
         return launch_dp<D, kDefaultPoly, false, false, true, true, true>(P, gx, gy, stream);
     }
     if (a.scatter_R > 0) {
@@ -1637,7 +1613,7 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
              encode_image_map(&P.map_kg, a.k, kh, a.N, D, g, true, 0, 0) &&
              encode_image_map(&P.map_vg, a.v, kh, a.N, D, g, true, 0, 0);
         if (!ok) return BSA_ERR_CUDA;
-        if (items_setting()) return launch_items<D, false, true, false, 2>(P, (int64_t)gx * gy, stream);
+        if (items_geometry()) return launch_items<D, false, true, false, 2>(P, (int64_t)gx * gy, stream);
         return launch_dp<D, kDefaultPoly, false, false, false, true, false>(P, gx, gy, stream);
     }
     const bool crm = a.crm != nullptr, gather = a.kv_map != nullptr;
@@ -1657,8 +1633,8 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
         return crm ? launch_dp<D, kDefaultPoly, true, true>(P, gx, gy, stream)
                    : launch_dp<D, kDefaultPoly, false, true>(P, gx, gy, stream);
     if (crm) return launch_dp<D, kDefaultPoly, true, false>(P, gx, gy, stream);
-    return poly_setting() == 2 ? launch_dp<D, 2, false, false>(P, gx, gy, stream)
-                               : launch_dp<D, 0, false, false>(P, gx, gy, stream);
+    return forward_options().exp2_fma == 2 ? launch_dp<D, 2, false, false>(P, gx, gy, stream)
+                                           : launch_dp<D, 0, false, false>(P, gx, gy, stream);
 }
 
 template <int D>
@@ -1674,6 +1650,11 @@ int32_t occupancy() {
 }
 
 }  // namespace
+
+bsa_forward_options& forward_options() {
+    thread_local bsa_forward_options opts{BSA_SCHEDULE_AUTO, 0};
+    return opts;
+}
 
 bsa_status launch_forward(const ForwardArgs& a, int32_t* status, cudaStream_t stream) {
     if (a.D == 128) return launch_d<128>(a, status, stream);

@@ -99,6 +99,8 @@ struct ForwardArgs {
 };
 // Returns BSA_OK, BSA_ERR_CUDA (launch / descriptor failure) or BSA_ERR_UNSUPPORTED.
 bsa_status launch_forward(const ForwardArgs& a, int32_t* status, cudaStream_t stream);
+// The calling host thread's forward options (bsa_set_forward_options).
+bsa_forward_options& forward_options();
 int32_t forward_resident_ctas(int32_t D);
 
 }  // namespace bsa

@@ -251,3 +251,22 @@ def test_plain_c_client_builds_links_and_runs(lib, tmp_path):
     assert (N, N_kv) == (512 + 128 * 128, 512 + 5 * 128 * 128) and max_kv > 0
     assert out[3] == "2"  # BSA_ERR_UNSUPPORTED
     assert out[4] == "0"
+
+
+def test_forward_options_are_checked(lib):
+    O = bsa.binding.ForwardOptions
+    assert lib.bsa_set_forward_options(ctypes.byref(O(3, 0))) == 1   # no such schedule
+    assert lib.bsa_set_forward_options(ctypes.byref(O(0, 1))) == 1   # exp2_fma must be 0 or 2
+    assert lib.bsa_set_forward_options(ctypes.byref(O(2, 2))) == 0
+    assert lib.bsa_set_forward_options(None) == 0                   # back to the defaults
+    with pytest.raises(bsa.BsaError):
+        bsa.set_forward_options(exp2_fma=3)
+    bsa.set_forward_options()
+
+
+def test_non_finite_scale_is_rejected(lib):
+    for bad in (float("inf"), float("-inf"), float("nan")):
+        assert _fwd(lib, scale=bad) == 1
+        args = [FAKE, FAKE, 1, 1, 256, 64, None, None, ctypes.c_float(bad), 0, FAKE, ctypes.c_size_t(1 << 20),
+                FAKE, None]
+        assert lib.bsa_block_scores(*args) == 1

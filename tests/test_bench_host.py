@@ -56,21 +56,26 @@ def test_reference_arm_image_layer_line():
 
 
 def test_recorded_traffic_follows_the_kernel_source(monkeypatch):
-    """ncu counters are reported only for the kernel they were taken on and
-    only on the workload they were taken on."""
+    """ncu counters are reported only for the kernel they were taken on, only
+    on the workload they were taken on and only in the row order used there."""
     import argparse
-    args = argparse.Namespace(config=2, heads=None, dense=False, crm=False, scores_on_gpu=False,
-                              order="reordered", kv_gather="auto")
     with open(os.path.join(ROOT, "profiles", "forward_traffic.json")) as f:
-        rec = json.load(f)["config2"]
+        recs = json.load(f)
+    key = sorted(recs)[0]
+    rec = recs[key]
+    args = argparse.Namespace(config=int(key[len("config"):]), heads=None, dense=False, crm=False,
+                              scores="auto", order="auto", kv_gather="auto")
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: rec["kernel_hash"])
-    assert bench.recorded_traffic(args) == rec["dram_bytes_per_launch"]
+    assert bench.recorded_traffic(args, rec["order"]) == rec["dram_bytes_per_launch"]
     assert rec["dram_bytes_per_launch"] == rec["dram_bytes_read"] + rec["dram_bytes_write"]
+    other = "reordered" if rec["order"] == "identity" else "identity"
+    assert bench.recorded_traffic(args, other) is None
+    unrecorded = next(c for c in range(1, 10) if f"config{c}" not in recs)
     for change in (dict(heads=2), dict(dense=True), dict(order="identity"), dict(kv_gather="kernel"),
-                   dict(config=5)):
-        assert bench.recorded_traffic(argparse.Namespace(**{**vars(args), **change})) is None
+                   dict(scores="given"), dict(config=unrecorded)):
+        assert bench.recorded_traffic(argparse.Namespace(**{**vars(args), **change}), rec["order"]) is None
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
-    assert bench.recorded_traffic(args) is None
+    assert bench.recorded_traffic(args, rec["order"]) is None
 
 
 def test_kernel_hash_ignores_comments_only(tmp_path, monkeypatch):
