@@ -270,8 +270,14 @@ size_t bsa_spectral_order_workspace_size(int64_t heads, int32_t nQB, int32_t nKB
  *  - Sizes whose workspace (bsa_spectral_order_workspace_size) exceeds
  *    BSA_SPECTRAL_NOALLOC_SCRATCH_BYTES are rejected with
  *    BSA_ERR_UNSUPPORTED before anything is launched.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - The first call on each device sets that device up: it looks up the
+ *    array's device address (cudaGetSymbolAddress) and the status word, and
+ *    loads the spectral-order kernels.  With CUDA's lazy module loading (the
+ *    default) that set-up is when the array and the kernels take their
+ *    device memory.  Make one call per device, before any stream capture and
+ *    before the phase in which nothing may allocate; a call with heads = 0
+ *    (every pointer may then be NULL) does the set-up and nothing else.
+ *  - Arguments are checked as bsa_spectral_order checks them, first.
  *  - All calls share the array.  Calls whose work overlaps on the GPU (other
  *    streams, other host threads) race on it: serialise them.  Each call
  *    clears what must start at zero, so leftovers of an earlier call do not

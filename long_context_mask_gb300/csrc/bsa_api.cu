@@ -184,6 +184,14 @@ static bool spectral_sizes_ok(int64_t heads, int32_t nQB, int32_t nKB) {
     return heads >= 0 && heads <= 65535 && nQB >= 2 && nQB <= 8192 && nKB >= 1 && nKB <= 65536;
 }
 
+extern "C++" {
+namespace bsa {
+bool spectral_args_ok(int64_t heads, int32_t nQB, int32_t nKB, int32_t max_kv, int32_t iters) {
+    return spectral_sizes_ok(heads, nQB, nKB) && max_kv >= 1 && max_kv <= nKB && iters >= 0 && iters <= 1000;
+}
+}  // namespace bsa
+}
+
 size_t bsa_spectral_order_workspace_size(int64_t heads, int32_t nQB, int32_t nKB) {
     if (!spectral_sizes_ok(heads, nQB, nKB)) return 0;
     return bsa::spectral_order_workspace_bytes(heads, nQB, nKB);
@@ -193,9 +201,7 @@ bsa_status bsa_spectral_order(const int32_t* kv_idx, const int32_t* kv_cnt, int3
                               int64_t heads, int32_t nQB, int32_t nKB, int32_t iters,
                               const float* x0, void* workspace, size_t workspace_bytes,
                               float* x_out, float* angle, int32_t* order, void* stream) {
-    if (!spectral_sizes_ok(heads, nQB, nKB) || max_kv < 1 || max_kv > nKB || iters < 0 ||
-        iters > 1000)
-        return BSA_ERR_INVALID_ARG;
+    if (!bsa::spectral_args_ok(heads, nQB, nKB, max_kv, iters)) return BSA_ERR_INVALID_ARG;
     if (heads == 0) return BSA_OK;
     if (!kv_idx || !kv_cnt || !x0 || !order || !workspace) return BSA_ERR_INVALID_ARG;
     if (workspace_bytes < bsa::spectral_order_workspace_bytes(heads, nQB, nKB))

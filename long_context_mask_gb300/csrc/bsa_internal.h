@@ -66,6 +66,10 @@ cudaError_t launch_block_scores(const void* q, const void* k, int32_t B, int32_t
 
 // bsa_order.cu
 size_t spectral_order_workspace_bytes(int64_t heads, int32_t nQB, int32_t nKB);
+// Loads the spectral-order kernels on the current device (no launch).
+cudaError_t load_spectral_kernels();
+// Sizes and counts every spectral-order entry point accepts (bsa_api.cu).
+bool spectral_args_ok(int64_t heads, int32_t nQB, int32_t nKB, int32_t max_kv, int32_t iters);
 cudaError_t launch_spectral_order(const int32_t* kv_idx, const int32_t* kv_cnt, int32_t max_kv,
                                   int64_t heads, int32_t nQB, int32_t nKB, int32_t iters,
                                   const float* x0, float* workspace, float* x_out, float* angle,

@@ -34,7 +34,10 @@ std::mutex g_scratch_mu;
 
 // Device address of the scratch array on the current device.  In host code
 // `g_noalloc_scratch` is only a stand-in symbol; the real address is looked
-// up once per device (a runtime query that allocates nothing).
+// up once per device.  The same first call on a device looks up the status
+// word and loads the spectral-order kernels: with lazy module loading (the
+// default) those steps load modules, which is when the array and the kernels
+// take their device memory.  Later calls allocate nothing.
 float* scratch_on_current_device() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -43,6 +46,7 @@ float* scratch_on_current_device() {
         float* p = nullptr;
         if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_noalloc_scratch) != cudaSuccess)
             return nullptr;
+        if (bsa::status_word_ptr() == nullptr || bsa::load_spectral_kernels() != cudaSuccess) return nullptr;
         g_scratch_ptr[dev] = p;
     }
     return g_scratch_ptr[dev];
@@ -57,17 +61,23 @@ extern "C" bsa_status bsa_spectral_order_noalloc(const int32_t* kv_idx, const in
                                                  int32_t nKB, int32_t iters, const float* x0,
                                                  float* x_out, float* angle, int32_t* order,
                                                  void* stream) {
-    const size_t need = bsa_spectral_order_workspace_size(heads, nQB, nKB);
-    if (need == 0 && heads != 0) return BSA_ERR_INVALID_ARG;  // sizes the ordinary call rejects
-    if (need > BSA_SPECTRAL_NOALLOC_SCRATCH_BYTES) return BSA_ERR_UNSUPPORTED;  // does not fit
-    if (max_kv < 1 || max_kv > nKB || iters < 0 || iters > 1000) return BSA_ERR_INVALID_ARG;
-    if (heads == 0) return BSA_OK;
-    if (!kv_idx || !kv_cnt || !x0 || !order) return BSA_ERR_INVALID_ARG;
-    if (!aligned(kv_idx, 4) || !aligned(kv_cnt, 4) || !aligned(x0, 8) || !aligned(order, 4) ||
-        (x_out && !aligned(x_out, 8)) || (angle && !aligned(angle, 4)))
-        return BSA_ERR_INVALID_ARG;
+    // the same argument checks as bsa_spectral_order, first
+    if (!bsa::spectral_args_ok(heads, nQB, nKB, max_kv, iters)) return BSA_ERR_INVALID_ARG;
+    if (bsa_spectral_order_workspace_size(heads, nQB, nKB) > BSA_SPECTRAL_NOALLOC_SCRATCH_BYTES)
+        return BSA_ERR_UNSUPPORTED;  // does not fit the fixed scratch
+    if (heads > 0) {
+        if (!kv_idx || !kv_cnt || !x0 || !order) return BSA_ERR_INVALID_ARG;
+        if (!aligned(kv_idx, 4) || !aligned(kv_cnt, 4) || !aligned(x0, 8) || !aligned(order, 4) ||
+            (x_out && !aligned(x_out, 8)) || (angle && !aligned(angle, 4)))
+            return BSA_ERR_INVALID_ARG;
+    }
+    // The per-device set-up (see scratch_on_current_device) runs on every
+    // device's first call, before the zero-size early return, so that a
+    // heads = 0 call can serve as the warm-up after which no call on that
+    // device allocates.
     float* scratch = scratch_on_current_device();
     if (!scratch) return BSA_ERR_CUDA;
+    if (heads == 0) return BSA_OK;
     int32_t* status = bsa::status_word_ptr();
     if (!status) return BSA_ERR_CUDA;
     const cudaError_t e =

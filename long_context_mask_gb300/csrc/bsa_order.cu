@@ -347,6 +347,19 @@ __global__ void __launch_bounds__(kSortThreads) k_spec_sort(int32_t nQB, int32_t
 
 }  // namespace
 
+cudaError_t load_spectral_kernels() {
+    // querying a kernel's attributes loads its module when modules load lazily
+    cudaFuncAttributes fa;
+    const void* fns[] = {(const void*)k_spec_zero,   (const void*)k_spec_init,   (const void*)k_spec_scatter,
+                         (const void*)k_spec_scatter_smem, (const void*)k_spec_center,
+                         (const void*)k_spec_gather, (const void*)k_spec_sort};
+    for (const void* f : fns) {
+        const cudaError_t e = cudaFuncGetAttributes(&fa, f);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 size_t spectral_order_workspace_bytes(int64_t heads, int32_t nQB, int32_t nKB) {
     return (size_t)heads * ws_floats_per_head(nQB, nKB) * sizeof(float);
 }

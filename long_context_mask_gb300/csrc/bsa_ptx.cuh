@@ -89,16 +89,6 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map
         "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
         : "memory");
 }
-// Four rows y0..y3 of width box-x starting at column x (tensor map box is one row high).
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int32_t x,
-                                            int32_t y0, int32_t y1, int32_t y2, int32_t y3,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
-        : "memory");
-}
 // ---------------------------------------------------------------- cp.async
 // 16-byte global -> shared copy through L2 (bypassing L1).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {

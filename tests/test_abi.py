@@ -270,3 +270,12 @@ def test_non_finite_scale_is_rejected(lib):
         args = [FAKE, FAKE, 1, 1, 256, 64, None, None, ctypes.c_float(bad), 0, FAKE, ctypes.c_size_t(1 << 20),
                 FAKE, None]
         assert lib.bsa_block_scores(*args) == 1
+
+
+def test_spectral_entry_points_share_their_argument_checks(lib):
+    """With heads = 0 and nQB = 1 (below the minimum of 2) both the ordinary
+    and the allocation-free spectral order refuse, on the host."""
+    assert lib.bsa_spectral_order(None, None, 1, 0, 1, 5, 10, None, None, ctypes.c_size_t(0), None, None,
+                                  None, None) == 1
+    assert lib.bsa_spectral_order_noalloc(None, None, 1, 0, 1, 5, 10, None, None, None, None, None) == 1
+    assert lib.bsa_spectral_order_noalloc(None, None, 6, 0, 4, 5, 10, None, None, None, None, None) == 1  # max_kv > nKB

@@ -73,6 +73,38 @@ def test_noalloc_matches_ordinary_entry_point_twice_in_a_row(lib):
             assert np.all(np.diff(ra[h][o[h]]) >= -2e-3)
 
 
+def test_noalloc_allocates_nothing_after_the_first_call(lib):
+    """After one zero-size call (the per-device set-up), two full calls leave
+    the device's free memory and torch's allocator untouched."""
+    idx, cnt, x0, nqb = _problem(37)
+    heads = 2
+    order = torch.empty((heads, nqb), dtype=torch.int32, device=DEV)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert lib.bsa_spectral_order_noalloc(None, None, 1, 0, nqb, nqb, 10, None, None, None, None,
+                                          stream) == 0
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    stats0 = torch.cuda.memory_stats()
+    for _ in range(2):
+        assert lib.bsa_spectral_order_noalloc(_ptr(idx), _ptr(cnt), idx.shape[1], heads, nqb, nqb, 10,
+                                              _ptr(x0), None, None, _ptr(order), stream) == 0
+    torch.cuda.synchronize()
+    assert bsa.device_status() == 0
+    free1, _ = torch.cuda.mem_get_info()
+    stats1 = torch.cuda.memory_stats()
+    assert free1 == free0
+    for key in ("allocation.all.allocated", "reserved_bytes.all.current", "allocated_bytes.all.current"):
+        assert stats1.get(key) == stats0.get(key), key
+
+
+def test_noalloc_checks_arguments_like_the_ordinary_call(lib):
+    """Sizes the ordinary entry point rejects are rejected here too, even with
+    heads = 0 (nQB = 1 is below the minimum of 2)."""
+    assert lib.bsa_spectral_order_noalloc(None, None, 1, 0, 1, 5, 10, None, None, None, None, None) == 1
+    assert lib.bsa_spectral_order(None, None, 1, 0, 1, 5, 10, None, None, ctypes.c_size_t(0), None, None,
+                                  None, None) == 1
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
     heads, nqb, nkb = 4096, 4096, 4096  # needs far more than the fixed scratch
     assert bsa.spectral_order_workspace_size(heads, nqb, nkb) > bsa.NOALLOC_SCRATCH_BYTES
