@@ -26,9 +26,11 @@ structure the pages describe):
                  (InstaGen section 3.2.1).
 * ``dynamic``    long-video shape: H24 N118784 D128; Q/K carry per-cluster /
                  per-block offsets so that query blocks fall into 8 shuffled
-                 low-rank access clusters; block scores are the planted
-                 cluster-block affinity plus seeded noise (drawn, not pooled
-                 from the tokens); per-row k ~ U{ceil(0.10 nB) .. floor(0.20 nB)}.
+                 low-rank access clusters; per-row k ~ U{ceil(0.10 nB) ..
+                 floor(0.20 nB)}.  The benchmark scores blocks from these
+                 tokens (mean-pooled QK^T, in the library); ``scores`` holds a
+                 planted alternative, the cluster-block affinity plus seeded
+                 noise (drawn, not pooled), for the index-build tests.
 * ``long_video`` the same at N401408 (401 latent frames), H2: one head's K/V
                  exceeds the L2 (WaveAlign's longest Wan2.1 workload).
 * ``llm``, ``llm_window``  LLaMA-3.1-8B prefill shapes (32 query heads over 8
@@ -279,8 +281,8 @@ CONFIG_NAMES = {
     2: "threshold-map mask B1 H12 N32768 D128, T~U(0,1) + frame band, p=0.15",
     3: "Scatter/Gather maps B1 H24 N16384 D128, T=R=128, one block per query block",
     4: "permuted exact top-16 + 8 PPS-sampled blocks B1 H40 N75776 D128",
-    5: "dynamic top-k (10-20%) of cluster-structured block scores, 8 shuffled clusters, B1 H24 N118784 D128",
-    6: "dynamic top-k (10-20%), 8 shuffled clusters, long video B1 H2 N401408 D128",
+    5: "dynamic top-k (10-20%) of mean-pooled QK^T block scores, 8 shuffled access clusters, B1 H24 N118784 D128",
+    6: "dynamic top-k (10-20%) of mean-pooled QK^T, 8 shuffled access clusters, long video B1 H2 N401408 D128",
     7: "causal block-level layer (every second 256-token block) B1 H32 H_kv8 N16384 D128",
     8: "causal sliding window 575 + 64 sinks B1 H32 H_kv8 N16384 D128",
     9: "INTRA Gather 0 image layer: 512 text + 128x128 image, 16x16 windows, B1 H24 N16896 D128",
