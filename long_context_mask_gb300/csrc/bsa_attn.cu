@@ -99,10 +99,17 @@ constexpr float kRescaleThreshold = 8.0f;  // blocks that compute their maximum 
 constexpr float kSumBound = 18446744073709551616.0f;  // 2^64
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
-constexpr int kExtraProducerWarp = 6;  // warps 6, 7 also copy gathered K/V rows
-constexpr int kGatherWarps = 3;        // warp 0 and warps 6, 7
-// 6 warps; 8 (two per SM sub-partition) when K/V rows are gathered
-constexpr int threads_for(bool gather) { return gather ? 256 : 192; }
+constexpr int kFirstSoftmaxWarp = 2;
+constexpr int kGatherWarps = 3;  // warp 0 and the two extra producer warps
+// Softmax warps: with a token mask (kMask) one per TMEM lane quadrant, each
+// thread a whole 128-column row; without, two per quadrant, each warp 16
+// rows with four threads per row (the row split, see softmax_block_rows).
+constexpr int softmax_warps(bool mask) { return mask ? 4 : 8; }
+// Extra producer warps (gathered K/V rows) follow the softmax warps.
+constexpr int extra_producer_warp(bool mask) { return kFirstSoftmaxWarp + softmax_warps(mask); }
+constexpr int threads_for(bool gather, bool mask) {
+    return 32 * (extra_producer_warp(mask) + (gather ? kGatherWarps - 1 : 0));
+}
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 384;
 constexpr int kSBuf = 3;  // TMEM score buffers
@@ -243,6 +250,149 @@ __device__ __forceinline__ float exp128(uint32_t (&s)[128], float sl2, float bia
     float lo, hi;
     f2unpack(add2(add2(acc0, acc1), add2(acc2, acc3)), lo, hi);
     return lo + hi;
+}
+
+// ---------------------------------------------------------------- row split
+// Two softmax warps per TMEM lane quadrant, each over 16 lanes (query rows):
+// thread t holds rows t/4 and t/4 + 8 of its warp's 16 ("a" and "b") and,
+// of each, the 32 columns 2 (t % 4) + 8 k and 2 (t % 4) + 8 k + 1 (the
+// tcgen05 16x256b layout: s[4k], s[4k+1] row a, s[4k+2], s[4k+3] row b).
+// The four threads of a row are lanes 4 (t/4) .. 4 (t/4) + 3 of the warp.
+
+// Row maxima of rows a and b over all 128 columns (shuffles within the row's
+// four threads).
+__device__ __forceinline__ void max_rows(const uint32_t (&s)[64], float& ma, float& mb) {
+    float a0 = -INFINITY, a1 = -INFINITY, b0 = -INFINITY, b1 = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 16; k += 2) {
+        a0 = fmax3(a0, __uint_as_float(s[4 * k + 0]), __uint_as_float(s[4 * k + 1]));
+        b0 = fmax3(b0, __uint_as_float(s[4 * k + 2]), __uint_as_float(s[4 * k + 3]));
+        a1 = fmax3(a1, __uint_as_float(s[4 * k + 4]), __uint_as_float(s[4 * k + 5]));
+        b1 = fmax3(b1, __uint_as_float(s[4 * k + 6]), __uint_as_float(s[4 * k + 7]));
+    }
+    ma = fmaxf(a0, a1);
+    mb = fmaxf(b0, b1);
+    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+}
+
+// P = 2^(s * sl2 + bias) for this thread's 64 scores, packed as bf16 pairs
+// in the 16x128b layout (s[2k] row a, s[2k+1] row b, column (t % 4) + 4 k);
+// la, lb receive this thread's share of the two row sums.
+template <int kPoly>
+__device__ __forceinline__ void exp_rows(uint32_t (&s)[64], float sl2, float bias_a, float bias_b, float& la,
+                                         float& lb) {
+    const uint64_t a2 = f2pack(sl2, sl2), ba = f2pack(bias_a, bias_a), bb = f2pack(bias_b, bias_b);
+    uint64_t acc_a0 = f2pack(0.f, 0.f), acc_a1 = acc_a0, acc_b0 = acc_a0, acc_b1 = acc_a0;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        float x[4];
+        f2unpack(fma2(f2pack(__uint_as_float(s[4 * k]), __uint_as_float(s[4 * k + 1])), a2, ba), x[0], x[1]);
+        f2unpack(fma2(f2pack(__uint_as_float(s[4 * k + 2]), __uint_as_float(s[4 * k + 3])), a2, bb), x[2], x[3]);
+        float p[4];
+        // column of x[i]: 2 (t % 4) + 8 k + (i & 1); its residue mod 8 decides the unit
+#pragma unroll
+        for (int i = 0; i < 4; ++i) p[i] = kPoly > 0 && (((threadIdx.x & 3) * 2 + (i & 1)) < kPoly) ? exp2_fma(x[i]) : ex2(x[i]);
+        if (k & 1) {
+            acc_a1 = add2(acc_a1, f2pack(p[0], p[1]));
+            acc_b1 = add2(acc_b1, f2pack(p[2], p[3]));
+        } else {
+            acc_a0 = add2(acc_a0, f2pack(p[0], p[1]));
+            acc_b0 = add2(acc_b0, f2pack(p[2], p[3]));
+        }
+        s[2 * k] = pack_bf16(p[0], p[1]);
+        s[2 * k + 1] = pack_bf16(p[2], p[3]);
+    }
+    float x0, x1;
+    f2unpack(add2(acc_a0, acc_a1), x0, x1);
+    la = x0 + x1;
+    f2unpack(add2(acc_b0, acc_b1), x0, x1);
+    lb = x0 + x1;
+}
+
+// One block of the online softmax for rows a and b (no token mask, so the
+// running maxima are finite after the first block): as softmax_block, the
+// block maximum only for the first block or when some row's exponentials
+// outgrow 2^64 (summed over this thread's 32 columns; a row's sum is then
+// below 2^66).  Returns true (warp-uniform) when O must be rescaled.
+template <int kPoly, typename Reload>
+__device__ __forceinline__ bool softmax_block_rows(uint32_t (&s)[64], int32_t j, float sl2, float lw2, float (&m)[2],
+                                                   float (&l)[2], float (&alpha)[2], Reload&& reload) {
+    alpha[0] = alpha[1] = 1.0f;
+    float la, lb;
+    if (j > 0) {
+        exp_rows<kPoly>(s, sl2, lw2 - m[0], lw2 - m[1], la, lb);
+        if (!__any_sync(0xffffffffu, !(la <= kSumBound) || !(lb <= kSumBound))) {
+            l[0] += la;
+            l[1] += lb;
+            return false;
+        }
+        reload();
+    }
+    float ma, mb;
+    max_rows(s, ma, mb);
+    const float mt[2] = {ma * sl2 + lw2, mb * sl2 + lw2};
+    bool rescale = false;
+    if (j == 0) {
+        m[0] = mt[0];
+        m[1] = mt[1];
+    } else {
+        rescale = __any_sync(0xffffffffu, mt[0] > m[0] + kRescaleThreshold || mt[1] > m[1] + kRescaleThreshold);
+        if (rescale) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float m_new = fmaxf(m[i], mt[i]);
+                alpha[i] = ex2(m[i] - m_new);
+                l[i] *= alpha[i];
+                m[i] = m_new;
+            }
+        }
+    }
+    exp_rows<kPoly>(s, sl2, lw2 - m[0], lw2 - m[1], la, lb);
+    l[0] += la;
+    l[1] += lb;
+    return rescale;
+}
+
+// A row's sum over its four threads (the same value in each).
+__device__ __forceinline__ float row_sum4(float x) {
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    return x + __shfl_xor_sync(0xffffffffu, x, 2);
+}
+
+// O columns of rows a and b out of tensor memory (16x256b layout, D / 4 per
+// row per thread), multiplied by per-row factors, back in.
+template <int D>
+__device__ __forceinline__ void scale_o_rows(uint32_t taddr, float fa, float fb) {
+    uint32_t o[D / 2];
+    if constexpr (D == 128) tmem_ld16x256_x16(taddr, o);
+    else tmem_ld16x256_x8(taddr, o);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < D / 2; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * (((i >> 1) & 1) ? fb : fa));
+    if constexpr (D == 128) tmem_st16x256_x16(taddr, o);
+    else tmem_st16x256_x8(taddr, o);
+}
+
+// Normalised O of rows a and b (bf16) to their output rows: this thread's
+// column pairs 2 (t % 4) + 8 k.
+template <int D>
+__device__ __forceinline__ void store_o_rows(uint32_t taddr, float inv_a, float inv_b, __nv_bfloat16* row_a,
+                                             __nv_bfloat16* row_b) {
+    uint32_t o[D / 2];
+    if constexpr (D == 128) tmem_ld16x256_x16(taddr, o);
+    else tmem_ld16x256_x8(taddr, o);
+    tmem_wait_ld();
+    const int c = 2 * (threadIdx.x & 3);
+#pragma unroll
+    for (int k = 0; k < D / 8; ++k) {
+        const uint32_t pa = pack_bf16(__uint_as_float(o[4 * k]) * inv_a, __uint_as_float(o[4 * k + 1]) * inv_a);
+        const uint32_t pb = pack_bf16(__uint_as_float(o[4 * k + 2]) * inv_b, __uint_as_float(o[4 * k + 3]) * inv_b);
+        if (row_a) *reinterpret_cast<uint32_t*>(row_a + 8 * k + c) = pa;
+        if (row_b) *reinterpret_cast<uint32_t*>(row_b + 8 * k + c) = pb;
+    }
 }
 
 // One block of the online softmax for this thread's row.  On entry s holds
@@ -412,7 +562,7 @@ __device__ __forceinline__ void geo_load_kv(const Params& P, uint32_t dst, uint3
 }
 
 template <int D, int kPoly, bool kCrm, bool kGather, bool kMask, bool kGeom, bool kQuad>
-__global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(threads_for(kGather, kMask), 1) k_bsa_forward(const __grid_constant__ Params P) {
     static_assert(!(kCrm && kMask), "the token mask reads block indices from the lists");
     static_assert(!kGeom || (!kGather && !kCrm), "the geometry mode loads tiles by TMA boxes");
     static_assert(!kQuad || kMask, "quadrant masks live in the masked variant");
@@ -475,7 +625,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
         }
         // Q by one TMA tile copy, or gathered by the 128 softmax threads
         mbar_init(smem_u32(&bars->q_full), P.q_map ? 128 : 1);
-        for (int s = 0; s < kSBuf; ++s) mbar_init(smem_u32(&bars->p_full[s]), 128);
+        for (int s = 0; s < kSBuf; ++s) mbar_init(smem_u32(&bars->p_full[s]), 32 * softmax_warps(kMask));
         mbar_init(smem_u32(&bars->mma_done), 1);
         bars->abort = 0;
         fence_mbar_init();
@@ -503,6 +653,7 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
+    constexpr int kExtraProducerWarp = extra_producer_warp(kMask);
     if (warp == kProducerWarp || warp >= kExtraProducerWarp) {
         // ------------------------------------------------------------ producers
         // Tile loads: warp 0 alone (one TMA copy per tile).  Gathered K/V
@@ -715,6 +866,112 @@ __global__ void __launch_bounds__(threads_for(kGather), 1) k_bsa_forward(const _
         if (!mbar_wait(smem_u32(&bars->mma_done), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT) && lane == 0)
             raise_status(P.status, BSA_ERR_TIMEOUT);
         __syncwarp();
+    } else if constexpr (!kMask) {
+        // ------------------------------------------------ softmax + epilogue (row split)
+        // Warp `half` of quadrant qd owns rows 32 qd + 16 half .. + 15; thread
+        // t rows ra = .. + t/4 and rb = ra + 8 (see softmax_block_rows).
+        const int qd = warp & 3;  // a warp reaches TMEM lanes 32 (warp % 4) .. + 31
+        const int half = (warp - kFirstSoftmaxWarp) >> 2;
+        const int ra = qd * 32 + half * 16 + (lane >> 2), rb = ra + 8;
+        const uint32_t t_base = tmem + ((uint32_t)(qd * 32 + half * 16) << 16);
+        int32_t tok[2] = {qb * 128 + ra, qb * 128 + rb};
+        bool tok_ok[2] = {true, true};
+        if constexpr (kGeom) {
+            tok[0] = g0::query_token(P.geo, qb * 128 + ra);
+            tok[1] = g0::query_token(P.geo, qb * 128 + rb);
+        }
+        if (P.q_map != nullptr) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                tok[i] = P.q_map[bh * N + qb * 128 + (i ? rb : ra)];
+                if (tok[i] < 0 || tok[i] >= N) {
+                    raise_status(P.status, BSA_ERR_BOUNDS);
+                    tok_ok[i] = false;
+                }
+            }
+            // the half-0 warps copy the quadrant's 32 query rows into the Q
+            // tile, lane l row 32 qd + l (row 0 stands in for an invalid token;
+            // that row's output is not written)
+            if (half == 0) {
+                int32_t tq = P.q_map[bh * N + qb * 128 + qd * 32 + lane];
+                if (tq < 0 || tq >= N) tq = 0;
+                copy_rows32<D>(s_q, P.q, bh, N, qd, lane, tq);
+                cp_async_arrive_noinc(smem_u32(&bars->q_full));
+            }
+        }
+        const float sl2 = P.scale_log2;
+        const float* lw_row = P.log_w ? P.log_w + row * max_kv : nullptr;
+        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};  // l: this thread's share of each row
+        bool ok = true;
+        float lw_next = (lw_row && n > 0) ? lw_row[0] : 0.0f;
+        for (int32_t j = 0; j < n; ++j) {
+            const float lw2 = lw_next * kLog2e;
+            lw_next = (lw_row && j + 1 < n) ? lw_row[j + 1] : 0.0f;
+            const uint32_t sbuf = (uint32_t)(j % kSBuf) * 128u;
+            const int32_t pk = ring_pos_k(j);
+            const bool w = mbar_wait(smem_u32(&bars->empty[pk % C::kStages]), (uint32_t)(pk / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+            if (__any_sync(0xffffffffu, !w || aborted(bars))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t s[64];
+            auto load_s = [&]() {
+                tmem_ld16x256_x16(t_base + sbuf, s);
+                tmem_wait_ld();
+            };
+            load_s();
+            float alpha[2];
+            const bool rescale = softmax_block_rows<kPoly>(s, j, sl2, lw2, m, l, alpha, load_s);
+            tmem_st16x128_x16(t_base + sbuf, s);  // P_j over the first 64 columns of S_j
+            if (rescale) {
+                // O must hold P_0..P_{j-1} V: wait for PV_{j-1}
+                const int32_t pv = ring_pos_v(j - 1, n);
+                const bool wv = mbar_wait(smem_u32(&bars->empty[pv % C::kStages]), (uint32_t)(pv / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                if (__any_sync(0xffffffffu, !wv)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                scale_o_rows<D>(t_base + kColO, alpha[0], alpha[1]);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars->p_full[j % kSBuf]));
+        }
+        if (!ok) {
+            if (lane == 0) set_abort(bars, P.status);
+        } else {
+            const float l_a = row_sum4(l[0]), l_b = row_sum4(l[1]);
+            __nv_bfloat16* row_a = tok_ok[0] ? P.o + (bh * N + tok[0]) * D : nullptr;
+            __nv_bfloat16* row_b = tok_ok[1] ? P.o + (bh * N + tok[1]) * D : nullptr;
+            const int c = 2 * (lane & 3);
+            if (n == 0) {
+#pragma unroll
+                for (int k = 0; k < D / 8; ++k) {
+                    if (row_a) *reinterpret_cast<uint32_t*>(row_a + 8 * k + c) = 0u;
+                    if (row_b) *reinterpret_cast<uint32_t*>(row_b + 8 * k + c) = 0u;
+                }
+                if ((lane & 3) == 0) {
+                    if (row_a) P.lse[bh * N + tok[0]] = -INFINITY;
+                    if (row_b) P.lse[bh * N + tok[1]] = -INFINITY;
+                }
+            } else {
+                const int32_t pv = ring_pos_v(n - 1, n);
+                const bool w = mbar_wait(smem_u32(&bars->empty[pv % C::kStages]), (uint32_t)(pv / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                if (__any_sync(0xffffffffu, !w)) {
+                    if (lane == 0) set_abort(bars, P.status);
+                } else {
+                    tc_fence_after();
+                    store_o_rows<D>(t_base + kColO, l_a > 0.0f ? 1.0f / l_a : 0.0f, l_b > 0.0f ? 1.0f / l_b : 0.0f,
+                                    row_a, row_b);
+                    if ((lane & 3) == 0) {
+                        if (row_a) P.lse[bh * N + tok[0]] = l_a > 0.0f ? (m[0] + log2f(l_a)) * kLn2 : -INFINITY;
+                        if (row_b) P.lse[bh * N + tok[1]] = l_b > 0.0f ? (m[1] + log2f(l_b)) * kLn2 : -INFINITY;
+                    }
+                }
+            }
+        }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
         const int qd = warp & 3;                 // TMEM lane quadrant of this warp
@@ -1015,7 +1272,7 @@ struct ItemCfg {
 };
 
 template <int D, int kPoly, bool kMask, bool kGeom, bool kQuad, int kQB>
-__global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_constant__ Params P, int64_t n_items) {
+__global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_items(const __grid_constant__ Params P, int64_t n_items) {
     static_assert(!kQuad || kMask, "quadrant masks live in the masked variant");
     static_assert(kQB == 1 || kQB == 2, "one or two Q buffers");
     using C = Cfg<D>;
@@ -1046,8 +1303,8 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
             mbar_init(smem_u32(&bars->q_full[b]), 1);
             mbar_init(smem_u32(&bars->q_empty[b]), 1);
         }
-        for (int s = 0; s < kSBuf; ++s) mbar_init(smem_u32(&bars->p_full[s]), 128);
-        mbar_init(smem_u32(&bars->o_free), 128);
+        for (int s = 0; s < kSBuf; ++s) mbar_init(smem_u32(&bars->p_full[s]), 32 * softmax_warps(kMask));
+        mbar_init(smem_u32(&bars->o_free), 32 * softmax_warps(kMask));
         mbar_init(smem_u32(&bars->mma_done), 1);
         bars->abort = 0;
         fence_mbar_init();
@@ -1253,6 +1510,113 @@ __global__ void __launch_bounds__(192, 1) k_bsa_forward_items(const __grid_const
         if (!mbar_wait(smem_u32(&bars->mma_done), 0, kWaitNs, P.status, BSA_ERR_TIMEOUT) && lane == 0)
             raise_status(P.status, BSA_ERR_TIMEOUT);
         __syncwarp();
+    } else if constexpr (!kMask) {
+        // ------------------------------------------------ softmax + epilogue (row split)
+        const int qd = warp & 3;
+        const int half = (warp - kFirstSoftmaxWarp) >> 2;
+        const int ra = qd * 32 + half * 16 + (lane >> 2), rb = ra + 8;
+        const uint32_t t_base = tmem + ((uint32_t)(qd * 32 + half * 16) << 16);
+        const float sl2 = P.scale_log2;
+        uint32_t t_glob = 0, g_glob = 0;
+        bool ok = true;
+        for (int64_t w = 0; ok; ++w) {
+            const int64_t f = item_of(w);
+            if (f >= n_items) break;
+            Item it;
+            if (!decode_item(P, f, it)) continue;
+            const int32_t n = it.n;
+            const int32_t tok_a = kGeom ? g0::query_token(P.geo, it.qb * 128 + ra) : it.qb * 128 + ra;
+            const int32_t tok_b = kGeom ? g0::query_token(P.geo, it.qb * 128 + rb) : it.qb * 128 + rb;
+            __nv_bfloat16* row_a = P.o + (it.bh * N + tok_a) * D;
+            __nv_bfloat16* row_b = P.o + (it.bh * N + tok_b) * D;
+            const int c = 2 * (lane & 3);
+            if (n == 0) {
+#pragma unroll
+                for (int k = 0; k < D / 8; ++k) {
+                    *reinterpret_cast<uint32_t*>(row_a + 8 * k + c) = 0u;
+                    *reinterpret_cast<uint32_t*>(row_b + 8 * k + c) = 0u;
+                }
+                if ((lane & 3) == 0) {
+                    P.lse[it.bh * N + tok_a] = -INFINITY;
+                    P.lse[it.bh * N + tok_b] = -INFINITY;
+                }
+                continue;
+            }
+            const float* lw_row = P.log_w ? P.log_w + it.row * max_kv : nullptr;
+            float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
+            float lw_next = lw_row ? lw_row[0] : 0.0f;
+            for (int32_t j = 0; j < n; ++j) {
+                const float lw2 = lw_next * kLog2e;
+                lw_next = (lw_row && j + 1 < n) ? lw_row[j + 1] : 0.0f;
+                const uint32_t gb = g_glob + (uint32_t)j;
+                const uint32_t sbuf = (gb % kSBuf) * 128u;
+                const uint32_t pk = t_glob + (uint32_t)ring_pos_k(j);
+                const bool wt = mbar_wait(smem_u32(&bars->empty[pk % S]), (pk / S) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                if (__any_sync(0xffffffffu, !wt || items_aborted(bars))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t s[64];
+                auto load_s = [&]() {
+                    tmem_ld16x256_x16(t_base + sbuf, s);
+                    tmem_wait_ld();
+                };
+                load_s();
+                float alpha[2];
+                const bool rescale = softmax_block_rows<kPoly>(s, j, sl2, lw2, m, l, alpha, load_s);
+                tmem_st16x128_x16(t_base + sbuf, s);
+                if (rescale) {
+                    // O must hold P_0..P_{j-1} V: wait for PV_{j-1}
+                    const uint32_t pv = t_glob + (uint32_t)ring_pos_v(j - 1, n);
+                    const bool wv = mbar_wait(smem_u32(&bars->empty[pv % S]), (pv / S) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                    if (__any_sync(0xffffffffu, !wv)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    scale_o_rows<D>(t_base + kColO, alpha[0], alpha[1]);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars->p_full[gb % kSBuf]));
+            }
+            if (!ok) break;
+            // Epilogue: once PV_{n-1} has run, read O out of tensor memory, hand
+            // the accumulator to the next item (o_free), then normalise and
+            // store while the next item's products proceed.
+            {
+                const uint32_t pv = t_glob + (uint32_t)ring_pos_v(n - 1, n);
+                const bool wt = mbar_wait(smem_u32(&bars->empty[pv % S]), (pv / S) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
+                if (__any_sync(0xffffffffu, !wt)) {
+                    ok = false;
+                    break;
+                }
+            }
+            tc_fence_after();
+            const float l_a = row_sum4(l[0]), l_b = row_sum4(l[1]);
+            const float inv_a = l_a > 0.0f ? 1.0f / l_a : 0.0f, inv_b = l_b > 0.0f ? 1.0f / l_b : 0.0f;
+            uint32_t o[D / 2];
+            if constexpr (D == 128) tmem_ld16x256_x16(t_base + kColO, o);
+            else tmem_ld16x256_x8(t_base + kColO, o);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars->o_free));
+#pragma unroll
+            for (int k = 0; k < D / 8; ++k) {
+                *reinterpret_cast<uint32_t*>(row_a + 8 * k + c) =
+                    pack_bf16(__uint_as_float(o[4 * k]) * inv_a, __uint_as_float(o[4 * k + 1]) * inv_a);
+                *reinterpret_cast<uint32_t*>(row_b + 8 * k + c) =
+                    pack_bf16(__uint_as_float(o[4 * k + 2]) * inv_b, __uint_as_float(o[4 * k + 3]) * inv_b);
+            }
+            if ((lane & 3) == 0) {
+                P.lse[it.bh * N + tok_a] = l_a > 0.0f ? (m[0] + log2f(l_a)) * kLn2 : -INFINITY;
+                P.lse[it.bh * N + tok_b] = l_b > 0.0f ? (m[1] + log2f(l_b)) * kLn2 : -INFINITY;
+            }
+            t_glob += 2u * (uint32_t)n;
+            g_glob += (uint32_t)n;
+        }
+        if (!ok && lane == 0) items_set_abort(bars, P.status);
     } else {
         // ------------------------------------------------------------ softmax + epilogue
         const int qd = warp & 3;                 // TMEM lane quadrant of this warp
@@ -1532,7 +1896,7 @@ bsa_status launch_items(const Params& P, int64_t n_items, cudaStream_t stream) {
     const int32_t resident = forward_resident_ctas(D);
     if (resident <= 0) return BSA_ERR_CUDA;
     const unsigned grid = (unsigned)(n_items < resident ? n_items : resident);
-    k_bsa_forward_items<D, kDefaultPoly, kMask, kGeom, kQuad, kQB><<<grid, 192, smem, stream>>>(P, n_items);
+    k_bsa_forward_items<D, kDefaultPoly, kMask, kGeom, kQuad, kQB><<<grid, threads_for(false, kMask), smem, stream>>>(P, n_items);
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
@@ -1540,7 +1904,7 @@ template <int D, int kPoly, bool kCrm, bool kGather, bool kMask = false, bool kG
 bsa_status launch_dp(const Params& P, unsigned grid_x, unsigned grid_y, cudaStream_t stream) {
     if (prepare_kernel<D, kPoly, kCrm, kGather, kMask, kGeom, kQuad>() != cudaSuccess) return BSA_ERR_CUDA;
     k_bsa_forward<D, kPoly, kCrm, kGather, kMask, kGeom, kQuad>
-        <<<dim3(grid_x, grid_y), threads_for(kGather), smem_bytes<D>(), stream>>>(P);
+        <<<dim3(grid_x, grid_y), threads_for(kGather, kMask), smem_bytes<D>(), stream>>>(P);
     return cudaGetLastError() == cudaSuccess ? BSA_OK : BSA_ERR_CUDA;
 }
 
@@ -1643,7 +2007,7 @@ int32_t occupancy() {
     // every instantiation holds one block per SM (shared memory bound)
     if (prepare_kernel<D, kDefaultPoly, false, false, false>() != cudaSuccess) return -1;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_bsa_forward<D, kDefaultPoly, false, false, false, false, false>,
-                                                      threads_for(false),
+                                                      threads_for(false, false),
                                                       smem_bytes<D>()) != cudaSuccess)
         return -1;
     return per_sm;

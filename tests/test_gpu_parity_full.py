@@ -221,9 +221,9 @@ def _tile_keys(img_h, img_w, n_text, groups):
 @pytest.mark.parametrize("img_h,img_w,n_text,groups", [(32, 32, 128, 2), (48, 16, 256, 2), (16, 24, 0, 1)])
 def test_gather0_and_packed_without_quadrant_masks(img_h, img_w, n_text, groups):
     """bsa_forward_gather0 with quad_mask = NULL and bsa_forward_packed without a
-    quadrant mask over the layout's map (N_kv > N) give the same result bit for
-    bit, and each query tile attends to every key of its listed tiles (a
-    token two listed tiles hold counts twice)."""
+    quadrant mask over the layout's map (N_kv > N): each query tile attends to
+    every key of its listed tiles (a token two listed tiles hold counts
+    twice)."""
     H = 2
     prob = synth.image_gather0(seed=63 + img_w, B=1, H=H, img_h=img_h, img_w=img_w, n_text=n_text,
                                groups=groups, D=128)
@@ -236,7 +236,16 @@ def test_gather0_and_packed_without_quadrant_masks(img_h, img_w, n_text, groups)
     bsa.forward_packed(q, k, v, idx, cnt, kv_map, o2, l2, quad_mask=None, q_map=q_map)
     torch.cuda.synchronize()
     status_ok()
-    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    # gather0 runs the token-masked kernel even without quadrant masks, the
+    # packed call without any mask the unmasked one: the two sum in different
+    # orders, so they agree to rounding, and each matches the oracle below
+    assert (o1.float() - o2.float()).abs().max().item() <= O_MAX_ABS
+    assert (l1 - l2).abs().max().item() <= LSE_MAX_ABS
+    for o_gpu, l_gpu in ((o1, l1), (o2, l2)):
+        _check_tiles(prob, o_gpu, l_gpu, H, img_h, img_w, n_text, groups)
+
+
+def _check_tiles(prob, o1, l1, H, img_h, img_w, n_text, groups):
     og = o1.float().cpu().numpy().reshape(H, prob.N, prob.D)
     lg = l1.cpu().numpy().reshape(H, prob.N)
     num = den = 0.0
