@@ -267,9 +267,11 @@ class Path:
     def host_inputs(self):
         """Tensors a step takes from the host (end-to-end leg); the static
         patterns of the image and Scatter layers (layout, maps) stay on the
-        device, and their geometry modes do not read maps at all."""
+        device, and their geometry modes do not read maps at all.  Block
+        scores computed inside the step are not inputs."""
         ts = (self.q, self.k, self.v) if (self.image or self.scatter_boxes) else (
-            self.q, self.k, self.v, self.src, self.q_map, self.kv_map, self.k_per_row, self.u)
+            self.q, self.k, self.v, None if self.scores_on_gpu else self.src, self.q_map, self.kv_map,
+            self.k_per_row, self.u)
         return [t for t in ts if t is not None]
 
     def attend(self, row_perm="auto"):
@@ -775,7 +777,18 @@ def main():
     h_l = [torch.empty_like(path.lse, device="cpu").pin_memory() for _ in range(2)]
     bi = sum(t.numel() * t.element_size() for t in h_in)
     bo = h_o[0].numel() * h_o[0].element_size() + h_l[0].numel() * h_l[0].element_size()
-    E = max(4, K // 4)
+    # one untimed round trip through every pinned buffer: the first copy from
+    # freshly pinned pages runs at a fraction of the link rate (52 ms instead
+    # of 11 for the dynamic workload's 2.27 GB), a once-per-buffer cost that a
+    # serving process pays when it sets up, not per step
+    for d_in in d_ins:
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+    for b in range(2):
+        h_o[b].copy_(paths[b].o, non_blocking=True)
+        h_l[b].copy_(paths[b].lse, non_blocking=True)
+    torch.cuda.synchronize()
+    E = max(4, K)
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ev = lambda: torch.cuda.Event()  # noqa: E731
     in_done, comp_done, out_done = [ev() for _ in range(E)], [ev() for _ in range(E)], [ev() for _ in range(E)]

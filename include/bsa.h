@@ -98,7 +98,8 @@ bsa_status bsa_build_index(bsa_idx_mode mode, const void* src, int64_t rows, int
  * query group and a key cluster).  A group / cluster is a 128-token block of
  * the gathered order (q_map / kv_map, identity when NULL).
  *
- *  q, k      device bf16 [B, H, N, D]; N a multiple of 128, D 8 .. 256 (x8).
+ *  q, k      device bf16 [B, H, N, D], 16-byte aligned; N a multiple of 128,
+ *            D 8 .. 256 (x8).
  *  q_map, kv_map  device int32 [B*H, N] or NULL (as in bsa_forward).
  *  scale     <= 0 selects 1/sqrt(D); a NaN or infinite scale is rejected
  *            (BSA_ERR_INVALID_ARG).

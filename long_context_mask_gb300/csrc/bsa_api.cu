@@ -169,7 +169,7 @@ bsa_status bsa_block_scores(const void* q, const void* k, int32_t B, int32_t H, 
     if (!q || !k || !scores || !workspace) return BSA_ERR_INVALID_ARG;
     if (workspace_bytes < bsa::block_scores_workspace_bytes((int64_t)B * H, N, D))
         return BSA_ERR_INVALID_ARG;
-    if (!aligned(q, 2) || !aligned(k, 2) || !aligned(scores, 4) || !aligned(workspace, 16) ||
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(scores, 4) || !aligned(workspace, 16) ||
         (q_map && !aligned(q_map, 4)) || (kv_map && !aligned(kv_map, 4)))
         return BSA_ERR_INVALID_ARG;
     int32_t* status = bsa::status_word_ptr();

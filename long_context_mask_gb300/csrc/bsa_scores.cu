@@ -9,8 +9,8 @@
 // 128-token block of the gathered order.
 //
 //   k_block_means   one thread block per (head, block, tensor): the fp32 mean
-//                   of the block's 128 rows (gathered through the map), one
-//                   thread per column; written to the caller's workspace.
+//                   of the block's 128 rows (gathered through the map), read
+//                   with 16-byte loads; written to the caller's workspace.
 //   k_block_scores  per head, a 64 x 64 tile of  mean(Q_u) . mean(K_v) * scale
 //                   (or its exponential) per thread block, from shared-memory
 //                   tiles of the two mean matrices.
@@ -28,28 +28,51 @@ namespace {
 constexpr int kTileS = 64;   // score tile edge
 constexpr int kKChunk = 32;  // columns of the mean matrices staged per step
 
-__global__ void k_block_means(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                              int32_t N, int32_t D, const int32_t* __restrict__ q_map,
-                              const int32_t* __restrict__ kv_map, float* __restrict__ means,
-                              int64_t per_tensor, int32_t* status) {
+// One thread block (128 threads) per (head, block, tensor).  D / 8 threads
+// cover a row with 16-byte loads (8 columns each) and 128 / (D / 8) rows are
+// read per pass, so every thread's loads are independent; the row groups'
+// partial sums meet in shared memory.  D is a multiple of 8, at most 256.
+constexpr int kMeanThreads = 128;
+__global__ void __launch_bounds__(kMeanThreads) k_block_means(
+    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int32_t N, int32_t D,
+    const int32_t* __restrict__ q_map, const int32_t* __restrict__ kv_map, float* __restrict__ means,
+    int64_t per_tensor, int32_t* status) {
+    __shared__ float part[kMeanThreads * 8];  // [row group][column]
     const int32_t b = blockIdx.x;
     const int64_t bh = blockIdx.y;
     const int which = blockIdx.z;  // 0: Q, 1: K
     const __nv_bfloat16* x = which ? k : q;
     const int32_t* map = which ? kv_map : q_map;
     const int32_t nb = N / kBlock;
-    for (int32_t d = threadIdx.x; d < D; d += blockDim.x) {
-        float s = 0.f;
-        for (int32_t t = 0; t < kBlock; ++t) {
+    const int lanes_per_row = D / 8;                   // 16-byte chunks per row
+    const int groups = kMeanThreads / lanes_per_row;   // rows read per pass
+    const int chunk = threadIdx.x % lanes_per_row, grp = threadIdx.x / lanes_per_row;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (grp < groups) {
+        for (int32_t t = grp; t < kBlock; t += groups) {
             const int32_t p = b * kBlock + t;
             int32_t i = map ? map[bh * N + p] : p;
             if (i < 0 || i >= N) {
-                if (d == 0) atomicCAS(status, 0, BSA_ERR_BOUNDS);
+                if (chunk == 0) atomicCAS(status, 0, BSA_ERR_BOUNDS);
                 i = 0;
             }
-            s += __bfloat162float(x[(bh * N + i) * D + d]);
+            const uint4 v = *reinterpret_cast<const uint4*>(x + (bh * N + i) * D + chunk * 8);
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(h[e]);
+                acc[2 * e] += f.x;
+                acc[2 * e + 1] += f.y;
+            }
         }
-        means[which * per_tensor + (bh * nb + b) * D + d] = s * (1.0f / kBlock);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) part[grp * D + chunk * 8 + e] = acc[e];
+    }
+    __syncthreads();
+    for (int32_t d = threadIdx.x; d < D; d += kMeanThreads) {
+        float sum = 0.f;
+        for (int g = 0; g < groups; ++g) sum += part[g * D + d];
+        means[which * per_tensor + (bh * nb + b) * D + d] = sum * (1.0f / kBlock);
     }
 }
 
@@ -113,7 +136,7 @@ cudaError_t launch_block_scores(const void* q, const void* k, int32_t B, int32_t
     const int64_t BH = (int64_t)B * H;
     const int32_t nb = N / kBlock;
     const int64_t per_tensor = BH * nb * (int64_t)D;
-    k_block_means<<<dim3((unsigned)nb, (unsigned)BH, 2), 128, 0, stream>>>(
+    k_block_means<<<dim3((unsigned)nb, (unsigned)BH, 2), kMeanThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), N, D, q_map,
         kv_map, workspace, per_tensor, status);
     const unsigned tiles = (unsigned)((nb + kTileS - 1) / kTileS);

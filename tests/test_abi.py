@@ -279,3 +279,11 @@ def test_spectral_entry_points_share_their_argument_checks(lib):
                                   None, None) == 1
     assert lib.bsa_spectral_order_noalloc(None, None, 1, 0, 1, 5, 10, None, None, None, None, None) == 1
     assert lib.bsa_spectral_order_noalloc(None, None, 6, 0, 4, 5, 10, None, None, None, None, None) == 1  # max_kv > nKB
+
+
+def test_block_scores_want_16_byte_aligned_tokens(lib):
+    args = [FAKE_ODD, FAKE, 1, 1, 256, 64, None, None, ctypes.c_float(0.0), 0, FAKE, ctypes.c_size_t(1 << 20),
+            FAKE, None]
+    assert lib.bsa_block_scores(*args) == 1
+    args[0], args[1] = FAKE, ctypes.c_void_p(0x10008)
+    assert lib.bsa_block_scores(*args) == 1
