@@ -47,10 +47,26 @@ import synth  # noqa: E402
 
 METRIC = "block-sparse attn fwd effective TFLOP/s (% of GB300 BF16 TC peak); ms/call"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+# A kernel launched back to back for at least this long runs under the
+# board's power limit (its clock samples show sw_power_cap); it is compared
+# with the GEMM rate sustained under that limit, a shorter run with the burst
+# rate.
+SUSTAINED_AFTER_MS = 100.0
 L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 
 
 # ---------------------------------------------------------------- helpers
+def tensor_peak(peaks: dict, launches: int, avg_ms: float):
+    """(peak TFLOP/s, which) for a kernel timed over `launches` back-to-back
+    launches of `avg_ms` each: the sustained bf16 GEMM rate once the sequence
+    lasts SUSTAINED_AFTER_MS, else the burst rate."""
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    if launches * avg_ms >= SUSTAINED_AFTER_MS:
+        return sustained, "sustained"
+    return burst, "burst"
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -827,22 +843,27 @@ def main():
 
     fwd_avg_ms = sum(fwd_ms) / len(fwd_ms)
     achieved = flops / (fwd_avg_ms * 1e-3) / 1e12
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak, which = tensor_peak(peaks, len(fwd_ms), fwd_avg_ms)
     traffic = recorded_traffic(args, path.order)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic, "kernel": "k_bsa_forward",
-                "peak_source": f"{peak_src} bf16 burst", "ms_per_launch": fwd_avg_ms,
-                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak))}
+                "peak_source": (f"{peak_src} bf16 {which} ({len(fwd_ms)} launches back to back, "
+                                f"{len(fwd_ms) * fwd_avg_ms:.0f} ms)"),
+                "ms_per_launch": fwd_avg_ms, "frac_of_burst": achieved / burst,
+                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained",
+                                                                FALLBACK_PEAKS["bf16_tflops_sustained"]))}
     # A workload whose FLOPs per compulsory byte (Q, K, V read once, O and LSE
     # written once) fall below the measured ridge is bounded by HBM instead.
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     alg_bytes = compulsory_bytes(prob)
-    if flops / alg_bytes < peak * 1e12 / (hbm * 1e9):
+    if flops / alg_bytes < burst * 1e12 / (hbm * 1e9):
         gbs = alg_bytes / (fwd_avg_ms * 1e-3) / 1e9
         roofline.update({"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                          "peak_source": f"{peak_src} HBM copy", "algorithmic_bytes": alg_bytes,
                          "tensor_tflops": achieved})
         roofline.pop("frac_of_sustained")
+        roofline.pop("frac_of_burst")
 
     if rank != 0:
         return
@@ -860,7 +881,7 @@ def main():
             "data": "synthetic", "config": config_dict(prob, args.config, density, world),
             "row_order": {"order": path.order, "chosen_by": "reorder guard" if guard else "--order",
                           "guard": guard, "forward_ms": orders_ms},
-            "pct_of_peak": 100.0 * value / world / peak,
+            "pct_of_peak": 100.0 * value / world / burst,
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": bi,
                     "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms},

@@ -111,3 +111,15 @@ def test_clock_summary_parses_samples():
     assert s.summary()["reasons"] == ["hw_slowdown", "sw_power_cap", "sw_thermal_slowdown"]
     s.lines = []
     assert s.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+
+def test_tensor_peak_by_sequence_length():
+    """A forward timed over a long back-to-back sequence (under the board's
+    power limit) is compared with the sustained GEMM rate, a short one with
+    the burst rate; the measured numbers are used when present."""
+    peaks = {"bf16_tflops": 1909.3, "bf16_tflops_sustained": 1714.8}
+    assert bench.tensor_peak(peaks, 20, 17.3) == (1714.8, "sustained")
+    assert bench.tensor_peak(peaks, 20, 1.15) == (1909.3, "burst")
+    assert bench.tensor_peak(peaks, 10, bench.SUSTAINED_AFTER_MS / 10) == (1714.8, "sustained")
+    assert bench.tensor_peak({}, 1, 1.0) == (bench.FALLBACK_PEAKS["bf16_tflops"], "burst")
+    assert bench.tensor_peak({}, 100, 10.0) == (bench.FALLBACK_PEAKS["bf16_tflops_sustained"], "sustained")
