@@ -516,10 +516,9 @@ bsa_status bsa_gather0_layout(int32_t img_h, int32_t img_w, int32_t n_text, int3
  * computed at run time, outputs scattered back).
  *
  * One thread block per SM walks the query tiles (rows of 7-8 tiles).  Same
- * result as bsa_forward_packed with the same quad_mask (bit for bit) on the
- * maps of bsa_gather0_layout, without reading them (with quad_mask = NULL
- * the two agree to rounding: bsa_forward_packed then runs its unmasked
- * kernel, whose softmax sums in another order): a query tile of two patches is
+ * result as bsa_forward_packed with the same quad_mask (bit for bit, also
+ * with quad_mask = NULL) on the maps of bsa_gather0_layout, without reading
+ * them: a query tile of two patches is
  * a 16-row x 8-column box of the image, a window band an 8-row x 16-column
  * box, a Scatter-group tile 128 tokens at stride groups, a text tile 128
  * consecutive tokens.  O and LSE rows go to the original tokens.

@@ -356,6 +356,16 @@ __device__ __forceinline__ bool softmax_block_rows(uint32_t (&s)[64], int32_t j,
     return rescale;
 }
 
+// P = 0 for this warp's 16 rows of a score buffer (the 16x128b layout the
+// softmax writes P in), for a block that no row of its quadrant sees.
+__device__ __forceinline__ void store_p_zero(uint32_t taddr) {
+    uint32_t z[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) z[c] = 0u;
+    tmem_st16x128_x16(taddr, z);
+    tmem_wait_st();
+}
+
 // A row's sum over its four threads (the same value in each).
 __device__ __forceinline__ float row_sum4(float x) {
     x += __shfl_xor_sync(0xffffffffu, x, 1);
@@ -565,7 +575,6 @@ template <int D, int kPoly, bool kCrm, bool kGather, bool kMask, bool kGeom, boo
 __global__ void __launch_bounds__(threads_for(kGather, kMask), 1) k_bsa_forward(const __grid_constant__ Params P) {
     static_assert(!(kCrm && kMask), "the token mask reads block indices from the lists");
     static_assert(!kGeom || (!kGather && !kCrm), "the geometry mode loads tiles by TMA boxes");
-    static_assert(!kQuad || kMask, "quadrant masks live in the masked variant");
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -901,12 +910,21 @@ __global__ void __launch_bounds__(threads_for(kGather, kMask), 1) k_bsa_forward(
         }
         const float sl2 = P.scale_log2;
         const float* lw_row = P.log_w ? P.log_w + row * max_kv : nullptr;
+        // quadrant visibility of the listed blocks (bit qd of entry j: this
+        // warp's rows see block j), 32 entries at a time, lane e entry base + e
+        const uint8_t* qm_row = (kQuad && P.quad_mask != nullptr) ? P.quad_mask + row * max_kv : nullptr;
+        uint32_t qm_chunk = 0xFu;
+        if constexpr (kQuad) qm_chunk = (qm_row != nullptr && lane < n) ? qm_row[lane] : 0xFu;
         float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};  // l: this thread's share of each row
         bool ok = true;
         float lw_next = (lw_row && n > 0) ? lw_row[0] : 0.0f;
         for (int32_t j = 0; j < n; ++j) {
             const float lw2 = lw_next * kLog2e;
             lw_next = (lw_row && j + 1 < n) ? lw_row[j + 1] : 0.0f;
+            if (kQuad && j > 0 && (j & 31) == 0)
+                qm_chunk = (qm_row != nullptr && j + lane < n) ? qm_row[j + lane] : 0xFu;
+            bool hidden = false;  // warp-uniform: no row of this quadrant sees block j
+            if constexpr (kQuad) hidden = ((__shfl_sync(0xffffffffu, qm_chunk, j & 31) >> qd) & 1u) == 0u;
             const uint32_t sbuf = (uint32_t)(j % kSBuf) * 128u;
             const int32_t pk = ring_pos_k(j);
             const bool w = mbar_wait(smem_u32(&bars->empty[pk % C::kStages]), (uint32_t)(pk / C::kStages) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
@@ -915,6 +933,13 @@ __global__ void __launch_bounds__(threads_for(kGather, kMask), 1) k_bsa_forward(
                 break;
             }
             tc_fence_after();
+            if (kQuad && hidden) {
+                // P_j = 0 for these rows; m, l and O are unchanged
+                store_p_zero(t_base + sbuf);
+                tc_fence_before();
+                mbar_arrive(smem_u32(&bars->p_full[j % kSBuf]));
+                continue;
+            }
             uint32_t s[64];
             auto load_s = [&]() {
                 tmem_ld16x256_x16(t_base + sbuf, s);
@@ -1273,7 +1298,6 @@ struct ItemCfg {
 
 template <int D, int kPoly, bool kMask, bool kGeom, bool kQuad, int kQB>
 __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_items(const __grid_constant__ Params P, int64_t n_items) {
-    static_assert(!kQuad || kMask, "quadrant masks live in the masked variant");
     static_assert(kQB == 1 || kQB == 2, "one or two Q buffers");
     using C = Cfg<D>;
     using IC = ItemCfg<D, kQB>;
@@ -1543,11 +1567,18 @@ __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_it
                 continue;
             }
             const float* lw_row = P.log_w ? P.log_w + it.row * max_kv : nullptr;
+            const uint8_t* qm_row = (kQuad && P.quad_mask != nullptr) ? P.quad_mask + it.row * max_kv : nullptr;
+            uint32_t qm_chunk = 0xFu;
+            if constexpr (kQuad) qm_chunk = (qm_row != nullptr && lane < n) ? qm_row[lane] : 0xFu;
             float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
             float lw_next = lw_row ? lw_row[0] : 0.0f;
             for (int32_t j = 0; j < n; ++j) {
                 const float lw2 = lw_next * kLog2e;
                 lw_next = (lw_row && j + 1 < n) ? lw_row[j + 1] : 0.0f;
+                if (kQuad && j > 0 && (j & 31) == 0)
+                    qm_chunk = (qm_row != nullptr && j + lane < n) ? qm_row[j + lane] : 0xFu;
+                bool hidden = false;  // warp-uniform: no row of this quadrant sees block j
+                if constexpr (kQuad) hidden = ((__shfl_sync(0xffffffffu, qm_chunk, j & 31) >> qd) & 1u) == 0u;
                 const uint32_t gb = g_glob + (uint32_t)j;
                 const uint32_t sbuf = (gb % kSBuf) * 128u;
                 const uint32_t pk = t_glob + (uint32_t)ring_pos_k(j);
@@ -1557,6 +1588,12 @@ __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_it
                     break;
                 }
                 tc_fence_after();
+                if (kQuad && hidden) {
+                    store_p_zero(t_base + sbuf);
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&bars->p_full[gb % kSBuf]));
+                    continue;
+                }
                 uint32_t s[64];
                 auto load_s = [&]() {
                     tmem_ld16x256_x16(t_base + sbuf, s);
@@ -1961,8 +1998,9 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
             ok = encode_image_map(&P.map_kg, a.k, kh, a.N, D, g, true, 0, 0) &&
                  encode_image_map(&P.map_vg, a.v, kh, a.N, D, g, true, 0, 0);
         if (!ok) return BSA_ERR_CUDA;
-        if (items_geometry()) return launch_items<D, true, true, true, 2>(P, (int64_t)gx * gy, stream);
-        return launch_dp<D, kDefaultPoly, false, false, true, true, true>(P, gx, gy, stream);
+        // no token masks in this mode: the row-split softmax with quadrant masks
+        if (items_geometry()) return launch_items<D, false, true, true, 2>(P, (int64_t)gx * gy, stream);
+        return launch_dp<D, kDefaultPoly, false, false, false, true, true>(P, gx, gy, stream);
     }
     if (a.scatter_R > 0) {
         // Scatter geometry mode: every query and key/value tile is 128 tokens
@@ -1983,8 +2021,10 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
     const bool crm = a.crm != nullptr, gather = a.kv_map != nullptr;
     if (a.masked) {
         if (crm) return BSA_ERR_UNSUPPORTED;
+        const bool token_mask = a.causal || a.window > 0 || P.n_valid < a.N;
         if (gather && P.quad_mask != nullptr)
-            return launch_dp<D, kDefaultPoly, false, true, true, false, true>(P, gx, gy, stream);
+            return token_mask ? launch_dp<D, kDefaultPoly, false, true, true, false, true>(P, gx, gy, stream)
+                              : launch_dp<D, kDefaultPoly, false, true, false, false, true>(P, gx, gy, stream);
         if (P.quad_mask != nullptr) return BSA_ERR_UNSUPPORTED;  // packed tiles need kv_map
         if (!gather && P.q_map == nullptr && items_tile_choice(a))
             return launch_items<D, true, false, false, 1>(P, (int64_t)gx * gy, stream);
