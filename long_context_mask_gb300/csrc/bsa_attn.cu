@@ -372,6 +372,50 @@ __device__ __forceinline__ float row_sum4(float x) {
     return x + __shfl_xor_sync(0xffffffffu, x, 2);
 }
 
+// Transpose of a 4 x 4 block of words held by the four threads of a row
+// (thread c of the row holds x[0..3]; afterwards x[j] is thread j's former
+// x[c]), by two butterfly exchanges.
+__device__ __forceinline__ void transpose4(uint32_t x[4], int c) {
+#pragma unroll
+    for (int m = 2; m >= 1; m >>= 1) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j & m) continue;
+            const bool hi = (c & m) != 0;
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, hi ? x[j] : x[j | m], m);
+            if (hi) x[j] = recv;
+            else x[j | m] = recv;
+        }
+    }
+}
+
+// O rows a and b (16x256b layout: o[4k..4k+3] = row a's columns 8k + 2c,
+// 8k + 2c + 1, then row b's, c = thread % 4) divided by their sums, as bf16.
+// Within each group of four words the row's four threads exchange words, so
+// that thread c then holds 8 consecutive columns, 8 (4g + c) .., and writes
+// them with one 16-byte store: the four threads of a row write 64 bytes of
+// it per store instead of 16.  Every lane takes part in the exchanges; a
+// null row pointer skips that row's stores.
+template <int D>
+__device__ __forceinline__ void store_o_pairs(const uint32_t* o, float inv_a, float inv_b, __nv_bfloat16* row_a,
+                                              __nv_bfloat16* row_b) {
+    const int c = threadIdx.x & 3;
+#pragma unroll
+    for (int g = 0; g < D / 32; ++g) {
+        uint32_t xa[4], xb[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int k = 4 * g + j;
+            xa[j] = pack_bf16(__uint_as_float(o[4 * k]) * inv_a, __uint_as_float(o[4 * k + 1]) * inv_a);
+            xb[j] = pack_bf16(__uint_as_float(o[4 * k + 2]) * inv_b, __uint_as_float(o[4 * k + 3]) * inv_b);
+        }
+        transpose4(xa, c);
+        transpose4(xb, c);
+        if (row_a) *reinterpret_cast<uint4*>(row_a + 8 * (4 * g + c)) = make_uint4(xa[0], xa[1], xa[2], xa[3]);
+        if (row_b) *reinterpret_cast<uint4*>(row_b + 8 * (4 * g + c)) = make_uint4(xb[0], xb[1], xb[2], xb[3]);
+    }
+}
+
 // O columns of rows a and b out of tensor memory (16x256b layout, D / 4 per
 // row per thread), multiplied by per-row factors, back in.
 template <int D>
@@ -395,14 +439,7 @@ __device__ __forceinline__ void store_o_rows(uint32_t taddr, float inv_a, float 
     if constexpr (D == 128) tmem_ld16x256_x16(taddr, o);
     else tmem_ld16x256_x8(taddr, o);
     tmem_wait_ld();
-    const int c = 2 * (threadIdx.x & 3);
-#pragma unroll
-    for (int k = 0; k < D / 8; ++k) {
-        const uint32_t pa = pack_bf16(__uint_as_float(o[4 * k]) * inv_a, __uint_as_float(o[4 * k + 1]) * inv_a);
-        const uint32_t pb = pack_bf16(__uint_as_float(o[4 * k + 2]) * inv_b, __uint_as_float(o[4 * k + 3]) * inv_b);
-        if (row_a) *reinterpret_cast<uint32_t*>(row_a + 8 * k + c) = pa;
-        if (row_b) *reinterpret_cast<uint32_t*>(row_b + 8 * k + c) = pb;
-    }
+    store_o_pairs<D>(o, inv_a, inv_b, row_a, row_b);
 }
 
 // One block of the online softmax for this thread's row.  On entry s holds
@@ -1252,30 +1289,33 @@ struct ItemBarriers {
 struct Item {
     int64_t bh, bh_kv, row;
     int32_t qb, n;
+    int32_t n_raw;  // the count as read (n is clamped to [0, max_kv])
 };
 
+__device__ __forceinline__ void report_count(const Params& P, int32_t n) {
+    if (n < 0 || n > P.max_kv) raise_status(P.status, n < 0 ? BSA_ERR_BOUNDS : BSA_ERR_OVERFLOW);
+}
+
 // Item f is execution slot f % nQB of head f / nQB.  false: a bad row order
-// entry (every role skips the item alike).  `report`: raise the status for
-// bad entries (one role does).
-__device__ __forceinline__ bool decode_item(const Params& P, int64_t f, Item& it, bool report = false) {
+// entry (every role skips the item alike; the producer reports it, and a bad
+// count, with report_count once it reaches the item).  Nothing here branches
+// on the count, so a role can decode the next item while the current one
+// runs without waiting for the load.
+__device__ __forceinline__ bool decode_item(const Params& P, int64_t f, Item& it) {
     const int32_t nQB = P.nQB;
     it.bh = f / nQB;
     const int32_t slot = (int32_t)(f - it.bh * nQB);
     int32_t qb = slot;
     if (P.row_perm != nullptr) {
         qb = P.row_perm[it.bh * nQB + slot];
-        if (qb < 0 || qb >= nQB) {
-            if (report) raise_status(P.status, BSA_ERR_BOUNDS);
-            return false;
-        }
+        if (qb < 0 || qb >= nQB) return false;
     }
     it.qb = qb;
     it.bh_kv = (it.bh / P.H) * (P.H / P.group) + (it.bh % P.H) / P.group;
     it.row = it.bh * nQB + qb;
-    int32_t n = P.kv_cnt[it.row];
-    if (report && (n < 0 || n > P.max_kv)) raise_status(P.status, n < 0 ? BSA_ERR_BOUNDS : BSA_ERR_OVERFLOW);
-    n = n < 0 ? 0 : (n > P.max_kv ? P.max_kv : n);
-    it.n = n;
+    const int32_t n = P.kv_cnt[it.row];
+    it.n_raw = n;
+    it.n = n < 0 ? 0 : (n > P.max_kv ? P.max_kv : n);
     return true;
 }
 
@@ -1359,11 +1399,31 @@ __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_it
         uint32_t t_glob = 0, qi = 0;
         uint32_t issued = 0, q_issued = 0;  // copies started (ring positions, Q loads)
         bool ok = true;
+        // Items are decoded one ahead: the next item's count and first 64 list
+        // entries (lane e: entries e, 32 + e) load while this item's copies
+        // are issued, so that no item starts by waiting for them.
+        Item next_it{};
+        bool next_ok = item_of(0) < n_items && decode_item(P, item_of(0), next_it);
+        int32_t next_e0 = 0, next_e1 = 0;
+        auto load_entries = [&]() {
+            const int32_t* l = P.kv_idx + next_it.row * max_kv;
+            next_e0 = next_ok && lane < max_kv ? l[lane] : 0;
+            next_e1 = next_ok && 32 + lane < max_kv ? l[32 + lane] : 0;
+        };
+        load_entries();
         for (int64_t w = 0; ok; ++w) {
-            const int64_t f = item_of(w);
-            if (f >= n_items) break;
-            Item it;
-            if (!decode_item(P, f, it, lane == 0)) continue;
+            if (item_of(w) >= n_items) break;
+            const Item it = next_it;
+            const bool it_ok = next_ok;
+            const int32_t cur_e0 = next_e0, cur_e1 = next_e1;
+            next_ok = item_of(w + 1) < n_items && decode_item(P, item_of(w + 1), next_it);
+            load_entries();
+            // bad entries are reported here, once the item's values are needed
+            if (!it_ok) {
+                if (lane == 0) raise_status(P.status, BSA_ERR_BOUNDS);  // a row-order entry out of range
+                continue;
+            }
+            if (lane == 0) report_count(P, it.n_raw);
             const int32_t n = it.n;
             if (n == 0) continue;
             const int32_t* list = P.kv_idx + it.row * max_kv;
@@ -1388,15 +1448,16 @@ __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_it
             // their own 32-entry window, with the next window already loaded
             // (lane e holds entry base + e): every entry is read once, about 32
             // tiles before it is needed.
-            auto fetch = [&](int32_t e) -> int32_t {
-                int32_t kb = e < n ? list[e] : 0;
+            auto checked = [&](int32_t e, int32_t kb) -> int32_t {
+                kb = e < n ? kb : 0;
                 if (kb < 0 || kb >= nKB) {
                     raise_status(P.status, BSA_ERR_BOUNDS);
                     kb = 0;  // keeps the pipeline in step; this row's result is unspecified
                 }
                 return kb;
             };
-            int32_t k_base = 0, k_cur = fetch(lane), k_nxt = fetch(32 + lane);
+            auto fetch = [&](int32_t e) -> int32_t { return checked(e, e < n ? list[e] : 0); };
+            int32_t k_base = 0, k_cur = checked(lane, cur_e0), k_nxt = checked(32 + lane, cur_e1);
             int32_t v_base = 0, v_cur = k_cur, v_nxt = k_nxt;
             auto stream_kb = [&](int32_t e, int32_t& base, int32_t& cur, int32_t& nxt) -> int32_t {
                 while (e >= base + 32) {
@@ -1462,11 +1523,14 @@ __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_it
         auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
             return __all_sync(0xffffffffu, mbar_wait(bar, parity, kWaitNs, P.status, BSA_ERR_TIMEOUT));
         };
+        Item next_it{};  // decoded one ahead (see the producer)
+        bool next_ok = item_of(0) < n_items && decode_item(P, item_of(0), next_it);
         for (int64_t w = 0; ok; ++w) {
-            const int64_t f = item_of(w);
-            if (f >= n_items) break;
-            Item it;
-            if (!decode_item(P, f, it) || it.n == 0) continue;
+            if (item_of(w) >= n_items) break;
+            const Item it = next_it;
+            const bool it_ok = next_ok;
+            next_ok = item_of(w + 1) < n_items && decode_item(P, item_of(w + 1), next_it);
+            if (!it_ok || it.n == 0) continue;
             const int32_t n = it.n;
             const uint32_t qbuf = qi % kQB;
             ok = wait_all(smem_u32(&bars->q_full[qbuf]), (qi / kQB) & 1u);
@@ -1543,11 +1607,14 @@ __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_it
         const float sl2 = P.scale_log2;
         uint32_t t_glob = 0, g_glob = 0;
         bool ok = true;
+        Item next_it{};  // decoded one ahead (see the producer)
+        bool next_ok = item_of(0) < n_items && decode_item(P, item_of(0), next_it);
         for (int64_t w = 0; ok; ++w) {
-            const int64_t f = item_of(w);
-            if (f >= n_items) break;
-            Item it;
-            if (!decode_item(P, f, it)) continue;
+            if (item_of(w) >= n_items) break;
+            const Item it = next_it;
+            const bool it_ok = next_ok;
+            next_ok = item_of(w + 1) < n_items && decode_item(P, item_of(w + 1), next_it);
+            if (!it_ok) continue;
             const int32_t n = it.n;
             const int32_t tok_a = kGeom ? g0::query_token(P.geo, it.qb * 128 + ra) : it.qb * 128 + ra;
             const int32_t tok_b = kGeom ? g0::query_token(P.geo, it.qb * 128 + rb) : it.qb * 128 + rb;
@@ -1639,13 +1706,7 @@ __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_it
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(smem_u32(&bars->o_free));
-#pragma unroll
-            for (int k = 0; k < D / 8; ++k) {
-                *reinterpret_cast<uint32_t*>(row_a + 8 * k + c) =
-                    pack_bf16(__uint_as_float(o[4 * k]) * inv_a, __uint_as_float(o[4 * k + 1]) * inv_a);
-                *reinterpret_cast<uint32_t*>(row_b + 8 * k + c) =
-                    pack_bf16(__uint_as_float(o[4 * k + 2]) * inv_b, __uint_as_float(o[4 * k + 3]) * inv_b);
-            }
+            store_o_pairs<D>(o, inv_a, inv_b, row_a, row_b);
             if ((lane & 3) == 0) {
                 P.lse[it.bh * N + tok_a] = l_a > 0.0f ? (m[0] + log2f(l_a)) * kLn2 : -INFINITY;
                 P.lse[it.bh * N + tok_b] = l_b > 0.0f ? (m[1] + log2f(l_b)) * kLn2 : -INFINITY;
