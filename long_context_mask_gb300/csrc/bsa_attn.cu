@@ -390,30 +390,46 @@ __device__ __forceinline__ void transpose4(uint32_t x[4], int c) {
 }
 
 // O rows a and b (16x256b layout: o[4k..4k+3] = row a's columns 8k + 2c,
-// 8k + 2c + 1, then row b's, c = thread % 4) divided by their sums, as bf16.
-// Within each group of four words the row's four threads exchange words, so
-// that thread c then holds 8 consecutive columns, 8 (4g + c) .., and writes
-// them with one 16-byte store: the four threads of a row write 64 bytes of
-// it per store instead of 16.  Every lane takes part in the exchanges; a
-// null row pointer skips that row's stores.
+// 8k + 2c + 1, then row b's, c = thread % 4) divided by their sums, as bf16
+// pairs: pk[k] row a's, pk[D/8 + k] row b's.
 template <int D>
-__device__ __forceinline__ void store_o_pairs(const uint32_t* o, float inv_a, float inv_b, __nv_bfloat16* row_a,
-                                              __nv_bfloat16* row_b) {
+__device__ __forceinline__ void pack_o_pairs(const uint32_t* o, float inv_a, float inv_b, uint32_t* pk) {
+#pragma unroll
+    for (int k = 0; k < D / 8; ++k) {
+        pk[k] = pack_bf16(__uint_as_float(o[4 * k]) * inv_a, __uint_as_float(o[4 * k + 1]) * inv_a);
+        pk[D / 8 + k] = pack_bf16(__uint_as_float(o[4 * k + 2]) * inv_b, __uint_as_float(o[4 * k + 3]) * inv_b);
+    }
+}
+
+// Stores packed O rows.  Within each group of four words the row's four
+// threads exchange words, so that thread c then holds 8 consecutive columns,
+// 8 (4g + c) .., and writes them with one 16-byte store: the four threads of
+// a row write 64 bytes of it per store instead of 16.  Every lane takes part
+// in the exchanges; a null row pointer skips that row's stores.
+template <int D>
+__device__ __forceinline__ void store_packed_pairs(const uint32_t* pk, __nv_bfloat16* row_a, __nv_bfloat16* row_b) {
     const int c = threadIdx.x & 3;
 #pragma unroll
     for (int g = 0; g < D / 32; ++g) {
         uint32_t xa[4], xb[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int k = 4 * g + j;
-            xa[j] = pack_bf16(__uint_as_float(o[4 * k]) * inv_a, __uint_as_float(o[4 * k + 1]) * inv_a);
-            xb[j] = pack_bf16(__uint_as_float(o[4 * k + 2]) * inv_b, __uint_as_float(o[4 * k + 3]) * inv_b);
+            xa[j] = pk[4 * g + j];
+            xb[j] = pk[D / 8 + 4 * g + j];
         }
         transpose4(xa, c);
         transpose4(xb, c);
         if (row_a) *reinterpret_cast<uint4*>(row_a + 8 * (4 * g + c)) = make_uint4(xa[0], xa[1], xa[2], xa[3]);
         if (row_b) *reinterpret_cast<uint4*>(row_b + 8 * (4 * g + c)) = make_uint4(xb[0], xb[1], xb[2], xb[3]);
     }
+}
+
+template <int D>
+__device__ __forceinline__ void store_o_pairs(const uint32_t* o, float inv_a, float inv_b, __nv_bfloat16* row_a,
+                                              __nv_bfloat16* row_b) {
+    uint32_t pk[D / 4];
+    pack_o_pairs<D>(o, inv_a, inv_b, pk);
+    store_packed_pairs<D>(pk, row_a, row_b);
 }
 
 // O columns of rows a and b out of tensor memory (16x256b layout, D / 4 per
@@ -1609,6 +1625,11 @@ __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_it
         bool ok = true;
         Item next_it{};  // decoded one ahead (see the producer)
         bool next_ok = item_of(0) < n_items && decode_item(P, item_of(0), next_it);
+        // An item's normalised O waits in registers and is stored while the
+        // next item's last PV runs, off the softmax warps' critical path.
+        uint32_t pend[D / 4];
+        __nv_bfloat16 *pend_a = nullptr, *pend_b = nullptr;
+        bool pending = false;
         for (int64_t w = 0; ok; ++w) {
             if (item_of(w) >= n_items) break;
             const Item it = next_it;
@@ -1686,9 +1707,10 @@ __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_it
                 mbar_arrive(smem_u32(&bars->p_full[gb % kSBuf]));
             }
             if (!ok) break;
-            // Epilogue: once PV_{n-1} has run, read O out of tensor memory, hand
-            // the accumulator to the next item (o_free), then normalise and
-            // store while the next item's products proceed.
+            // Epilogue: the previous item's O leaves while PV_{n-1} runs; once
+            // it has run, read O out of tensor memory, hand the accumulator to
+            // the next item (o_free) and keep the normalised rows for later.
+            if (pending) store_packed_pairs<D>(pend, pend_a, pend_b);
             {
                 const uint32_t pv = t_glob + (uint32_t)ring_pos_v(n - 1, n);
                 const bool wt = mbar_wait(smem_u32(&bars->empty[pv % S]), (pv / S) & 1u, kWaitNs, P.status, BSA_ERR_TIMEOUT);
@@ -1706,7 +1728,10 @@ __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_it
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(smem_u32(&bars->o_free));
-            store_o_pairs<D>(o, inv_a, inv_b, row_a, row_b);
+            pack_o_pairs<D>(o, inv_a, inv_b, pend);
+            pend_a = row_a;
+            pend_b = row_b;
+            pending = true;
             if ((lane & 3) == 0) {
                 P.lse[it.bh * N + tok_a] = l_a > 0.0f ? (m[0] + log2f(l_a)) * kLn2 : -INFINITY;
                 P.lse[it.bh * N + tok_b] = l_b > 0.0f ? (m[1] + log2f(l_b)) * kLn2 : -INFINITY;
@@ -1714,6 +1739,7 @@ __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_it
             t_glob += 2u * (uint32_t)n;
             g_glob += (uint32_t)n;
         }
+        if (ok && pending) store_packed_pairs<D>(pend, pend_a, pend_b);
         if (!ok && lane == 0) items_set_abort(bars, P.status);
     } else {
         // ------------------------------------------------------------ softmax + epilogue
