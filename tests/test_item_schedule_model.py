@@ -11,9 +11,11 @@ which completes tile and Q loads out of order, and the tensor pipe, which
 runs MMA groups and commits in issue order) as interleaved processes over
 barrier completion counts, with randomised scheduling, row lengths and
 rescale decisions, and checks that
-  * no run deadlocks, and
-  * no barrier ever completes a second time past a waiter's target
-    (the parity of every wait is unambiguous).
+  * no run deadlocks,
+  * no barrier ever completes a second time past a waiter's target, and
+  * no wait is issued while its barrier still lacks the completion before
+    the one it waits for
+(together: the parity of every wait is unambiguous).
 The waits, arrivals and commits follow k_bsa_forward_items in the order the
 kernel issues them; the ring size S and the Q buffer count take the values of
 the kernel's instantiations.
@@ -175,6 +177,10 @@ class Model:
                 self.waiting.pop(c, None)
                 try:
                     w = next(self.procs[c])
+                    # a parity wait for completion k issued while the barrier
+                    # has completed only k - 1 times would pass at once
+                    assert self.count.get(w[1], 0) >= w[2], f"{c} waits for completion {w[2]} of {w[1]}, " \
+                        f"which has completed {self.count.get(w[1], 0)} times"
                     state[c] = w
                     self.waiting[c] = (w[1], w[2])
                 except StopIteration:
