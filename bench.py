@@ -374,10 +374,11 @@ def sample_heads(prob):
     return None if per_head_flops < 2e12 or bh <= 2 else (0, bh - 1)
 
 
-def time_oracle(prob, lists, budget_s: float, max_blocks: int | None = None, seed: int = 0):
+def time_oracle(prob, lists, budget_s: float, max_blocks: int | None = None, seed: int = 0,
+                full_heads: bool = False):
     """Oracle on a bounded sample of query blocks (seeded, spread over the
-    heads of sample_heads()).  Returns (effective TFLOP/s, seconds, blocks,
-    threads)."""
+    heads of sample_heads()), or with full_heads every query block of those
+    heads.  Returns (effective TFLOP/s, seconds, blocks, threads)."""
     import oracle
     if is_image_layer(prob):
         return time_oracle_image(prob, budget_s, seed)
@@ -399,7 +400,7 @@ def time_oracle(prob, lists, budget_s: float, max_blocks: int | None = None, see
         t_total += time.perf_counter() - t0
         fl += float(cnt[sel].sum()) * 4 * 128 * 128 * prob.D
         done += len(sel)
-        if t_total >= budget_s or (max_blocks and done >= max_blocks):
+        if not (full_heads and heads is not None) and (t_total >= budget_s or (max_blocks and done >= max_blocks)):
             break
     return fl / t_total / 1e12, t_total, done, oracle.num_threads()
 
@@ -869,11 +870,22 @@ def main():
         return
     cpu = None
     if not args.no_cpu_baseline:
-        v, s, b, threads = time_oracle(prob, host_lists(prob, pooled), args.cpu_budget)
-        cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"{b} {sample_unit(prob)} ({sample_text(prob)}), "
-                         f"{s:.1f} s fp64 on host cores",
-               "full_workload_s_extrapolated": flops / (v * 1e12) if v else None}
+        heads = sample_heads(prob)
+        full = heads is not None and not is_image_layer(prob)
+        v, s, b, threads = time_oracle(prob, host_lists(prob, pooled), args.cpu_budget, full_heads=full)
+        if full:
+            # the CPU plan's subset for workloads too large for the oracle:
+            # whole heads (the first and the last), then a labelled linear
+            # extrapolation to every head
+            sample = (f"{len(heads)} full heads ({heads[0]} and {heads[1]}): {b} {sample_unit(prob)}, "
+                      f"{s:.1f} s fp64 on host cores; full workload extrapolated as per-head time x "
+                      f"{prob.B * prob.H} heads")
+            extrapolated = s / len(heads) * prob.B * prob.H
+        else:
+            sample = f"{b} {sample_unit(prob)} ({sample_text(prob)}), {s:.1f} s fp64 on host cores"
+            extrapolated = flops / (v * 1e12) if v else None
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample,
+               "full_workload_s_extrapolated": extrapolated}
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
             "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step,
             "ms_per_step_median": statistics.median(step_ms) if world == 1 else None,

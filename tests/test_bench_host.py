@@ -123,3 +123,15 @@ def test_tensor_peak_by_sequence_length():
     assert bench.tensor_peak(peaks, 10, bench.SUSTAINED_AFTER_MS / 10) == (1714.8, "sustained")
     assert bench.tensor_peak({}, 1, 1.0) == (bench.FALLBACK_PEAKS["bf16_tflops"], "burst")
     assert bench.tensor_peak({}, 100, 10.0) == (bench.FALLBACK_PEAKS["bf16_tflops_sustained"], "sustained")
+
+
+def test_cpu_baseline_full_heads(monkeypatch):
+    """Workloads too large for the oracle are timed on whole heads (every
+    query block of the first and the last head), not on a time budget."""
+    prob = synth.CONFIGS[1]()
+    monkeypatch.setattr(bench, "sample_heads", lambda p: (0, p.B * p.H - 1))
+    lists = bench.host_lists(prob)
+    v, s, b, threads = bench.time_oracle(prob, lists, budget_s=1e-9, full_heads=True)
+    assert b == 2 * prob.nqb and v > 0 and threads >= 1
+    _, _, b_budget, _ = bench.time_oracle(prob, lists, budget_s=1e-9)
+    assert b_budget < b
