@@ -1317,10 +1317,12 @@ __device__ __forceinline__ void report_count(const Params& P, int32_t n) {
 // count, with report_count once it reaches the item).  Nothing here branches
 // on the count, so a role can decode the next item while the current one
 // runs without waiting for the load.
-__device__ __forceinline__ bool decode_item(const Params& P, int64_t f, Item& it) {
+__device__ __forceinline__ bool decode_item(const Params& P, int64_t f, Item& it, int64_t BH) {
+    // BH > 0: heads interleaved, consecutive items are the same execution slot
+    // of consecutive heads (see kInterleave); else head-major
     const int32_t nQB = P.nQB;
-    it.bh = f / nQB;
-    const int32_t slot = (int32_t)(f - it.bh * nQB);
+    it.bh = BH > 0 ? f % BH : f / nQB;
+    const int32_t slot = (int32_t)(BH > 0 ? f / BH : f - it.bh * nQB);
     int32_t qb = slot;
     if (P.row_perm != nullptr) {
         qb = P.row_perm[it.bh * nQB + slot];
@@ -1371,6 +1373,13 @@ __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_it
     auto item_of = [&](int64_t w) -> int64_t {
         return w * G + ((w & 1) ? (G - 1 - (int64_t)blockIdx.x) : (int64_t)blockIdx.x);
     };
+    // The Gather 0 layer walks the heads interleaved (item f is execution slot
+    // f / BH of head f % BH): a text query tile lists about three times the
+    // tiles of an image tile, and head-major order hands some blocks two of
+    // them and others none.  Elsewhere head-major order keeps a wave on
+    // neighbouring rows of one head (DRAM pages and L2 reuse).
+    constexpr bool kInterleave = kGeom && kQuad;
+    const int64_t heads_il = kInterleave ? n_items / P.nQB : 0;
 
     if (*reinterpret_cast<const volatile int32_t*>(P.status) == BSA_ERR_TIMEOUT) return;
 
@@ -1419,7 +1428,7 @@ __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_it
         // entries (lane e: entries e, 32 + e) load while this item's copies
         // are issued, so that no item starts by waiting for them.
         Item next_it{};
-        bool next_ok = item_of(0) < n_items && decode_item(P, item_of(0), next_it);
+        bool next_ok = item_of(0) < n_items && decode_item(P, item_of(0), next_it, heads_il);
         int32_t next_e0 = 0, next_e1 = 0;
         auto load_entries = [&]() {
             const int32_t* l = P.kv_idx + next_it.row * max_kv;
@@ -1432,7 +1441,7 @@ __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_it
             const Item it = next_it;
             const bool it_ok = next_ok;
             const int32_t cur_e0 = next_e0, cur_e1 = next_e1;
-            next_ok = item_of(w + 1) < n_items && decode_item(P, item_of(w + 1), next_it);
+            next_ok = item_of(w + 1) < n_items && decode_item(P, item_of(w + 1), next_it, heads_il);
             load_entries();
             // bad entries are reported here, once the item's values are needed
             if (!it_ok) {
@@ -1540,12 +1549,12 @@ __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_it
             return __all_sync(0xffffffffu, mbar_wait(bar, parity, kWaitNs, P.status, BSA_ERR_TIMEOUT));
         };
         Item next_it{};  // decoded one ahead (see the producer)
-        bool next_ok = item_of(0) < n_items && decode_item(P, item_of(0), next_it);
+        bool next_ok = item_of(0) < n_items && decode_item(P, item_of(0), next_it, heads_il);
         for (int64_t w = 0; ok; ++w) {
             if (item_of(w) >= n_items) break;
             const Item it = next_it;
             const bool it_ok = next_ok;
-            next_ok = item_of(w + 1) < n_items && decode_item(P, item_of(w + 1), next_it);
+            next_ok = item_of(w + 1) < n_items && decode_item(P, item_of(w + 1), next_it, heads_il);
             if (!it_ok || it.n == 0) continue;
             const int32_t n = it.n;
             const uint32_t qbuf = qi % kQB;
@@ -1624,7 +1633,7 @@ __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_it
         uint32_t t_glob = 0, g_glob = 0;
         bool ok = true;
         Item next_it{};  // decoded one ahead (see the producer)
-        bool next_ok = item_of(0) < n_items && decode_item(P, item_of(0), next_it);
+        bool next_ok = item_of(0) < n_items && decode_item(P, item_of(0), next_it, heads_il);
         // An item's normalised O waits in registers and is stored while the
         // next item's last PV runs, off the softmax warps' critical path.
         uint32_t pend[D / 4];
@@ -1634,7 +1643,7 @@ __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_it
             if (item_of(w) >= n_items) break;
             const Item it = next_it;
             const bool it_ok = next_ok;
-            next_ok = item_of(w + 1) < n_items && decode_item(P, item_of(w + 1), next_it);
+            next_ok = item_of(w + 1) < n_items && decode_item(P, item_of(w + 1), next_it, heads_il);
             if (!it_ok) continue;
             const int32_t n = it.n;
             const int32_t tok_a = kGeom ? g0::query_token(P.geo, it.qb * 128 + ra) : it.qb * 128 + ra;
@@ -1753,7 +1762,7 @@ __global__ void __launch_bounds__(threads_for(false, kMask), 1) k_bsa_forward_it
             const int64_t f = item_of(w);
             if (f >= n_items) break;
             Item it;
-            if (!decode_item(P, f, it)) continue;
+            if (!decode_item(P, f, it, heads_il)) continue;
             const int32_t n = it.n;
             const int32_t tok = kGeom ? g0::query_token(P.geo, it.qb * 128 + r) : it.qb * 128 + r;
             __nv_bfloat16* orow = P.o + (it.bh * N + tok) * D;
