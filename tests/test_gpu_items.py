@@ -73,3 +73,39 @@ def test_items_match_one_block_per_row(case):
     o2, l2 = _run(case, "per_row")
     assert np.array_equal(o1, o2)
     assert np.array_equal(l1.view(np.int32), l2.view(np.int32))
+
+
+def test_items_flag_bad_entries():
+    """Per-item blocks meet bad list entries, counts and row-order entries the
+    way one block per row does: the status word says which, nothing faults,
+    and the next launch runs clean."""
+    prob = synth.threshold(H=2, N=8192)
+    T = torch.from_numpy(prob.T).cuda()
+    idx = torch.empty((prob.rows, prob.nqb), dtype=torch.int32, device="cuda")
+    cnt = torch.empty(prob.rows, dtype=torch.int32, device="cuda")
+    bsa.build_index(bsa.IDX_THRESHOLD_F32, T, idx, cnt, p=prob.p)
+    q, k, v = prob.q.cuda(), prob.k.cuda(), prob.v.cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    bsa.set_forward_options(schedule="per_item")
+    try:
+        bad = idx.clone()
+        bad[5, 0] = prob.nqb + 7                 # a KV block out of range
+        bsa.forward(q, k, v, bad, cnt, o, lse)
+        torch.cuda.synchronize()
+        assert bsa.device_status() == 6          # BSA_ERR_BOUNDS
+        over = cnt.clone()
+        over[3] = idx.shape[1] + 5               # a count above the list capacity
+        bsa.forward(q, k, v, idx, over, o, lse)
+        torch.cuda.synchronize()
+        assert bsa.device_status() == 3          # BSA_ERR_OVERFLOW
+        perm = torch.arange(prob.nqb, dtype=torch.int32, device="cuda").repeat(2, 1)
+        perm[1, 4] = prob.nqb                    # a row-order entry out of range
+        bsa.forward(q, k, v, idx, cnt, o, lse, row_perm=perm)
+        torch.cuda.synchronize()
+        assert bsa.device_status() == 6
+        bsa.forward(q, k, v, idx, cnt, o, lse)
+        torch.cuda.synchronize()
+        assert bsa.device_status() == 0
+    finally:
+        bsa.set_forward_options()
