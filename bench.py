@@ -746,6 +746,10 @@ def main():
         # ---- timed region: K steps (L2 flushed before each, outside the events)
         barrier(world)
         torch.cuda.synchronize()
+        # extra flushes ahead of the loop keep the GPU busy while the host
+        # enqueues the first steps, so that no step's events span host time
+        for _ in range(3):
+            flush.zero_()
         for i in range(K):
             flush.zero_()
             ev[i][0].record(stream)
