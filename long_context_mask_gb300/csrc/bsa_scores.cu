@@ -11,9 +11,9 @@
 //   k_block_means   one thread block per (head, block, tensor): the fp32 mean
 //                   of the block's 128 rows (gathered through the map), read
 //                   with 16-byte loads; written to the caller's workspace.
-//   k_block_scores  per head, a 64 x 64 tile of  mean(Q_u) . mean(K_v) * scale
-//                   (or its exponential) per thread block, from shared-memory
-//                   tiles of the two mean matrices.
+//   k_block_scores  per head, a 128 x 128 tile of  mean(Q_u) . mean(K_v) * scale
+//                   (or its exponential) per thread block, 8 x 8 outputs per
+//                   thread from shared-memory stages of the two mean matrices.
 // The work is a read of Q and K (HBM-bound) and a small fp32 product.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -25,8 +25,6 @@
 namespace bsa {
 namespace {
 
-constexpr int kTileS = 64;   // score tile edge
-constexpr int kKChunk = 32;  // columns of the mean matrices staged per step
 
 // One thread block (128 threads) per (head, block, tensor).  D / 8 threads
 // cover a row with 16-byte loads (8 columns each) and 128 / (D / 8) rows are
@@ -76,51 +74,70 @@ __global__ void __launch_bounds__(kMeanThreads) k_block_means(
     }
 }
 
+// One thread block (256 threads) per 128 x 128 tile of one head's score
+// matrix.  Per step the block stages 16 columns of the two mean matrices in
+// shared memory, transposed (column k of the means is row k of the stage);
+// thread (ty, tx) accumulates rows 8 ty .. 8 ty + 7 against columns
+// tx + 16 j (j < 8): two 16-byte loads of its rows and eight 4-byte loads of
+// its columns per 64 FMAs, and its stores along a row are consecutive across
+// the warp's threads.
+constexpr int kScoreTile = 128;
+constexpr int kScoreK = 16;
 __global__ void __launch_bounds__(256) k_block_scores(const float* __restrict__ means,
                                                       int64_t per_tensor, int32_t nb, int32_t D,
                                                       float scale, int32_t mode,
                                                       float* __restrict__ scores) {
-    __shared__ float qs[kTileS][kKChunk + 1];
-    __shared__ float ks[kTileS][kKChunk + 1];
+    __shared__ __align__(16) float as[kScoreK][kScoreTile + 4];
+    __shared__ __align__(16) float bs[kScoreK][kScoreTile + 4];
     const int64_t bh = blockIdx.z;
-    const int32_t u0 = blockIdx.y * kTileS, v0 = blockIdx.x * kTileS;
+    const int32_t u0 = blockIdx.y * kScoreTile, v0 = blockIdx.x * kScoreTile;
     const float* qm = means + bh * nb * (int64_t)D;
     const float* km = means + per_tensor + bh * nb * (int64_t)D;
-    // each thread owns a 4 x 4 patch of the 64 x 64 tile
-    const int tr = (threadIdx.x / 16) * 4, tc = (threadIdx.x % 16) * 4;
-    float acc[4][4] = {};
-    for (int32_t d0 = 0; d0 < D; d0 += kKChunk) {
-        for (int i = threadIdx.x; i < kTileS * kKChunk; i += blockDim.x) {
-            const int r = i / kKChunk, c = i % kKChunk;
-            qs[r][c] = (u0 + r < nb && d0 + c < D) ? qm[(int64_t)(u0 + r) * D + d0 + c] : 0.f;
-            ks[r][c] = (v0 + r < nb && d0 + c < D) ? km[(int64_t)(v0 + r) * D + d0 + c] : 0.f;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    // staging: thread t copies row t / 2, columns 8 (t % 2) .. + 7 of each tile
+    const int sr = threadIdx.x >> 1, sc = (threadIdx.x & 1) * 8;
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int32_t d0 = 0; d0 < D; d0 += kScoreK) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int32_t d = d0 + sc + j;
+            as[sc + j][sr] = (u0 + sr < nb && d < D) ? qm[(int64_t)(u0 + sr) * D + d] : 0.f;
+            bs[sc + j][sr] = (v0 + sr < nb && d < D) ? km[(int64_t)(v0 + sr) * D + d] : 0.f;
         }
         __syncthreads();
-#pragma unroll 4
-        for (int c = 0; c < kKChunk; ++c) {
-            float a[4], bb[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                a[i] = qs[tr + i][c];
-                bb[i] = ks[tc + i][c];
-            }
+        for (int c = 0; c < kScoreK; ++c) {
+            const float4 a0 = *reinterpret_cast<const float4*>(&as[c][ty * 8]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&as[c][ty * 8 + 4]);
+            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            float bv[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int j = 0; j < 8; ++j) bv[j] = bs[c][tx + 16 * j];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], bv[j], acc[i][j]);
         }
         __syncthreads();
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i) {
+        const int32_t u = u0 + ty * 8 + i;
+        if (u >= nb) continue;
+        float* row = scores + (bh * nb + u) * (int64_t)nb;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int32_t u = u0 + tr + i, v = v0 + tc + j;
-            if (u < nb && v < nb) {
-                const float s = acc[i][j] * scale;
-                scores[(bh * nb + u) * (int64_t)nb + v] = mode == 1 ? expf(s) : s;
+        for (int j = 0; j < 8; ++j) {
+            const int32_t v = v0 + tx + 16 * j;
+            if (v < nb) {
+                const float sv = acc[i][j] * scale;
+                row[v] = mode == 1 ? expf(sv) : sv;
             }
         }
+    }
 }
 
 }  // namespace
@@ -139,7 +156,7 @@ cudaError_t launch_block_scores(const void* q, const void* k, int32_t B, int32_t
     k_block_means<<<dim3((unsigned)nb, (unsigned)BH, 2), kMeanThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), N, D, q_map,
         kv_map, workspace, per_tensor, status);
-    const unsigned tiles = (unsigned)((nb + kTileS - 1) / kTileS);
+    const unsigned tiles = (unsigned)((nb + kScoreTile - 1) / kScoreTile);
     const float sc = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
     k_block_scores<<<dim3(tiles, tiles, (unsigned)BH), 256, 0, stream>>>(workspace, per_tensor, nb, D,
                                                                          sc, mode, scores);
