@@ -2094,8 +2094,9 @@ bsa_status launch_d(const ForwardArgs& a, int32_t* status, cudaStream_t stream) 
             ok = encode_image_map(&P.map_kg, a.k, kh, a.N, D, g, true, 0, 0) &&
                  encode_image_map(&P.map_vg, a.v, kh, a.N, D, g, true, 0, 0);
         if (!ok) return BSA_ERR_CUDA;
-        // no token masks in this mode: the row-split softmax with quadrant masks
-        if (items_geometry()) return launch_items<D, false, true, true, 2>(P, (int64_t)gx * gy, stream);
+        // no token masks in this mode: the row-split softmax with quadrant masks;
+        // rows of about 7 tiles keep the full six-slot ring and one Q buffer
+        if (items_geometry()) return launch_items<D, false, true, true, 1>(P, (int64_t)gx * gy, stream);
         return launch_dp<D, kDefaultPoly, false, false, false, true, true>(P, gx, gy, stream);
     }
     if (a.scatter_R > 0) {
