@@ -190,7 +190,7 @@ class Model:
 
 
 # (ring slots, Q buffers) of the kernel's instantiations: D = 128 and D = 64,
-# one Q buffer on the tile path, two on the geometry layers
+# one Q buffer on the tile path and the Gather 0 layer, two on the Scatter layer
 CONFIGS = [(6, 1), (5, 2), (12, 1), (11, 2)]
 
 
